@@ -1,0 +1,462 @@
+"""Benchmark of the FP8 scaled linear layer hot path on one GB300.
+
+Workload (the headline configuration): one FP8 linear, M = N = K = 4096,
+TE-style delayed scaling, X ~ N(0,1) and G ~ N(0,1e-3) drawn fresh for every
+step (20 seeded sets, 1.25 GiB together, rotated so the inputs of a step are
+never L2-resident), W ~ N(0,0.02) fixed, 16-step weight amax history, X and G
+scales lagged one call.  One step = the whole hot path:
+    state step (refresh every 16th) ->
+    quantise X (delayed, emits amax_x) ; quantise+transpose W (emits amax_w) ->
+    fprop GEMM -> record amax_w ; lag-update x scale ->
+    quantise+transpose G (emits amax_g) ; quantise X again, transposed, with the
+    updated x scale -> dgrad GEMM ; wgrad GEMM -> lag-update g scale.
+Metric: GEMM TFLOP/s of the whole step (3 x 2*4096^3 FLOP per step divided by
+the step time), plus per-kernel achieved TFLOP/s and GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (torchrun), every rank runs an independent replica on its own
+GPU (weak scaling; the path has no exchange on one GPU) and rank 0 reports
+the aggregate with the max time over ranks.  --impl reference times the CPU
+oracle (the slow, obviously correct restatement) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import shutil
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "FP8 linear fwd+bwd TFLOP/s & quantize GB/s vs GB300 FP8/HBM peak"
+CFG = synth.CONFIG2
+M, N, K = CFG["M"], CFG["N"], CFG["K"]
+N_SETS = CFG["steps"]
+GEMM_FLOP = 2.0 * M * N * K
+STEP_FLOP = 3 * GEMM_FLOP
+# algorithmic bytes of the quantisers per step (bf16 in, e4m3 out)
+QBYTES = {"quant_x_fwd": 3 * M * K, "quant_t_w": 4 * N * K, "quant_t_g": 4 * M * N,
+          "quant_t_x_bwd": 3 * M * K}
+FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate on Blackwell (4.5 : 2.25 PFLOP/s)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, src="fallback")
+
+
+def profile_traffic(name: str):
+    """Per-launch DRAM bytes recorded in the committed ncu summary, or None."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", open(p).read())
+    return float(m.group(1)) if m else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            self.proc = subprocess.Popen(
+                [exe, f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() in ("active", "1")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- GPU arm ---
+
+class Step:
+    """Device buffers and the C-ABI call sequence of one delayed-scaling step."""
+
+    def __init__(self, fp8, torch, dev, x_sets, g_sets, w):
+        self.fp8, self.torch, self.dev = fp8, torch, dev
+        u8 = dict(dtype=torch.uint8, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.x_sets, self.g_sets, self.w = x_sets, g_sets, w
+        self.xq = torch.empty((M, K), **u8)
+        self.xqt = torch.empty((K, M), **u8)
+        self.wq = torch.empty((N, K), **u8)
+        self.wqt = torch.empty((K, N), **u8)
+        self.gq = torch.empty((M, N), **u8)
+        self.gqt = torch.empty((N, M), **u8)
+        self.y = torch.empty((M, N), **bf)
+        self.dx = torch.empty((M, K), **bf)
+        self.dw = torch.empty((N, K), **bf)
+        self.amax = torch.zeros(4, **f32)
+        self.meta = fp8.Fp8Meta(16, device=dev)
+        self.count = [0]
+        self.launches = 0
+        self.events = None
+
+    def _ev(self, name):
+        if self.events is not None:
+            e = self.torch.cuda.Event(enable_timing=True)
+            e.record()
+            self.events.append((name, e))
+
+    def run(self, t, x=None, g=None):
+        fp8, m = self.fp8, self.meta
+        x = self.x_sets[t % len(self.x_sets)] if x is None else x
+        g = self.g_sets[t % len(self.g_sets)] if g is None else g
+        a_x, a_w, a_g = self.amax[0:1], self.amax[1:2], self.amax[2:3]
+        before = self.count[0]
+        fp8.fp8_state_step(self.count, 16, [m])
+        refreshed = self.count[0] % 16 == 0
+        self._ev("quant_x_fwd")
+        fp8.fp8_quantize(x, fp8.DELAYED, None, m.x_scale_inv, self.xq, a_x)
+        self._ev("quant_t_w")
+        fp8.fp8_quantize_transpose(self.w, fp8.DELAYED, None, m.scale_inv, self.wq, self.wqt,
+                                   amax_out=a_w)
+        self._ev("gemm_fprop")
+        fp8.fp8_linear_fprop(self.xq, m.x_scale, self.wq, m.scale, M, N, K, fp8.DELAYED, None,
+                             self.y)
+        self._ev("meta")
+        fp8.fp8_meta_record(m, fp8.SLOT_W, a_w)
+        fp8.fp8_meta_record(m, fp8.SLOT_X, a_x)
+        self._ev("quant_t_g")
+        fp8.fp8_quantize_transpose(g, fp8.DELAYED, None, m.g_scale_inv, self.gq, self.gqt,
+                                   amax_out=a_g)
+        self._ev("quant_t_x_bwd")
+        fp8.fp8_quantize_transpose(x, fp8.DELAYED, None, m.x_scale_inv, None, self.xqt)
+        self._ev("gemm_dgrad")
+        fp8.fp8_linear_dgrad(self.gq, m.g_scale, self.wqt, m.scale, M, N, K, fp8.DELAYED, self.dx)
+        self._ev("gemm_wgrad")
+        fp8.fp8_linear_wgrad(self.gqt, m.g_scale, self.xqt, m.x_scale, M, N, K, fp8.DELAYED,
+                             self.dw)
+        self._ev("meta")
+        fp8.fp8_meta_record(m, fp8.SLOT_G, a_g)
+        self._ev("end")
+        # kernels: 4 quantisers + 3 GEMMs + 3 meta updates (+1 refresh)
+        self.launches += 10 + (1 if refreshed else 0)
+        assert self.count[0] == before + 1
+
+
+def kernel_times(events):
+    """Average ms per launch of each named segment, from consecutive events."""
+    acc = {}
+    for (name, e0), (_, e1) in zip(events, events[1:]):
+        if name == "end":
+            continue
+        acc.setdefault(name, []).append(e0.elapsed_time(e1))
+    return {k: sum(v) / len(v) for k, v in acc.items()}
+
+
+def gpu_arm(args, rank, world):
+    import torch
+    import scaled_linear_layers_gb300 as fp8
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def to_dev(h):
+        return torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    seed = CFG["seed"] + rank
+    w = to_dev(synth.normal_bf16((N, K), CFG["w_sigma"], seed, "w"))
+    x_host = [synth.normal_bf16((M, K), CFG["x_sigma"], seed, "x", t) for t in range(N_SETS)]
+    g_host = [synth.normal_bf16((M, N), CFG["g_sigma"], seed, "g", t) for t in range(N_SETS)]
+    x_sets = [to_dev(h) for h in x_host]
+    g_sets = [to_dev(h) for h in g_host]
+    step = Step(fp8, torch, dev, x_sets, g_sets, w)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for t in range(args.warmup):
+        step.run(t)
+    fp8.fp8_check_device_status()
+    barrier()
+
+    # --- device-resident timed region
+    step.launches = 0
+    step.events = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start.record()
+        for t in range(args.warmup, args.warmup + args.steps):
+            step.run(t)
+        t_end.record()
+        barrier()
+    launches = step.launches
+    ms_total = t_start.elapsed_time(t_end)
+    segs = kernel_times(step.events)
+    step.events = None
+    fp8.fp8_check_device_status()
+
+    # --- end-to-end: pinned host inputs in, results out, every step
+    xp = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory() for h in x_host[:4]]
+    gp = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory() for h in g_host[:4]]
+    x_buf = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    g_buf = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    outs = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
+            torch.empty((M, K), dtype=torch.bfloat16).pin_memory(),
+            torch.empty((N, K), dtype=torch.bfloat16).pin_memory()]
+    h2d = x_buf.numel() * 2 + g_buf.numel() * 2
+    d2h = sum(o.numel() * 2 for o in outs)
+    e2e_steps = max(3, args.steps // 2)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(e2e_steps):
+        x_buf.copy_(xp[t % 4], non_blocking=True)
+        g_buf.copy_(gp[t % 4], non_blocking=True)
+        step.run(t, x_buf, g_buf)
+        outs[0].copy_(step.y, non_blocking=True)
+        outs[1].copy_(step.dx, non_blocking=True)
+        outs[2].copy_(step.dw, non_blocking=True)
+    e1.record()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+
+    ms_step = ms_total / args.steps
+    ms_e2e_step = ms_e2e / e2e_steps
+    if world > 1:
+        t = torch.tensor([ms_step, ms_e2e_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, ms_e2e_step = t.tolist()
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16"] * FP8_PER_BF16
+    gemm_ms = statistics.mean(segs[k] for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"))
+    gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
+    kernels = {}
+    for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"):
+        kernels[k] = {"us": round(segs[k] * 1e3, 2),
+                      "tflops": round(GEMM_FLOP / (segs[k] * 1e-3) / 1e12, 1)}
+    for k, b in QBYTES.items():
+        gbs = b / (segs[k] * 1e-3) / 1e9
+        kernels[k] = {"us": round(segs[k] * 1e3, 2), "gbs": round(gbs, 1),
+                      "frac_hbm": round(gbs / peaks["hbm"], 3),
+                      "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 3)}
+    value = STEP_FLOP * world / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 operands, fp32 accumulate, bf16 out",
+        "data": "synthetic (seeded normal inputs of the configuration's shapes)",
+        "config": {"workload": "one FP8 linear fwd+dgrad+wgrad, delayed scaling, M=N=K=4096, "
+                               "16-step amax history, fresh X/G per step",
+                   "M": M, "N": N, "K": K, "recipe": "delayed", "input_sets": N_SETS,
+                   "l2": "inputs rotate over 20 X/G sets (1.25 GiB) > 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp8_peak, 3),
+                     "traffic": profile_traffic("gemm_fp8_tensor_4096.md"),
+                     "kernel": "gemm_f8_tensor_kernel (mean of fprop/dgrad/wgrad launches)",
+                     "peak_source": f"{peaks['src']} bf16 burst {peaks['bf16']} TFLOP/s x 2 (fp8:bf16 nominal)"},
+        "kernels": kernels,
+        "e2e": {"value": round(STEP_FLOP * world / (ms_e2e_step * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e_step, 4)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+# ---------------------------------------------------------- oracle (CPU) ---
+
+PANEL = 16  # GEMM rows the oracle computes per GEMM; scaled to the full M
+
+
+def oracle_sample_step(step_idx: int, w_h, state_meta):
+    """One step of the oracle on a bounded sample: every quantiser over its
+    full tensor, and each GEMM on a PANEL-row panel.  Returns seconds spent
+    and the seconds extrapolated to the full step (GEMM time x M/PANEL)."""
+    import oracle
+    from oracle import state as ost
+    x = synth.normal_bf16((M, K), CFG["x_sigma"], CFG["seed"], "x", step_idx % N_SETS)
+    g = synth.normal_bf16((M, N), CFG["g_sigma"], CFG["seed"], "g", step_idx % N_SETS)
+    st, meta = state_meta
+    t0 = time.perf_counter()
+    st.step()
+    xq, amax_x = oracle.quantize(x, meta.x_scale_inv)
+    wq, amax_w = oracle.quantize(w_h, meta.scale_inv)
+    tq = time.perf_counter()
+    oracle.gemm(xq[:PANEL], wq, meta.x_scale, meta.scale)
+    tg = time.perf_counter() - tq
+    meta.record(amax_w)
+    meta.x_scale, meta.x_scale_inv = ost.lag_update(amax_x)
+    gq, amax_g = oracle.quantize(g, meta.g_scale_inv)
+    xq2, _ = oracle.quantize(x, meta.x_scale_inv)
+    wqt = oracle.transpose_u8(wq)
+    gqt = oracle.transpose_u8(gq)
+    xqt = oracle.transpose_u8(xq2)
+    t1 = time.perf_counter()
+    oracle.gemm(gq[:PANEL], wqt, meta.g_scale, meta.scale)
+    oracle.gemm(gqt[:PANEL], xqt, meta.g_scale, meta.x_scale)
+    tg += time.perf_counter() - t1
+    meta.g_scale, meta.g_scale_inv = ost.lag_update(amax_g)
+    spent = time.perf_counter() - t0
+    full = (spent - tg) + tg * (M / PANEL)
+    return spent, full
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    from oracle import state as ost
+    oracle.build()
+    w_h = synth.normal_bf16((N, K), CFG["w_sigma"], CFG["seed"], "w")
+    st = ost.State(16)
+    meta = st.new_meta()
+    for t in range(args.warmup):
+        oracle_sample_step(t, w_h, (st, meta))
+    spent_total, full_total = 0.0, 0.0
+    for t in range(args.warmup, args.warmup + args.steps):
+        s, f = oracle_sample_step(t, w_h, (st, meta))
+        spent_total += s
+        full_total += f
+    ms_step = full_total / args.steps * 1e3
+    value = STEP_FLOP / (ms_step * 1e-3) / 1e12
+    sample = (f"per step: the 4 quantisers over full 4096x4096 tensors, each GEMM on a "
+              f"{PANEL}-row panel, time extrapolated linearly to M=4096")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 GEMM on decoded e4m3, fp32 scales", "data": "synthetic",
+        "config": {"workload": "one FP8 linear fwd+dgrad+wgrad, delayed scaling, M=N=K=4096, "
+                               "16-step amax history, fresh X/G per step",
+                   "M": M, "N": N, "K": K, "recipe": "delayed"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "cpu_seconds": round(spent_total, 2)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline_for_gpu_line(steps: int = 2):
+    """The oracle timed on this host for the GPU line's cpu_baseline field
+    (rank 0, one GPU only): a bounded sample of 2 steps (~10-30 s)."""
+    import oracle
+    from oracle import state as ost
+    oracle.build()
+    w_h = synth.normal_bf16((N, K), CFG["w_sigma"], CFG["seed"], "w")
+    st = ost.State(16)
+    meta = st.new_meta()
+    spent_total, full_total = 0.0, 0.0
+    for t in range(steps):
+        s, f = oracle_sample_step(t, w_h, (st, meta))
+        spent_total += s
+        full_total += f
+    ms_step = full_total / steps * 1e3
+    return {"value": round(STEP_FLOP / (ms_step * 1e-3) / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{steps} steps; per step the 4 quantisers over full 4096x4096 tensors and "
+                      f"each GEMM on a {PANEL}-row panel, GEMM time extrapolated to M=4096",
+            "cpu_seconds": round(spent_total, 2), "ms_per_step_extrapolated": round(ms_step, 1)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+    else:
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            # before the first CUDA call, so no process state is shared with it
+            cpu = cpu_baseline_for_gpu_line()
+        line = gpu_arm(args, rank, world)
+        if line is not None:
+            line["cpu_baseline"] = cpu
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+/*
+ * fp8linear.h — C ABI of the GB300 (sm_103a) FP8 scaled linear layer.
+ *
+ * The layer computes, for X [M,K] (tokens x in-features), W [N,K]
+ * (out-features x in-features) and the upstream gradient G [M,N], all bf16
+ * row-major:
+ *     Y  = X  · Wᵀ   (fprop)   [M,N]
+ *     dX = G  · W    (dgrad)   [M,K]
+ *     dW = Gᵀ · X    (wgrad)   [N,K]
+ * with every operand quantised to E4M3 and every GEMM computed as
+ * D = s_A · s_B · (A · B) with fp32 accumulation and a bf16 result.  Sources:
+ * AstrAI "astrai/extension/fp8_state.py" (the comment above FP8TensorMeta:
+ * "D = A_SCALE * B_SCALE * A * B", per-tensor scales amax/448, quantisation
+ * multiplies by 1/scale; fp8_linear_forward / fp8_linear_backward), the
+ * SpecForge "Add training.fp8_linear" page (dynamic tensorwise scaling; token
+ * counts must be a multiple of 16) and the NeMo "Add FP8 support for
+ * SALMAutomodel" page (TE recipe=block, padding appended at the end).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are caller-owned DEVICE memory, 16-byte aligned.
+ *     bf16 tensors are passed as uint16_t bit patterns, e4m3 as uint8_t.
+ *   - Scales are fp32 DEVICE pointers: `scale` = amax/448 multiplies the GEMM
+ *     result (dequantisation), `scale_inv` = 448/amax multiplies the input
+ *     before the cast (quantisation).  The host never reads them, so nothing
+ *     synchronises.
+ *   - Work is enqueued on the caller's stream `s` (NULL = legacy default
+ *     stream).  No call synchronises except fp8_check_device_status.  No call
+ *     allocates device memory.  Calls are re-entrant; the only global state is
+ *     a thread-local error string and one device status word.
+ *   - Every call returns an fp8_status; FP8_OK means the work was enqueued.
+ *     Host-side validation happens before anything is enqueued, so a call that
+ *     fails validation has no effect.  fp8_last_error() describes the last
+ *     failure on the calling thread.
+ */
+#ifndef FP8LINEAR_H
+#define FP8LINEAR_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    FP8_ERR_SHAPE = 2,       /* a size is negative or the shapes disagree           */
+    FP8_ERR_ALIGNMENT = 3,   /* a dim is not a multiple of 16 (128 for block tiles),
+                                or a pointer is not 16-byte aligned.  Callers keep
+                                such a linear in bf16.                             */
+    FP8_ERR_UNSUPPORTED = 4, /* the current device is not sm_103 (GB300)            */
+    FP8_ERR_CUDA = 5,        /* a CUDA runtime call failed                          */
+    FP8_ERR_TIMEOUT = 6      /* a kernel's bounded wait ran out (see
+                                fp8_check_device_status); its outputs are invalid  */
+} fp8_status;
+
+typedef enum {
+    FP8_RECIPE_DELAYED = 0,  /* TE-style delayed scaling: scale_inv is an INPUT
+                                (from the previous call or the amax history); the
+                                quantiser emits this call's amax for the next one  */
+    FP8_RECIPE_DYNAMIC = 1,  /* current tensorwise scaling: amax of this tensor,
+                                then scale/scale_inv are OUTPUTS                    */
+    FP8_RECIPE_BLOCK = 2,    /* 1x128 tiles along the contraction dim (activations,
+                                gradients); fp32 scale per tile, OUTPUTS            */
+    FP8_RECIPE_BLOCK_2D = 3  /* 128x128 tiles (weights); fp32 scale per tile,
+                                OUTPUTS; one scale grid serves W and Wᵀ            */
+} fp8_recipe;
+
+/* ------------------------------------------------------------------------ */
+/* Quantisation                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* amax_out = max |x| over n bf16 elements, as fp32 (a NaN input makes it NaN).
+ * amax_out is overwritten (the call zeroes it first).  Any n >= 0.
+ * Source: AstrAI fp8_state.py module docstring (amax of each quantised tensor);
+ * SpecForge page (dynamic tensorwise scaling takes the current amax). */
+fp8_status fp8_amax(const uint16_t *x, int64_t n, float *amax_out, cudaStream_t s);
+
+/* q = e4m3(fl32(x * scale_inv)), round-to-nearest-even, saturating to ±448,
+ * for x [rows, cols] row-major; q [rows, cols] row-major.
+ *   DELAYED: scale_inv [1] is read; scale is unused (may be NULL); amax_out
+ *            (nullable) receives amax(x) — the quantiser's own amax, which the
+ *            caller turns into the next call's scale (fp8_meta_record).
+ *   DYNAMIC: amax_out [1] is REQUIRED and receives amax(x); scale [1] and
+ *            scale_inv [1] receive max(amax,1e-12)/448 and 448/max(amax,1e-12).
+ *   BLOCK:   cols % 128 == 0; scale and scale_inv [rows, cols/128] receive the
+ *            per-1x128-tile scales; amax_out (nullable) receives amax(x).
+ *   BLOCK_2D: rows % 128 == 0 and cols % 128 == 0; scale and scale_inv
+ *            [rows/128, cols/128]; amax_out nullable.
+ * Any rows, cols >= 0 for DELAYED/DYNAMIC (n = rows*cols need not be a
+ * multiple of anything).  Source: AstrAI fp8_state.py, fp8_linear_forward
+ * ("the quantize kernel emits the current amax"), _update_delayed_scale. */
+fp8_status fp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, fp8_recipe r,
+                        float *scale, float *scale_inv, uint8_t *q, float *amax_out,
+                        cudaStream_t s);
+
+/* One read of x [rows, cols] producing q [rows, cols] (nullable) and its
+ * transpose qt [cols, rows], both e4m3 with the same rounding as fp8_quantize.
+ * qt gives wgrad and dgrad their operands with the contraction dim contiguous.
+ * rows % 16 == 0 and cols % 16 == 0 (BLOCK/BLOCK_2D: % 128).
+ *   DELAYED / DYNAMIC: scale, scale_inv, amax_out as for fp8_quantize;
+ *            scale_t / scale_inv_t unused (may be NULL).
+ *   BLOCK:   q uses 1x128 row tiles (scale/scale_inv [rows, cols/128]); qt uses
+ *            128x1 column tiles, i.e. 1x128 tiles of its own rows
+ *            (scale_t/scale_inv_t [cols, rows/128]).  q and its scales may be NULL
+ *            together when only qt is wanted (wgrad operands).
+ *   BLOCK_2D: 128x128 tiles; scale/scale_inv [rows/128, cols/128] serve both q
+ *            and qt; scale_t/scale_inv_t unused.
+ * Source: AstrAI fp8_state.py fp8_linear_backward (x and w quantised again for
+ * the backward GEMMs); NeMo SALMAutomodel page (TE recipe=block). */
+fp8_status fp8_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, fp8_recipe r,
+                                  float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
+                                  float *scale_t, float *scale_inv_t, float *amax_out,
+                                  cudaStream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* Scaled FP8 GEMMs (tcgen05, fp32 accumulation in tensor memory, bf16 out)  */
+/* ------------------------------------------------------------------------ */
+/* M, N, K > 0 and each a multiple of 16 (SpecForge page: float8 GEMMs need the
+ * token count to be a multiple of 16; the same holds for the feature dims).
+ * BLOCK recipe: M, N, K multiples of 128.  Results overwrite the output.
+ * Tensorwise recipes (DELAYED, DYNAMIC): x_scale, w_scale, g_scale are [1].
+ * BLOCK recipe: activation/gradient scales are per 1x128 tile of the operand
+ * as passed (row-major [rows, contraction/128]) and w_scale is the 128x128
+ * grid [N/128, K/128] of W.
+ * Source: AstrAI fp8_state.py comment "D = A_SCALE * B_SCALE * A * B" and
+ * fp8_linear_forward / fp8_linear_backward. */
+
+/* y [M,N] = bf16( x_scale·w_scale · xq[M,K] · wq[N,K]ᵀ + bias[N] ).
+ * bias (bf16 [N]) is nullable; it is added in fp32 before the bf16 rounding.
+ * BLOCK: x_scale [M, K/128]; bias is not supported (must be NULL). */
+fp8_status fp8_linear_fprop(const uint8_t *xq, const float *x_scale,
+                            const uint8_t *wq, const float *w_scale,
+                            int64_t M, int64_t N, int64_t K, fp8_recipe r,
+                            const uint16_t *bias, uint16_t *y, cudaStream_t s);
+
+/* dx [M,K] = bf16( g_scale·w_scale · gq[M,N] · wqt[K,N]ᵀ ), wqt = Wqᵀ.
+ * BLOCK: g_scale [M, N/128]; w_scale is W's [N/128, K/128] grid. */
+fp8_status fp8_linear_dgrad(const uint8_t *gq, const float *g_scale,
+                            const uint8_t *wqt, const float *w_scale,
+                            int64_t M, int64_t N, int64_t K, fp8_recipe r,
+                            uint16_t *dx, cudaStream_t s);
+
+/* dw [N,K] = bf16( g_scale·x_scale · gqt[N,M] · xqt[K,M]ᵀ ), gqt = Gqᵀ,
+ * xqt = Xqᵀ.  The result overwrites dw (no accumulation into a main grad).
+ * BLOCK: g_scale [N, M/128] and x_scale [K, M/128] are the column-tile scales
+ * that fp8_quantize_transpose writes to scale_t. */
+fp8_status fp8_linear_wgrad(const uint8_t *gqt, const float *g_scale,
+                            const uint8_t *xqt, const float *x_scale,
+                            int64_t M, int64_t N, int64_t K, fp8_recipe r,
+                            uint16_t *dw, cudaStream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* Delayed-scaling state (one per weight)                                    */
+/* ------------------------------------------------------------------------ */
+/* Device block layout (fp32), FP8_META_FLOATS(interval) floats, 16-B aligned:
+ *   [0] scale   [1] scale_inv      weight, from the amax-history window
+ *   [2] x_scale [3] x_scale_inv    activation, lagged one call
+ *   [4] g_scale [5] g_scale_inv    gradient, lagged one call
+ *   [6..7] reserved
+ *   [8 .. 8+interval) amax_history ring
+ * Source: AstrAI fp8_state.py FP8TensorMeta (all fields start at 1). */
+enum { FP8_META_SCALE = 0, FP8_META_SCALE_INV = 1, FP8_META_X_SCALE = 2,
+       FP8_META_X_SCALE_INV = 3, FP8_META_G_SCALE = 4, FP8_META_G_SCALE_INV = 5,
+       FP8_META_HISTORY = 8 };
+#define FP8_META_FLOATS(interval) (8 + (interval))
+
+typedef struct {
+    float *dev;      /* caller-owned device block, FP8_META_FLOATS(interval) floats */
+    int32_t interval;/* history length = refresh period (16 by default)            */
+    int32_t idx;     /* next history slot (host side, like FP8TensorMeta.idx)       */
+} fp8_meta;
+
+typedef enum { FP8_SLOT_W = 0, FP8_SLOT_X = 1, FP8_SLOT_G = 2 } fp8_slot;
+
+/* Sets every scale and every history slot to 1 and idx to 0.
+ * 1 <= interval <= 1024. */
+fp8_status fp8_meta_init(fp8_meta *m, float *dev_block, int32_t interval, cudaStream_t s);
+
+/* W: history[idx] = *amax_dev and idx = (idx+1) % interval (FP8TensorMeta.record).
+ * X, G: a = max(*amax_dev, 1e-12); x_scale (g_scale) = a/448 and
+ *       x_scale_inv (g_scale_inv) = 448/a, for the next call
+ *       (_update_delayed_scale).  Device-side; no synchronisation. */
+fp8_status fp8_meta_record(fp8_meta *m, fp8_slot which, const float *amax_dev, cudaStream_t s);
+
+/* m = max(history); if m > 0: scale = m/448, scale_inv = 448/m; else unchanged
+ * (FP8TensorMeta.refresh). */
+fp8_status fp8_meta_refresh(fp8_meta *m, cudaStream_t s);
+
+/* FP8State.step: *step_count += 1 and, when it becomes a multiple of
+ * interval, refresh every meta in metas[0..n).  Call once per training step
+ * (at autocast entry), never again for the backward of the same step. */
+fp8_status fp8_state_step(int64_t *step_count, int32_t interval, fp8_meta *metas, int32_t n,
+                          cudaStream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* Token padding                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Rows rounded up to a multiple: ((rows + multiple - 1) / multiple) * multiple.
+ * Host only; returns -1 for rows < 0 or multiple < 1. */
+int64_t fp8_padded_rows(int64_t rows, int64_t multiple);
+
+/* out [padded_rows, cols] = x [rows, cols] followed by zero rows, padded_rows =
+ * fp8_padded_rows(rows, multiple) (written to *padded_rows, host pointer,
+ * nullable).  x and out must not overlap.  Zero rows change no amax and no
+ * real output row.  Source: SpecForge page (multiple of 16), NeMo SALMAutomodel
+ * review (pad tokens appended at the end). */
+fp8_status fp8_pad_tokens(const uint16_t *x, int64_t rows, int64_t cols, int64_t multiple,
+                          uint16_t *out, int64_t *padded_rows, cudaStream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises `s`, then reads and clears the device status word that kernels
+ * set when a bounded wait runs out.  Returns FP8_ERR_TIMEOUT if it was set,
+ * FP8_ERR_CUDA on a CUDA error, else FP8_OK. */
+fp8_status fp8_check_device_status(cudaStream_t s);
+
+/* Diagnostic: launches one block that waits on a barrier nothing will ever
+ * complete, with a wait limit of timeout_us microseconds (1..1000000); the
+ * wait gives up, sets the device status word and the kernel returns.  Used to
+ * test the timeout path without faulting or hanging the GPU. */
+fp8_status fp8_selftest_wait_timeout(uint32_t timeout_us, cudaStream_t s);
+
+/* Text of the last failure on this thread ("" if none). */
+const char *fp8_last_error(void);
+
+/* Library version, e.g. "fp8linear 0.1 sm_103a". */
+const char *fp8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8LINEAR_H */

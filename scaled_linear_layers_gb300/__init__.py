@@ -1,0 +1,191 @@
+"""GB300-native FP8 scaled linear layer: thin Python binding of libfp8linear.so.
+
+Every function has the name of the C entry point it calls (see
+include/fp8linear.h) and only marshals arguments: torch tensors in, their
+device pointers, sizes and the current CUDA stream out to C.  All arithmetic
+runs in the library's sm_103a kernels; torch provides device memory and
+streams.  Importing this package requires the built library (no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (BLOCK, BLOCK_2D, DELAYED, DYNAMIC, SLOT_G, SLOT_W, SLOT_X, Fp8Error,
+                   META_G_SCALE, META_G_SCALE_INV, META_HISTORY, META_SCALE, META_SCALE_INV,
+                   META_X_SCALE, META_X_SCALE_INV)
+
+_LIB = _lib.load()
+
+__all__ = [
+    "fp8_amax", "fp8_quantize", "fp8_quantize_transpose", "fp8_linear_fprop",
+    "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_meta_init", "fp8_meta_record",
+    "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
+    "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
+    "Fp8Error", "DELAYED", "DYNAMIC", "BLOCK", "BLOCK_2D", "SLOT_W", "SLOT_X", "SLOT_G",
+    "library_path",
+]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a torch.Tensor or None, got {type(t)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int):
+    if status != 0:
+        raise Fp8Error(status, _LIB.fp8_last_error().decode())
+
+
+def _bf16(t):
+    assert t.dtype == torch.bfloat16 and t.is_contiguous(), "bf16 contiguous tensor expected"
+    return t
+
+
+def _u8(t):
+    if t is None:
+        return None
+    assert t.dtype in (torch.uint8, torch.float8_e4m3fn) and t.is_contiguous()
+    return t
+
+
+def fp8_version() -> str:
+    return _LIB.fp8_version().decode()
+
+
+def fp8_amax(x, amax_out, stream=None):
+    _check(_LIB.fp8_amax(_ptr(_bf16(x)), x.numel(), _ptr(amax_out), _stream(stream)))
+
+
+def fp8_quantize(x, recipe, scale, scale_inv, q, amax_out=None, stream=None):
+    x2 = _bf16(x).reshape(-1, x.shape[-1]) if x.dim() != 1 else x.reshape(1, -1)
+    _check(_LIB.fp8_quantize(_ptr(x2), x2.shape[0], x2.shape[1], recipe, _ptr(scale),
+                             _ptr(scale_inv), _ptr(_u8(q)), _ptr(amax_out), _stream(stream)))
+
+
+def fp8_quantize_transpose(x, recipe, scale, scale_inv, q, qt, scale_t=None, scale_inv_t=None,
+                           amax_out=None, stream=None):
+    _bf16(x)
+    assert x.dim() == 2
+    _check(_LIB.fp8_quantize_transpose(_ptr(x), x.shape[0], x.shape[1], recipe, _ptr(scale),
+                                       _ptr(scale_inv), _ptr(_u8(q)), _ptr(_u8(qt)), _ptr(scale_t),
+                                       _ptr(scale_inv_t), _ptr(amax_out), _stream(stream)))
+
+
+def fp8_linear_fprop(xq, x_scale, wq, w_scale, M, N, K, recipe, bias, y, stream=None):
+    _check(_LIB.fp8_linear_fprop(_ptr(_u8(xq)), _ptr(x_scale), _ptr(_u8(wq)), _ptr(w_scale), M, N,
+                                 K, recipe, _ptr(bias), _ptr(y), _stream(stream)))
+
+
+def fp8_linear_dgrad(gq, g_scale, wqt, w_scale, M, N, K, recipe, dx, stream=None):
+    _check(_LIB.fp8_linear_dgrad(_ptr(_u8(gq)), _ptr(g_scale), _ptr(_u8(wqt)), _ptr(w_scale), M,
+                                 N, K, recipe, _ptr(dx), _stream(stream)))
+
+
+def fp8_linear_wgrad(gqt, g_scale, xqt, x_scale, M, N, K, recipe, dw, stream=None):
+    _check(_LIB.fp8_linear_wgrad(_ptr(_u8(gqt)), _ptr(g_scale), _ptr(_u8(xqt)), _ptr(x_scale), M,
+                                 N, K, recipe, _ptr(dw), _stream(stream)))
+
+
+class Fp8Meta:
+    """One weight's delayed-scaling state: the C fp8_meta struct plus the
+    device block it points to (a torch float32 tensor this object owns)."""
+
+    def __init__(self, interval: int = 16, device="cuda", stream=None):
+        self.block = torch.empty(8 + interval, dtype=torch.float32, device=device)
+        self.c = _lib.fp8_meta()
+        _check(_LIB.fp8_meta_init(ctypes.byref(self.c), _ptr(self.block), interval,
+                                  _stream(stream)))
+
+    def view(self, index: int):
+        return self.block[index:index + 1]
+
+    @property
+    def scale(self):
+        return self.view(META_SCALE)
+
+    @property
+    def scale_inv(self):
+        return self.view(META_SCALE_INV)
+
+    @property
+    def x_scale(self):
+        return self.view(META_X_SCALE)
+
+    @property
+    def x_scale_inv(self):
+        return self.view(META_X_SCALE_INV)
+
+    @property
+    def g_scale(self):
+        return self.view(META_G_SCALE)
+
+    @property
+    def g_scale_inv(self):
+        return self.view(META_G_SCALE_INV)
+
+    @property
+    def history(self):
+        return self.block[META_HISTORY:]
+
+    @property
+    def idx(self) -> int:
+        return self.c.idx
+
+
+def fp8_meta_init(meta: Fp8Meta, interval: int = 16, stream=None):
+    _check(_LIB.fp8_meta_init(ctypes.byref(meta.c), _ptr(meta.block), interval, _stream(stream)))
+
+
+def fp8_meta_record(meta: Fp8Meta, which: int, amax_dev, stream=None):
+    _check(_LIB.fp8_meta_record(ctypes.byref(meta.c), which, _ptr(amax_dev), _stream(stream)))
+
+
+def fp8_meta_refresh(meta: Fp8Meta, stream=None):
+    _check(_LIB.fp8_meta_refresh(ctypes.byref(meta.c), _stream(stream)))
+
+
+def fp8_state_step(step_count: list, interval: int, metas, stream=None):
+    """step_count is a one-element list holding the host counter (updated in place)."""
+    arr = (_lib.fp8_meta * max(1, len(metas)))()
+    for i, m in enumerate(metas):
+        arr[i] = m.c
+    cnt = ctypes.c_int64(step_count[0])
+    _check(_LIB.fp8_state_step(ctypes.byref(cnt), interval, arr, len(metas), _stream(stream)))
+    step_count[0] = cnt.value
+    for i, m in enumerate(metas):
+        m.c = arr[i]
+
+
+def fp8_padded_rows(rows: int, multiple: int = 16) -> int:
+    return int(_LIB.fp8_padded_rows(rows, multiple))
+
+
+def fp8_pad_tokens(x, multiple, out, stream=None) -> int:
+    _bf16(x)
+    padded = ctypes.c_int64(0)
+    _check(_LIB.fp8_pad_tokens(_ptr(x), x.shape[0], x.shape[1], multiple, _ptr(out),
+                               ctypes.byref(padded), _stream(stream)))
+    return padded.value
+
+
+def fp8_check_device_status(stream=None):
+    _check(_LIB.fp8_check_device_status(_stream(stream)))
+
+
+def fp8_selftest_wait_timeout(timeout_us: int, stream=None):
+    _check(_LIB.fp8_selftest_wait_timeout(timeout_us, _stream(stream)))

@@ -1,0 +1,403 @@
+// C-ABI entry points: host-side validation, then launches on the caller's
+// stream.  Nothing here allocates device memory or synchronises (except
+// fp8_check_device_status).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8 {
+
+extern uint64_t g_wait_limit_ns;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+fp8_status fail(fp8_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fp8_status cuda_status(cudaError_t e, const char *where, const char *why = nullptr) {
+    if (e == cudaSuccess) return FP8_OK;
+    return fail(FP8_ERR_CUDA, "%s: %s%s%s", where, cudaGetErrorString(e), why ? " — " : "",
+                why ? why : "");
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+
+fp8_status check_device(const char *who) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, who);
+    if (dev < 0 || dev >= kMaxDevices) return fail(FP8_ERR_UNSUPPORTED, "%s: device %d", who, dev);
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = sms > 0 ? sms : 1;
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        if (g_arch_ok[dev] < 0)
+            snprintf(g_err, sizeof g_err, "device %d is sm_%d%d", dev, major, minor);
+    }
+    if (g_arch_ok[dev] < 0)
+        return fail(FP8_ERR_UNSUPPORTED, "%s: this library runs on sm_103 (GB300) only", who);
+    return FP8_OK;
+}
+
+fp8_status check_dim16(const char *who, const char *name, int64_t v, int64_t mult) {
+    if (v % mult != 0)
+        return fail(FP8_ERR_ALIGNMENT, "%s: Expected %s to be divisible by %lld, but got %s=%lld",
+                    who, name, (long long)mult, name, (long long)v);
+    return FP8_OK;
+}
+
+#define FP8_TRY(expr)                   \
+    do {                                \
+        fp8_status _st = (expr);        \
+        if (_st != FP8_OK) return _st;  \
+    } while (0)
+
+#define FP8_NEED(ptr, who)                                                       \
+    do {                                                                         \
+        if ((ptr) == nullptr) return fail(FP8_ERR_NULL, "%s: %s is NULL", who, #ptr); \
+    } while (0)
+
+#define FP8_ALIGN(ptr, who)                                                                   \
+    do {                                                                                      \
+        if ((ptr) != nullptr && !aligned16(ptr))                                              \
+            return fail(FP8_ERR_ALIGNMENT, "%s: %s is not 16-byte aligned", who, #ptr);       \
+    } while (0)
+
+}  // namespace
+
+int num_sms() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+}  // namespace fp8
+
+using namespace fp8;
+
+extern "C" {
+
+const char *fp8_last_error(void) { return g_err; }
+
+const char *fp8_version(void) { return "fp8linear 0.1 sm_103a"; }
+
+fp8_status fp8_amax(const uint16_t *x, int64_t n, float *amax_out, cudaStream_t s) {
+    const char *who = "fp8_amax";
+    if (n < 0) return fail(FP8_ERR_SHAPE, "%s: n=%lld < 0", who, (long long)n);
+    FP8_NEED(amax_out, who);
+    if (n > 0) FP8_NEED(x, who);
+    FP8_ALIGN(x, who);
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_amax(x, n, amax_out, s), who);
+}
+
+fp8_status fp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, fp8_recipe r, float *scale,
+                        float *scale_inv, uint8_t *q, float *amax_out, cudaStream_t s) {
+    const char *who = "fp8_quantize";
+    if (rows < 0 || cols < 0)
+        return fail(FP8_ERR_SHAPE, "%s: negative shape [%lld, %lld]", who, (long long)rows,
+                    (long long)cols);
+    const int64_t n = rows * cols;
+    if (n > 0) {
+        FP8_NEED(x, who);
+        FP8_NEED(q, who);
+    }
+    FP8_ALIGN(x, who);
+    FP8_ALIGN(q, who);
+    switch (r) {
+    case FP8_RECIPE_DELAYED:
+        FP8_NEED(scale_inv, who);
+        FP8_TRY(check_device(who));
+        return cuda_status(launch_quantize_tensor(x, n, false, scale, scale_inv, q, amax_out, s), who);
+    case FP8_RECIPE_DYNAMIC:
+        FP8_NEED(scale, who);
+        FP8_NEED(scale_inv, who);
+        FP8_NEED(amax_out, who);
+        FP8_TRY(check_device(who));
+        return cuda_status(launch_quantize_tensor(x, n, true, scale, scale_inv, q, amax_out, s), who);
+    case FP8_RECIPE_BLOCK:
+        FP8_TRY(check_dim16(who, "cols", cols, 128));
+        FP8_NEED(scale, who);
+        FP8_NEED(scale_inv, who);
+        FP8_TRY(check_device(who));
+        return cuda_status(launch_quantize_rowtiles(x, rows, cols, scale, scale_inv, q, amax_out, s),
+                           who);
+    case FP8_RECIPE_BLOCK_2D:
+        FP8_TRY(check_dim16(who, "rows", rows, 128));
+        FP8_TRY(check_dim16(who, "cols", cols, 128));
+        FP8_NEED(scale, who);
+        FP8_NEED(scale_inv, who);
+        if (rows > 0x7FFFFFFF || cols > 0x7FFFFFFF)
+            return fail(FP8_ERR_SHAPE, "%s: dims must fit in 31 bits", who);
+        FP8_TRY(check_device(who));
+        // the cast+transpose kernel without its transposed output
+        return cuda_status(launch_quantize_transpose(x, rows, cols, 2, scale, scale_inv, q, nullptr,
+                                                     nullptr, nullptr, amax_out, s),
+                           who);
+    }
+    return fail(FP8_ERR_SHAPE, "%s: unknown recipe %d", who, (int)r);
+}
+
+fp8_status fp8_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, fp8_recipe r,
+                                  float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
+                                  float *scale_t, float *scale_inv_t, float *amax_out,
+                                  cudaStream_t s) {
+    const char *who = "fp8_quantize_transpose";
+    if (rows < 0 || cols < 0)
+        return fail(FP8_ERR_SHAPE, "%s: negative shape [%lld, %lld]", who, (long long)rows,
+                    (long long)cols);
+    if (rows > 0x7FFFFFFF || cols > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: dims must fit in 31 bits", who);
+    const int64_t mult = (r == FP8_RECIPE_BLOCK || r == FP8_RECIPE_BLOCK_2D) ? 128 : 16;
+    FP8_TRY(check_dim16(who, "rows", rows, mult));
+    FP8_TRY(check_dim16(who, "cols", cols, mult));
+    if (rows * cols > 0) {
+        FP8_NEED(x, who);
+        FP8_NEED(qt, who);
+    }
+    FP8_ALIGN(x, who);
+    FP8_ALIGN(q, who);
+    FP8_ALIGN(qt, who);
+    int mode;
+    switch (r) {
+    case FP8_RECIPE_DELAYED:
+        FP8_NEED(scale_inv, who);
+        mode = 0;
+        break;
+    case FP8_RECIPE_DYNAMIC:
+        FP8_NEED(scale, who);
+        FP8_NEED(scale_inv, who);
+        FP8_NEED(amax_out, who);
+        mode = 1;
+        break;
+    case FP8_RECIPE_BLOCK_2D:
+        FP8_NEED(scale, who);
+        FP8_NEED(scale_inv, who);
+        mode = 2;
+        break;
+    case FP8_RECIPE_BLOCK:
+        FP8_NEED(scale_t, who);
+        FP8_NEED(scale_inv_t, who);
+        if (q != nullptr) {
+            FP8_NEED(scale, who);
+            FP8_NEED(scale_inv, who);
+        }
+        mode = 3;
+        break;
+    default:
+        return fail(FP8_ERR_SHAPE, "%s: unknown recipe %d", who, (int)r);
+    }
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_quantize_transpose(x, rows, cols, mode, scale, scale_inv, q, qt,
+                                                 scale_t, scale_inv_t, amax_out, s),
+                       who);
+}
+
+static fp8_status gemm_common(const char *who, const uint8_t *A, const float *sa, const uint8_t *B,
+                              const float *sb, int64_t M, int64_t N, int64_t K, fp8_recipe r,
+                              uint16_t *D, const char *mname, const char *nname, const char *kname) {
+    if (M <= 0 || N <= 0 || K <= 0)
+        return fail(FP8_ERR_SHAPE, "%s: empty or negative GEMM [%s=%lld, %s=%lld, %s=%lld]", who,
+                    mname, (long long)M, nname, (long long)N, kname, (long long)K);
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: dims must fit in 31 bits", who);
+    const int64_t mult = r == FP8_RECIPE_BLOCK ? 128 : 16;
+    FP8_TRY(check_dim16(who, mname, M, mult));
+    FP8_TRY(check_dim16(who, nname, N, mult));
+    FP8_TRY(check_dim16(who, kname, K, mult));
+    FP8_NEED(A, who);
+    FP8_NEED(B, who);
+    FP8_NEED(sa, who);
+    FP8_NEED(sb, who);
+    FP8_NEED(D, who);
+    FP8_ALIGN(A, who);
+    FP8_ALIGN(B, who);
+    FP8_ALIGN(D, who);
+    if (r != FP8_RECIPE_DELAYED && r != FP8_RECIPE_DYNAMIC && r != FP8_RECIPE_BLOCK)
+        return fail(FP8_ERR_SHAPE, "%s: recipe %d is not a GEMM recipe", who, (int)r);
+    return check_device(who);
+}
+
+fp8_status fp8_linear_fprop(const uint8_t *xq, const float *x_scale, const uint8_t *wq,
+                            const float *w_scale, int64_t M, int64_t N, int64_t K, fp8_recipe r,
+                            const uint16_t *bias, uint16_t *y, cudaStream_t s) {
+    const char *who = "fp8_linear_fprop";
+    FP8_TRY(gemm_common(who, xq, x_scale, wq, w_scale, M, N, K, r, y, "M", "N", "K"));
+    const char *why = nullptr;
+    if (r == FP8_RECIPE_BLOCK) {
+        if (bias != nullptr) return fail(FP8_ERR_UNSUPPORTED, "%s: bias with the block recipe", who);
+        // A = Xq [M,K], scales [M, K/128]; B = Wq [N,K], 128x128 grid [N/128, K/128]
+        return cuda_status(launch_gemm_block(xq, wq, M, N, K, x_scale, K / 128, w_scale, K / 128, 1,
+                                             128, y, s, &why),
+                           who, why);
+    }
+    FP8_ALIGN(bias, who);
+    return cuda_status(launch_gemm_tensor(xq, wq, M, N, K, x_scale, w_scale, bias, y, s, &why), who,
+                       why);
+}
+
+fp8_status fp8_linear_dgrad(const uint8_t *gq, const float *g_scale, const uint8_t *wqt,
+                            const float *w_scale, int64_t M, int64_t N, int64_t K, fp8_recipe r,
+                            uint16_t *dx, cudaStream_t s) {
+    const char *who = "fp8_linear_dgrad";
+    // dX [M,K]: GEMM rows M, cols K, contraction N
+    FP8_TRY(gemm_common(who, gq, g_scale, wqt, w_scale, M, N, K, r, dx, "M", "N", "K"));
+    const char *why = nullptr;
+    if (r == FP8_RECIPE_BLOCK) {
+        // A = Gq [M,N], scales [M, N/128]; B = Wqᵀ [K,N]: the scale of B row k,
+        // contraction block nb is W's grid entry [nb, k/128].
+        return cuda_status(launch_gemm_block(gq, wqt, M, K, N, g_scale, N / 128, w_scale, 1,
+                                             K / 128, 128, dx, s, &why),
+                           who, why);
+    }
+    return cuda_status(launch_gemm_tensor(gq, wqt, M, K, N, g_scale, w_scale, nullptr, dx, s, &why),
+                       who, why);
+}
+
+fp8_status fp8_linear_wgrad(const uint8_t *gqt, const float *g_scale, const uint8_t *xqt,
+                            const float *x_scale, int64_t M, int64_t N, int64_t K, fp8_recipe r,
+                            uint16_t *dw, cudaStream_t s) {
+    const char *who = "fp8_linear_wgrad";
+    // dW [N,K]: GEMM rows N, cols K, contraction M
+    FP8_TRY(gemm_common(who, gqt, g_scale, xqt, x_scale, M, N, K, r, dw, "M", "N", "K"));
+    const char *why = nullptr;
+    if (r == FP8_RECIPE_BLOCK) {
+        // A = Gqᵀ [N,M], scales [N, M/128]; B = Xqᵀ [K,M], scales [K, M/128]
+        return cuda_status(launch_gemm_block(gqt, xqt, N, K, M, g_scale, M / 128, x_scale, M / 128,
+                                             1, 1, dw, s, &why),
+                           who, why);
+    }
+    return cuda_status(launch_gemm_tensor(gqt, xqt, N, K, M, g_scale, x_scale, nullptr, dw, s, &why),
+                       who, why);
+}
+
+fp8_status fp8_meta_init(fp8_meta *m, float *dev_block, int32_t interval, cudaStream_t s) {
+    const char *who = "fp8_meta_init";
+    FP8_NEED(m, who);
+    FP8_NEED(dev_block, who);
+    FP8_ALIGN(dev_block, who);
+    if (interval < 1 || interval > 1024)
+        return fail(FP8_ERR_SHAPE, "%s: interval=%d outside 1..1024", who, interval);
+    FP8_TRY(check_device(who));
+    m->dev = dev_block;
+    m->interval = interval;
+    m->idx = 0;
+    return cuda_status(launch_meta_init(dev_block, interval, s), who);
+}
+
+fp8_status fp8_meta_record(fp8_meta *m, fp8_slot which, const float *amax_dev, cudaStream_t s) {
+    const char *who = "fp8_meta_record";
+    FP8_NEED(m, who);
+    FP8_NEED(m->dev, who);
+    FP8_NEED(amax_dev, who);
+    if (m->interval < 1 || m->idx < 0 || m->idx >= m->interval)
+        return fail(FP8_ERR_SHAPE, "%s: corrupt meta (interval=%d idx=%d)", who, m->interval, m->idx);
+    FP8_TRY(check_device(who));
+    switch (which) {
+    case FP8_SLOT_W: {
+        fp8_status st = cuda_status(launch_meta_copy(m->dev + FP8_META_HISTORY + m->idx, amax_dev, s), who);
+        if (st == FP8_OK) m->idx = (m->idx + 1) % m->interval;
+        return st;
+    }
+    case FP8_SLOT_X:
+        return cuda_status(launch_meta_lag(m->dev + FP8_META_X_SCALE, m->dev + FP8_META_X_SCALE_INV,
+                                           amax_dev, s),
+                           who);
+    case FP8_SLOT_G:
+        return cuda_status(launch_meta_lag(m->dev + FP8_META_G_SCALE, m->dev + FP8_META_G_SCALE_INV,
+                                           amax_dev, s),
+                           who);
+    }
+    return fail(FP8_ERR_SHAPE, "%s: unknown slot %d", who, (int)which);
+}
+
+fp8_status fp8_meta_refresh(fp8_meta *m, cudaStream_t s) {
+    const char *who = "fp8_meta_refresh";
+    FP8_NEED(m, who);
+    FP8_NEED(m->dev, who);
+    if (m->interval < 1) return fail(FP8_ERR_SHAPE, "%s: corrupt meta", who);
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_meta_refresh(m->dev, m->interval, s), who);
+}
+
+fp8_status fp8_state_step(int64_t *step_count, int32_t interval, fp8_meta *metas, int32_t n,
+                          cudaStream_t s) {
+    const char *who = "fp8_state_step";
+    FP8_NEED(step_count, who);
+    if (interval < 1) return fail(FP8_ERR_SHAPE, "%s: interval=%d", who, interval);
+    if (n < 0 || (n > 0 && metas == nullptr)) return fail(FP8_ERR_NULL, "%s: metas", who);
+    *step_count += 1;
+    if (*step_count % interval != 0) return FP8_OK;
+    for (int32_t i = 0; i < n; ++i) FP8_TRY(fp8_meta_refresh(&metas[i], s));
+    return FP8_OK;
+}
+
+int64_t fp8_padded_rows(int64_t rows, int64_t multiple) {
+    if (rows < 0 || multiple < 1) return -1;
+    return (rows + multiple - 1) / multiple * multiple;
+}
+
+fp8_status fp8_pad_tokens(const uint16_t *x, int64_t rows, int64_t cols, int64_t multiple,
+                          uint16_t *out, int64_t *padded_rows, cudaStream_t s) {
+    const char *who = "fp8_pad_tokens";
+    if (rows < 0 || cols < 0 || multiple < 1)
+        return fail(FP8_ERR_SHAPE, "%s: rows=%lld cols=%lld multiple=%lld", who, (long long)rows,
+                    (long long)cols, (long long)multiple);
+    const int64_t padded = fp8_padded_rows(rows, multiple);
+    if (padded_rows != nullptr) *padded_rows = padded;
+    if (padded * cols > 0) FP8_NEED(out, who);
+    if (rows * cols > 0) FP8_NEED(x, who);
+    FP8_ALIGN(x, who);
+    FP8_ALIGN(out, who);
+    if (x != nullptr && out != nullptr && rows * cols > 0) {
+        const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
+        if (xb < ob + padded * cols * 2 && ob < xb + rows * cols * 2)
+            return fail(FP8_ERR_SHAPE, "%s: x and out overlap", who);
+    }
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_pad_rows(x, rows, cols, padded, out, s), who);
+}
+
+fp8_status fp8_check_device_status(cudaStream_t s) {
+    const char *who = "fp8_check_device_status";
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e, who);
+    unsigned int v = 0;
+    e = read_and_clear_device_status(&v);
+    if (e != cudaSuccess) return cuda_status(e, who);
+    if (v == 0) return FP8_OK;
+    return fail(FP8_ERR_TIMEOUT, "%s: a bounded wait ran out (status bits 0x%x: %s%s%s%s)", who, v,
+                (v & kStatusTimeoutTma) ? "tma " : "", (v & kStatusTimeoutMma) ? "mma " : "",
+                (v & kStatusTimeoutEpilogue) ? "epilogue " : "",
+                (v & kStatusTimeoutSelftest) ? "selftest" : "");
+}
+
+fp8_status fp8_selftest_wait_timeout(uint32_t timeout_us, cudaStream_t s) {
+    const char *who = "fp8_selftest_wait_timeout";
+    if (timeout_us < 1 || timeout_us > 1000000)
+        return fail(FP8_ERR_SHAPE, "%s: timeout_us=%u outside 1..1000000", who, timeout_us);
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_selftest_wait(timeout_us, s), who);
+}
+
+}  // extern "C"

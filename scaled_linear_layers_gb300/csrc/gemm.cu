@@ -1,0 +1,321 @@
+// Scaled FP8 GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+//   D[M,N] = bf16( s_A * s_B * sum_k A[m,k] * B[n,k] (+ bias[n]) )
+//
+// A [M,K] and B [N,K] are e4m3 with the contraction dim contiguous (fprop:
+// X·Wᵀ; dgrad: G·(Wᵀ)ᵀ; wgrad: Gᵀ·(Xᵀ)ᵀ — the quantise+transpose kernel
+// supplies the K-major copies).  One persistent CTA per SM, 192 threads:
+//   warp 0      TMA producer: 128x128-byte A and 256x128-byte B boxes, 128-byte
+//               swizzle, into a 4-stage shared-memory ring (48 KB per stage);
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//               and one lane issues tcgen05.mma kind::f8f6f4 (M=128, N=256,
+//               K=32 per instruction, 4 per stage), committing each stage back
+//               to the producer and each finished tile to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, multiply
+//               by s_A*s_B, add bias, round to bf16 and store; the second
+//               accumulator lets the next tile's MMAs run meanwhile.
+// Every mbarrier wait is bounded; on expiry the kernel records a status bit,
+// drains its own MMAs and frees its TMEM before returning.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int A_STAGE = BM * BK, B_STAGE = BN * BK, STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int GROUP_M = 8;
+constexpr uint32_t IDESC = idesc_f8_f32(BM, BN);
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+
+struct GemmArgs {
+    int M, N, K;
+    const float *sa, *sb;
+    const uint16_t *bias;
+    uint16_t *d;
+    int64_t ldd;
+    uint64_t wait_limit_ns;
+    unsigned int *status;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &tm, int &tn) {
+    const int group = GROUP_M * n_tiles;
+    const int gid = tile / group;
+    const int first_m = gid * GROUP_M;
+    const int gsz = min(m_tiles - first_m, GROUP_M);
+    const int in = tile - gid * group;
+    tm = first_m + in % gsz;
+    tn = in / gsz;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_f8_tensor_kernel(const __grid_constant__ CUtensorMap tma_a,
+                          const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_STAGE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *full = bars;                 // [STAGES] TMA -> MMA
+    uint64_t *empty = bars + STAGES;       // [STAGES] MMA -> TMA
+    uint64_t *tfull = bars + 2 * STAGES;   // [2] MMA -> epilogue
+    uint64_t *tempty = tfull + 2;          // [2] epilogue -> MMA
+    uint64_t *drain = tempty + 2;          // [1] MMA completion before teardown
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int nk = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int tm, tn;
+                tile_coords(tile, m_tiles, n_tiles, tm, tn);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns,
+                                           kStatusTimeoutTma, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_2d(sA + stage * A_STAGE, &tma_a, &full[stage], kb * BK, tm * BM);
+                    tma_load_2d(sB + stage * B_STAGE, &tma_b, &full[stage], kb * BK, tn * BN);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the copies already issued land before the CTA exits:
+                // the last STAGES issues are the only ones possibly in flight.
+                for (int s = 0; s < STAGES; ++s) {
+                    stage = stage == 0 ? STAGES - 1 : stage - 1;
+                    if (stage == STAGES - 1) phase ^= 1u;
+                    volatile int no_abort = 0;
+                    mbar_wait_bounded(&full[stage], phase, &no_abort, 10000000ull, kStatusTimeoutTma, p.status);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p.wait_limit_ns,
+                                       kStatusTimeoutMma, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.wait_limit_ns,
+                                           kStatusTimeoutMma, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
+                    const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_f8(d_tmem, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k),
+                               IDESC, (kb | k) != 0);
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(&tfull[acc]);
+            }
+            // all MMAs issued by this thread complete before TMEM is freed
+            mma_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(drain, 0, &no_abort, p.wait_limit_ns, kStatusTimeoutMma, p.status);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const float s = __fmul_rn(*p.sa, *p.sb);
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.wait_limit_ns,
+                                   kStatusTimeoutEpilogue, p.status))
+                break;
+            tc_fence_after();
+            int tm, tn;
+            tile_coords(tile, m_tiles, n_tiles, tm, tn);
+            const int row = tm * BM + quarter * 32 + lane;
+            uint16_t *drow = p.d + (int64_t)row * p.ldd;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                       (uint32_t)(acc * BN + c * 32),
+                                   r);
+                tmem_ld_wait();
+                const int col = tn * BN + c * 32;
+                if (row < p.M && col < p.N) {
+                    uint32_t packed[16];
+                    if (p.bias != nullptr) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float b0 = __uint_as_float((uint32_t)p.bias[col + 2 * j] << 16);
+                            const float b1 =
+                                __uint_as_float((uint32_t)p.bias[col + 2 * j + 1] << 16);
+                            packed[j] =
+                                pack_bf16x2(__fadd_rn(__fmul_rn(__uint_as_float(r[2 * j]), s), b0),
+                                            __fadd_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), s), b1));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            packed[j] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * j]), s),
+                                                    __fmul_rn(__uint_as_float(r[2 * j + 1]), s));
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(drow + col);
+                    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    if (col + 16 < p.N) {  // N is a multiple of 16
+                        dst[2] = make_uint4(packed[8], packed[9], packed[10], packed[11]);
+                        dst[3] = make_uint4(packed[12], packed[13], packed[14], packed[15]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------- host side ---
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+// 2D e4m3 matrix [rows, K] with K contiguous; box = box_rows x 128 bytes.
+bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t rows, int64_t K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
+
+cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                               const float *sa, const float *sb, const uint16_t *bias,
+                               uint16_t *D, cudaStream_t s, const char **why) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_f8_tensor_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, A, M, K, BM) || !make_tmap(&tb, B, N, K, BN)) {
+        *why = "cuTensorMapEncodeTiled failed";
+        return cudaErrorInvalidValue;
+    }
+    GemmArgs args;
+    args.M = (int)M;
+    args.N = (int)N;
+    args.K = (int)K;
+    args.sa = sa;
+    args.sb = sb;
+    args.bias = bias;
+    args.d = D;
+    args.ldd = N;
+    args.wait_limit_ns = g_wait_limit_ns;
+    args.status = device_status_word();
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+    gemm_f8_tensor_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, args);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8

@@ -1,0 +1,51 @@
+// Internal launchers shared by the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8 {
+
+int num_sms();  // SM count of the current device (cached per device)
+
+// Device address of the status word of the current device (nullptr on error).
+unsigned int *device_status_word();
+// Reads the status word and clears it if it was set (synchronous copies).
+cudaError_t read_and_clear_device_status(unsigned int *out);
+
+cudaError_t launch_amax(const uint16_t *x, int64_t n, float *amax_out, cudaStream_t s);
+cudaError_t launch_quantize_tensor(const uint16_t *x, int64_t n, bool dynamic, float *scale,
+                                   float *scale_inv, uint8_t *q, float *amax_out, cudaStream_t s);
+cudaError_t launch_quantize_rowtiles(const uint16_t *x, int64_t rows, int64_t cols, float *scale,
+                                     float *scale_inv, uint8_t *q, float *amax_out,
+                                     cudaStream_t s);
+// mode: 0 tensor/delayed, 1 tensor/dynamic, 2 128x128 tiles, 3 row+column tiles
+cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, int mode,
+                                      float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
+                                      float *scale_t, float *scale_inv_t, float *amax_out,
+                                      cudaStream_t s);
+cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,
+                            uint16_t *out, cudaStream_t s);
+
+// D [M,N] (row-major, leading dim N) = s_a*s_b * A[M,K] · B[N,K]ᵀ (+ bias[N]),
+// A and B e4m3 with K contiguous.  Tensorwise scales: sa, sb point to one
+// float each.
+cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                               const float *sa, const float *sb, const uint16_t *bias,
+                               uint16_t *D, cudaStream_t s, const char **why);
+
+// Block-scaled variant: the contraction is split into 128-blocks; A's block
+// scales are sa[i * sa_ld + kb]; B's are sb[(j / b_rows_per_scale) *
+// sb_row_stride + kb * sb_k_stride].
+cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                              const float *sa, int64_t sa_ld, const float *sb,
+                              int64_t sb_row_stride, int64_t sb_k_stride, int b_rows_per_scale,
+                              uint16_t *D, cudaStream_t s, const char **why);
+
+cudaError_t launch_meta_init(float *dev, int interval, cudaStream_t s);
+cudaError_t launch_meta_copy(float *dst, const float *src, cudaStream_t s);
+cudaError_t launch_meta_lag(float *scale, float *scale_inv, const float *amax, cudaStream_t s);
+cudaError_t launch_meta_refresh(float *dev, int interval, cudaStream_t s);
+cudaError_t launch_selftest_wait(uint32_t timeout_us, cudaStream_t s);
+
+}  // namespace fp8

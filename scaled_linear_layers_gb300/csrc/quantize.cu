@@ -1,0 +1,511 @@
+// HBM-bound kernels: amax, quantise (tensorwise and 1x128 row tiles), the fused
+// quantise + transpose (tensorwise, 128x128 tiles, and 1x128 / 128x1 tiles),
+// and token padding.
+//
+// All of them stream bf16 with 16-byte loads, reduce amax on the bf16 bit
+// patterns (|x| of non-negative bf16 orders like the unsigned pattern) with
+// warp reductions and one atomicMax per block, and cast with
+// cvt.rn.satfinite.e4m3x2.f32 after one IEEE fp32 multiply by scale_inv.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8 {
+
+namespace {
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v) {
+    return max(max(absmax_bits2(v.x), absmax_bits2(v.y)), max(absmax_bits2(v.z), absmax_bits2(v.w)));
+}
+
+// Block-wide max of a per-thread bf16-magnitude bit pattern; result valid in
+// thread 0.  `red` holds one word per warp.
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t m = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, red[w]);
+        v = m;
+    }
+    return v;
+}
+
+// amax bits (a bf16 magnitude pattern) -> fp32 bits of the same value.
+__device__ __forceinline__ unsigned int bf16bits_to_f32bits(uint32_t b) { return b << 16; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ amax ---
+
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ x, int64_t n,
+                                                   float *__restrict__ amax_out) {
+    __shared__ uint32_t red[8];
+    uint32_t m = 0;
+    const int64_t nvec = n >> 3;  // 8 bf16 per 16-byte vector
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+        uint4 a = ldg_nc_v4(xv + i), b = ldg_nc_v4(xv + i + stride);
+        uint4 c = ldg_nc_v4(xv + i + 2 * stride), d = ldg_nc_v4(xv + i + 3 * stride);
+        m = max(m, max(max(absmax_bits8(a), absmax_bits8(b)), max(absmax_bits8(c), absmax_bits8(d))));
+    }
+    for (; i < nvec; i += stride) m = max(m, absmax_bits8(ldg_nc_v4(xv + i)));
+    if (blockIdx.x == 0)
+        for (int64_t j = (nvec << 3) + threadIdx.x; j < n; j += blockDim.x)
+            m = max(m, (uint32_t)(x[j] & 0x7FFFu));
+    m = block_max_u32(m, red);
+    if (threadIdx.x == 0 && m != 0)
+        atomicMax(reinterpret_cast<unsigned int *>(amax_out), bf16bits_to_f32bits(m));
+}
+
+// ------------------------------------------------------ tensorwise cast ---
+// DELAYED: scale_inv is read from `scale_src`; the kernel also emits amax
+//          (if amax_out != nullptr).
+// DYNAMIC: `scale_src` holds this tensor's amax (from amax_kernel); each block
+//          derives scale_inv from it, block 0 publishes scale and scale_inv.
+template <bool kDynamic>
+__global__ void __launch_bounds__(256)
+    quantize_kernel(const uint16_t *__restrict__ x, int64_t n, const float *__restrict__ scale_src,
+                    uint8_t *__restrict__ q, float *__restrict__ amax_out,
+                    float *__restrict__ scale_out, float *__restrict__ scale_inv_out) {
+    __shared__ uint32_t red[8];
+    float si;
+    if (kDynamic) {
+        float s;
+        scales_from_amax(*scale_src, s, si);
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            *scale_out = s;
+            *scale_inv_out = si;
+        }
+    } else {
+        si = *scale_src;
+    }
+    uint32_t m = 0;
+    const int64_t nchunk = n >> 4;  // 16 elements = 32 B in, 16 B out
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+    uint4 *qv = reinterpret_cast<uint4 *>(q);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + stride < nchunk; i += 2 * stride) {
+        uint4 a0 = ldg_nc_v4(xv + 2 * i), a1 = ldg_nc_v4(xv + 2 * i + 1);
+        uint4 b0 = ldg_nc_v4(xv + 2 * (i + stride)), b1 = ldg_nc_v4(xv + 2 * (i + stride) + 1);
+        if (!kDynamic) m = max(m, max(max(absmax_bits8(a0), absmax_bits8(a1)),
+                                      max(absmax_bits8(b0), absmax_bits8(b1))));
+        qv[i] = make_uint4(quant4(a0.x, a0.y, si), quant4(a0.z, a0.w, si), quant4(a1.x, a1.y, si),
+                           quant4(a1.z, a1.w, si));
+        qv[i + stride] = make_uint4(quant4(b0.x, b0.y, si), quant4(b0.z, b0.w, si),
+                                    quant4(b1.x, b1.y, si), quant4(b1.z, b1.w, si));
+    }
+    for (; i < nchunk; i += stride) {
+        uint4 a0 = ldg_nc_v4(xv + 2 * i), a1 = ldg_nc_v4(xv + 2 * i + 1);
+        if (!kDynamic) m = max(m, max(absmax_bits8(a0), absmax_bits8(a1)));
+        qv[i] = make_uint4(quant4(a0.x, a0.y, si), quant4(a0.z, a0.w, si), quant4(a1.x, a1.y, si),
+                           quant4(a1.z, a1.w, si));
+    }
+    if (blockIdx.x == 0) {  // ragged tail: fewer than 16 elements
+        for (int64_t j = (nchunk << 4) + threadIdx.x; j < n; j += blockDim.x) {
+            uint32_t h = x[j];
+            if (!kDynamic) m = max(m, h & 0x7FFFu);
+            q[j] = (uint8_t)(cvt_e4m3x2(__fmul_rn(__uint_as_float(h << 16), si), 0.0f) & 0xFFu);
+        }
+    }
+    if (!kDynamic && amax_out != nullptr) {
+        m = block_max_u32(m, red);
+        if (threadIdx.x == 0 && m != 0)
+            atomicMax(reinterpret_cast<unsigned int *>(amax_out), bf16bits_to_f32bits(m));
+    }
+}
+
+// ----------------------------------------------------- 1x128 row tiles ---
+// One half-warp per 128-element tile: 16 lanes x 8 bf16.  Each warp takes a
+// pair of consecutive tiles and, per iteration, a second pair 2*nwarps
+// tiles further on, so every lane of the warp runs the same loop (the
+// shuffles need the whole warp).  Writes the tile's scale / scale_inv
+// ([rows, cols/128] row-major = tile index order) and its 128 e4m3 bytes;
+// emits the global amax if asked.
+__global__ void __launch_bounds__(256)
+    quantize_rowtiles_kernel(const uint16_t *__restrict__ x, int64_t ntiles,
+                             uint8_t *__restrict__ q, float *__restrict__ scale,
+                             float *__restrict__ scale_inv, float *__restrict__ amax_out) {
+    __shared__ uint32_t red[8];
+    const int lane16 = threadIdx.x & 15;
+    const int half = (threadIdx.x >> 4) & 1;
+    const int64_t wg = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    uint32_t gm = 0;
+    for (int64_t tb = 2 * wg; tb < ntiles; tb += 4 * nw) {
+        const int64_t ta = tb + half, tc = tb + 2 * nw + half;
+        const bool va = ta < ntiles, vc = tc < ntiles;
+        const uint4 a = va ? ldg_nc_v4(reinterpret_cast<const uint4 *>(x + ta * 128) + lane16)
+                           : make_uint4(0, 0, 0, 0);
+        const uint4 c = vc ? ldg_nc_v4(reinterpret_cast<const uint4 *>(x + tc * 128) + lane16)
+                           : make_uint4(0, 0, 0, 0);
+        uint32_t ma = absmax_bits8(a), mc = absmax_bits8(c);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) {
+            ma = max(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, o));
+            mc = max(mc, __shfl_xor_sync(0xFFFFFFFFu, mc, o));
+        }
+        gm = max(gm, max(ma, mc));
+        float s, si;
+        if (va) {
+            scales_from_amax(__uint_as_float(ma << 16), s, si);
+            if (lane16 == 0) {
+                scale[ta] = s;
+                scale_inv[ta] = si;
+            }
+            reinterpret_cast<uint2 *>(q + ta * 128)[lane16] =
+                make_uint2(quant4(a.x, a.y, si), quant4(a.z, a.w, si));
+        }
+        if (vc) {
+            scales_from_amax(__uint_as_float(mc << 16), s, si);
+            if (lane16 == 0) {
+                scale[tc] = s;
+                scale_inv[tc] = si;
+            }
+            reinterpret_cast<uint2 *>(q + tc * 128)[lane16] =
+                make_uint2(quant4(c.x, c.y, si), quant4(c.z, c.w, si));
+        }
+    }
+    if (amax_out != nullptr) {
+        gm = block_max_u32(gm, red);
+        if (threadIdx.x == 0 && gm != 0)
+            atomicMax(reinterpret_cast<unsigned int *>(amax_out), bf16bits_to_f32bits(gm));
+    }
+}
+
+// ------------------------------------------------ fused cast + transpose ---
+// One CTA of 256 threads per 128x128 tile of x [R, C] (R, C multiples of 16;
+// edge tiles are masked).  Load: thread t holds rows (t>>4)+16*i, i < 8, and
+// the 8 columns 8*(t&15)..+7 — 8 x 16-byte loads in flight.  The tile is
+// quantised in registers, q is stored directly (8 bytes per row chunk), and
+// the bytes quantised for the transpose go to a 16 KB shared tile whose
+// 32-bit words are XOR-swizzled by 4*(row/16).  Read back: lane (a = l&7,
+// b = l>>3) of warp wp takes word column w = 4*wp + b of rows 16a..16a+15 —
+// conflict-free under the swizzle — transposes four 4x4 byte blocks with
+// byte permutes and stores 16 bytes to each of qt's rows 4w..4w+3, so 8
+// lanes write one contiguous 128-byte row segment.
+//
+// Scale modes:
+//   kTensorDelayed: one scale_inv read from scale_src; amax emitted.
+//   kTensorDynamic: scale_src holds amax; scales derived and published by
+//                   block (0,0).
+//   kTile2D:        one scale per 128x128 tile from the tile's amax
+//                   (scale grid [R/128, C/128]), used for q and qt.
+//   kRowCol:        q uses 1x128 row-tile scales (scale/scale_inv
+//                   [R, C/128]); qt uses 128x1 column-tile scales
+//                   (scale_t/scale_inv_t [C, R/128]).
+enum QtMode { kTensorDelayed = 0, kTensorDynamic = 1, kTile2D = 2, kRowCol = 3 };
+
+template <int kMode>
+__global__ void __launch_bounds__(256)
+    quantize_transpose_kernel(const uint16_t *__restrict__ x, int R, int C,
+                              const float *__restrict__ scale_src, uint8_t *__restrict__ q,
+                              uint8_t *__restrict__ qt, float *__restrict__ amax_out,
+                              float *__restrict__ scale, float *__restrict__ scale_inv,
+                              float *__restrict__ scale_t, float *__restrict__ scale_inv_t) {
+    __shared__ uint32_t tile[128 * 32];
+    __shared__ uint32_t red[8];
+    __shared__ uint32_t colmax[8][128];
+    __shared__ float col_si[128];
+    __shared__ float tile_si;
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int r0 = blockIdx.y * 128, c0 = blockIdx.x * 128;
+    const int chunk = t & 15, rsub = t >> 4;
+    const int gc = c0 + chunk * 8;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int gr = r0 + rsub + 16 * i;
+        v[i] = (gr < R && gc < C) ? ldg_nc_v4(x + (int64_t)gr * C + gc) : make_uint4(0, 0, 0, 0);
+    }
+
+    float si_all = 0.f;
+    if (kMode == kTensorDelayed) si_all = *scale_src;
+    if (kMode == kTensorDynamic) {
+        float s;
+        scales_from_amax(*scale_src, s, si_all);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+            *scale = s;
+            *scale_inv = si_all;
+        }
+    }
+
+    // amax: whole tile (tensor / tile modes), or per row and per column.
+    float row_si[8];
+    if (kMode == kRowCol) {
+        // rows: the 16 threads sharing rsub hold one 128-element row per i
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t m = absmax_bits8(v[i]);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            float s, si;
+            scales_from_amax(__uint_as_float(m << 16), s, si);
+            row_si[i] = si;
+            const int gr = r0 + rsub + 16 * i;
+            if (chunk == 0 && gr < R && scale != nullptr) {
+                const int64_t idx = (int64_t)gr * (C >> 7) + blockIdx.x;
+                scale[idx] = s;
+                scale_inv[idx] = si;
+            }
+        }
+        // columns: per thread 8 columns over its 8 rows, then across lanes
+        // l and l^16 (same chunk), then across the 8 warps in shared memory.
+        uint32_t cm[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm[e] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                cm[2 * e] = max(cm[2 * e], w4[e] & 0x7FFFu);
+                cm[2 * e + 1] = max(cm[2 * e + 1], (w4[e] >> 16) & 0x7FFFu);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm[e] = max(cm[e], __shfl_xor_sync(0xFFFFFFFFu, cm[e], 16));
+        if (lane < 16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) colmax[warp][chunk * 8 + e] = cm[e];
+        }
+        __syncthreads();
+        if (t < 128) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) m = max(m, colmax[w][t]);
+            float s, si;
+            scales_from_amax(__uint_as_float(m << 16), s, si);
+            col_si[t] = si;
+            if (c0 + t < C) {
+                const int64_t idx = (int64_t)(c0 + t) * (R >> 7) + blockIdx.y;
+                scale_t[idx] = s;
+                scale_inv_t[idx] = si;
+            }
+        }
+        if (amax_out != nullptr && t < 128) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) m = max(m, colmax[w][t]);
+            m = __reduce_max_sync(0xFFFFFFFFu, m);
+            if (lane == 0 && m != 0)
+                atomicMax(reinterpret_cast<unsigned int *>(amax_out), bf16bits_to_f32bits(m));
+        }
+        __syncthreads();
+    } else {
+        uint32_t m = 0;
+        if (kMode != kTensorDynamic) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = max(m, absmax_bits8(v[i]));
+            m = block_max_u32(m, red);
+        }
+        if (kMode == kTile2D) {
+            if (t == 0) {
+                float s, si;
+                scales_from_amax(__uint_as_float(m << 16), s, si);
+                const int64_t idx = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+                scale[idx] = s;
+                scale_inv[idx] = si;
+                tile_si = si;
+            }
+            __syncthreads();
+            si_all = tile_si;
+        }
+        if (kMode != kTensorDynamic && amax_out != nullptr && t == 0 && m != 0)
+            atomicMax(reinterpret_cast<unsigned int *>(amax_out), bf16bits_to_f32bits(m));
+    }
+
+    // quantise: q (row scales) straight to global, transpose bytes to smem
+    float csi[8];
+    if (kMode == kRowCol) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) csi[e] = col_si[chunk * 8 + e];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = rsub + 16 * i;
+        const int gr = r0 + row;
+        uint32_t t0, t1;
+        if (kMode == kRowCol) {
+            const float si = row_si[i];
+            if (q != nullptr && gr < R && gc < C)
+                *reinterpret_cast<uint2 *>(q + (int64_t)gr * C + gc) =
+                    make_uint2(quant4(v[i].x, v[i].y, si), quant4(v[i].z, v[i].w, si));
+            t0 = cvt_e4m3x2(__fmul_rn(bf16_lo(v[i].x), csi[0]), __fmul_rn(bf16_hi(v[i].x), csi[1])) |
+                 (cvt_e4m3x2(__fmul_rn(bf16_lo(v[i].y), csi[2]), __fmul_rn(bf16_hi(v[i].y), csi[3]))
+                  << 16);
+            t1 = cvt_e4m3x2(__fmul_rn(bf16_lo(v[i].z), csi[4]), __fmul_rn(bf16_hi(v[i].z), csi[5])) |
+                 (cvt_e4m3x2(__fmul_rn(bf16_lo(v[i].w), csi[6]), __fmul_rn(bf16_hi(v[i].w), csi[7]))
+                  << 16);
+        } else {
+            t0 = quant4(v[i].x, v[i].y, si_all);
+            t1 = quant4(v[i].z, v[i].w, si_all);
+            if (q != nullptr && gr < R && gc < C)
+                *reinterpret_cast<uint2 *>(q + (int64_t)gr * C + gc) = make_uint2(t0, t1);
+        }
+        const int wcol = (chunk * 2) ^ (4 * (row >> 4));
+        *reinterpret_cast<uint2 *>(&tile[row * 32 + wcol]) = make_uint2(t0, t1);
+    }
+    if (qt == nullptr) return;  // 2D-tile quantisation without the transpose
+    __syncthreads();
+
+    // transposed read-back
+    const int a = lane & 7, b = lane >> 3;
+    const int w = 4 * warp + b;
+    uint32_t wv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) wv[i] = tile[(16 * a + i) * 32 + (w ^ (4 * a))];
+    uint32_t col[4][4];  // col[j][k]: rows 16a+4k..+3 of column 4w+j
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t x0 = wv[4 * k], x1 = wv[4 * k + 1], x2 = wv[4 * k + 2], x3 = wv[4 * k + 3];
+        const uint32_t p0 = __byte_perm(x0, x1, 0x5140), p1 = __byte_perm(x0, x1, 0x7362);
+        const uint32_t p2 = __byte_perm(x2, x3, 0x5140), p3 = __byte_perm(x2, x3, 0x7362);
+        col[0][k] = __byte_perm(p0, p2, 0x5410);
+        col[1][k] = __byte_perm(p0, p2, 0x7632);
+        col[2][k] = __byte_perm(p1, p3, 0x5410);
+        col[3][k] = __byte_perm(p1, p3, 0x7632);
+    }
+    const int gr = r0 + 16 * a;
+    if (gr < R) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gcc = c0 + 4 * w + j;
+            if (gcc < C)
+                *reinterpret_cast<uint4 *>(qt + (int64_t)gcc * R + gr) =
+                    make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
+        }
+    }
+}
+
+// --------------------------------------------------------------- padding ---
+
+__global__ void __launch_bounds__(256) pad_rows_kernel_v16(const uint4 *__restrict__ x,
+                                                           int64_t n_in, int64_t n_out,
+                                                           uint4 *__restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_out; i += stride)
+        out[i] = i < n_in ? ldg_nc_v4(x + i) : make_uint4(0, 0, 0, 0);
+}
+
+__global__ void __launch_bounds__(256) pad_rows_kernel_scalar(const uint16_t *__restrict__ x,
+                                                              int64_t n_in, int64_t n_out,
+                                                              uint16_t *__restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_out; i += stride)
+        out[i] = i < n_in ? x[i] : (uint16_t)0;
+}
+
+// ------------------------------------------------------------ launchers ---
+
+static int grid_for(int64_t work_items, int per_block) {
+    int64_t g = (work_items + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+cudaError_t launch_amax(const uint16_t *x, int64_t n, float *amax_out, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    if (e != cudaSuccess || n == 0) return e;
+    amax_kernel<<<grid_for((n >> 3) / 4 + 1, 256), 256, 0, s>>>(x, n, amax_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_tensor(const uint16_t *x, int64_t n, bool dynamic, float *scale,
+                                   float *scale_inv, uint8_t *q, float *amax_out,
+                                   cudaStream_t s) {
+    cudaError_t e;
+    const int grid = grid_for((n >> 4) / 2 + 1, 256);
+    if (dynamic) {
+        if ((e = launch_amax(x, n, amax_out, s)) != cudaSuccess) return e;
+        quantize_kernel<true><<<grid, 256, 0, s>>>(x, n, amax_out, q, nullptr, scale, scale_inv);
+    } else {
+        if (amax_out != nullptr && (e = cudaMemsetAsync(amax_out, 0, sizeof(float), s)) != cudaSuccess)
+            return e;
+        if (n == 0) return cudaSuccess;
+        quantize_kernel<false><<<grid, 256, 0, s>>>(x, n, scale_inv, q, amax_out, nullptr, nullptr);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rowtiles(const uint16_t *x, int64_t rows, int64_t cols, float *scale,
+                                     float *scale_inv, uint8_t *q, float *amax_out,
+                                     cudaStream_t s) {
+    cudaError_t e;
+    if (amax_out != nullptr && (e = cudaMemsetAsync(amax_out, 0, sizeof(float), s)) != cudaSuccess)
+        return e;
+    const int64_t ntiles = rows * (cols / 128);
+    if (ntiles == 0) return cudaSuccess;
+    quantize_rowtiles_kernel<<<grid_for(ntiles, 32), 256, 0, s>>>(x, ntiles, q, scale, scale_inv,
+                                                                  amax_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, int mode,
+                                      float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
+                                      float *scale_t, float *scale_inv_t, float *amax_out,
+                                      cudaStream_t s) {
+    cudaError_t e;
+    const float *src = nullptr;
+    if (mode == kTensorDynamic) {
+        if ((e = launch_amax(x, rows * cols, amax_out, s)) != cudaSuccess) return e;
+        src = amax_out;
+    } else {
+        if (amax_out != nullptr && (e = cudaMemsetAsync(amax_out, 0, sizeof(float), s)) != cudaSuccess)
+            return e;
+        if (mode == kTensorDelayed) src = scale_inv;
+    }
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    dim3 grid((unsigned)((cols + 127) / 128), (unsigned)((rows + 127) / 128));
+    float *amax_k = mode == kTensorDynamic ? nullptr : amax_out;
+    switch (mode) {
+    case kTensorDelayed:
+        quantize_transpose_kernel<kTensorDelayed><<<grid, 256, 0, s>>>(
+            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
+        break;
+    case kTensorDynamic:
+        quantize_transpose_kernel<kTensorDynamic><<<grid, 256, 0, s>>>(
+            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
+        break;
+    case kTile2D:
+        quantize_transpose_kernel<kTile2D><<<grid, 256, 0, s>>>(
+            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
+        break;
+    default:
+        quantize_transpose_kernel<kRowCol><<<grid, 256, 0, s>>>(
+            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,
+                            uint16_t *out, cudaStream_t s) {
+    const int64_t n_in = rows * cols, n_out = padded * cols;
+    if (n_out == 0) return cudaSuccess;
+    if (cols % 8 == 0) {
+        pad_rows_kernel_v16<<<grid_for(n_out / 8, 256), 256, 0, s>>>(
+            reinterpret_cast<const uint4 *>(x), n_in / 8, n_out / 8, reinterpret_cast<uint4 *>(out));
+    } else {
+        pad_rows_kernel_scalar<<<grid_for(n_out, 256), 256, 0, s>>>(x, n_in, n_out, out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fp8

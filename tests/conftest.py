@@ -11,3 +11,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running full-size case")
+
+
+def pytest_sessionstart(session):
+    # the C-ABI library and the oracle are built in-tree before collection
+    import __graft_entry__
+    __graft_entry__.build()

@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/fp8linear.h declares, and rejects bad arguments on the host before
+anything is enqueued (the rejection happens before the device is touched, so
+these run on a CPU-only machine)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8linear.h")
+GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "page_facts.json")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    from scaled_linear_layers_gb300 import _lib
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8_[a-z0-9_]+)\s*\(", text)) - {"fp8_meta", "fp8_status"})
+
+
+def test_header_declares_the_expected_boundary():
+    syms = declared_symbols()
+    for name in ["fp8_quantize", "fp8_quantize_transpose", "fp8_linear_fprop", "fp8_linear_dgrad",
+                 "fp8_linear_wgrad", "fp8_meta_record", "fp8_meta_refresh", "fp8_pad_tokens"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from scaled_linear_layers_gb300 import _lib
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_library_does_not_link_the_oracle(lib):
+    from scaled_linear_layers_gb300 import _lib
+    assert not hasattr(lib, "orc_e4m3_encode")
+    with open(_lib.LIB_PATH, "rb") as f:
+        assert b"orc_" not in f.read()
+
+
+def test_version(lib):
+    assert lib.fp8_version().decode().startswith("fp8linear")
+
+
+def test_padded_rows_page_example(lib):
+    ex = GOLDEN["unaligned_token_count_example"]
+    m = GOLDEN["token_multiple"]["value"]
+    assert lib.fp8_padded_rows(ex["rows"], m) == 3872
+    assert lib.fp8_padded_rows(0, 16) == 0
+    assert lib.fp8_padded_rows(16, 16) == 16
+    assert lib.fp8_padded_rows(17, 16) == 32
+    assert lib.fp8_padded_rows(-1, 16) == -1
+    assert lib.fp8_padded_rows(5, 0) == -1
+
+
+def test_gemm_rejects_unaligned_token_count_with_the_pages_message(lib):
+    ex = GOLDEN["unaligned_token_count_example"]
+    st = lib.fp8_linear_fprop(None, None, None, None, 4096, 4096, ex["rows"], 0, None, None, None)
+    assert st == 3  # FP8_ERR_ALIGNMENT
+    msg = lib.fp8_last_error().decode()
+    assert f"Expected K to be divisible by 16, but got K={ex['rows']}" in msg
+    st = lib.fp8_linear_wgrad(None, None, None, None, ex["rows"], 4096, 4096, 0, None, None)
+    assert st == 3 and f"but got M={ex['rows']}" in lib.fp8_last_error().decode()
+
+
+def test_gemm_block_recipe_needs_multiples_of_128(lib):
+    st = lib.fp8_linear_fprop(None, None, None, None, 256, 256, 144, 2, None, None, None)
+    assert st == 3 and "divisible by 128" in lib.fp8_last_error().decode()
+
+
+def test_null_shape_and_alignment_errors(lib):
+    assert lib.fp8_linear_fprop(None, None, None, None, 0, 16, 16, 0, None, None, None) == 2
+    assert lib.fp8_linear_fprop(None, None, None, None, 16, 16, 16, 0, None, None, None) == 1
+    assert "is NULL" in lib.fp8_last_error().decode()
+    assert lib.fp8_quantize(None, 4, 4, 0, None, None, None, None, None) == 1
+    assert lib.fp8_quantize(None, -1, 4, 0, None, None, None, None, None) == 2
+    bad = ctypes.c_void_p(0x1001)  # never dereferenced: rejected on the host
+    good = ctypes.c_void_p(0x2000)
+    assert lib.fp8_quantize(bad, 4, 4, 0, None, good, good, None, None) == 3
+    assert "16-byte aligned" in lib.fp8_last_error().decode()
+    assert lib.fp8_quantize_transpose(good, 24, 16, 0, None, good, good, good, None, None, None,
+                                      None) == 3
+    assert lib.fp8_quantize_transpose(good, 16, 16, 9, None, good, good, good, None, None, None,
+                                      None) == 2
+    # dynamic scaling needs somewhere to put the amax
+    assert lib.fp8_quantize(good, 4, 4, 1, good, good, good, None, None) == 1
+
+
+def test_state_step_host_counter(lib):
+    from scaled_linear_layers_gb300 import _lib
+    cnt = ctypes.c_int64(0)
+    for i in range(15):  # no refresh due before the 16th step: host only
+        assert lib.fp8_state_step(ctypes.byref(cnt), 16, None, 0, None) == 0
+    assert cnt.value == 15
+    assert lib.fp8_state_step(ctypes.byref(cnt), 16, None, 0, None) == 0
+    assert cnt.value == 16
+    assert lib.fp8_state_step(ctypes.byref(cnt), 0, None, 0, None) == 2
+    m = _lib.fp8_meta()
+    assert lib.fp8_meta_record(ctypes.byref(m), 0, None, None) == 1
+
+
+def test_pad_tokens_rejects_overlap_and_bad_multiple(lib):
+    p = ctypes.c_void_p(0x10000)
+    out_rows = ctypes.c_int64(0)
+    assert lib.fp8_pad_tokens(p, 10, 16, 0, p, ctypes.byref(out_rows), None) == 2
+    assert lib.fp8_pad_tokens(p, 10, 16, 16, p, ctypes.byref(out_rows), None) == 2
+    assert "overlap" in lib.fp8_last_error().decode()
+    assert out_rows.value == 16
