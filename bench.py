@@ -86,11 +86,18 @@ class ClockSampler:
         if exe:
             self.proc = subprocess.Popen(
                 [exe, f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()  # the first sample marks the sampler as running
+            while not self.lines and time.time() - t0 < 10 and self.proc.poll() is None:
+                time.sleep(0.01)
         return self
+
+    def mark(self):
+        """Index of the next sample: samples from here on fall in the region."""
+        return len(self.lines)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -105,9 +112,9 @@ class ClockSampler:
                 self.proc.kill()
             self.t.join(timeout=2)
 
-    def summary(self):
+    def summary(self, start: int = 0):
         rows = []
-        for ln in self.lines:
+        for ln in self.lines[start:]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) != 6:
                 continue
@@ -242,11 +249,13 @@ def gpu_arm(args, rank, world):
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
+        first = clk.mark()
         t_start.record()
         for t in range(args.warmup, args.warmup + args.steps):
             step.run(t)
         t_end.record()
         barrier()
+        clocks = clk.summary(first)
     launches = step.launches
     ms_total = t_start.elapsed_time(t_end)
     segs = kernel_times(step.events)
@@ -263,7 +272,7 @@ def gpu_arm(args, rank, world):
             torch.empty((N, K), dtype=torch.bfloat16).pin_memory()]
     h2d = x_buf.numel() * 2 + g_buf.numel() * 2
     d2h = sum(o.numel() * 2 for o in outs)
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = max(3, min(args.steps, 200))
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -331,7 +340,7 @@ def gpu_arm(args, rank, world):
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e_step, 4)},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     return line
 
@@ -435,8 +444,8 @@ def cpu_baseline_for_gpu_line(steps: int = 2):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fp8 {
 
@@ -190,9 +191,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
-            if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.wait_limit_ns,
-                                   kStatusTimeoutEpilogue, p.status))
-                break;
+            // the warp leaves together: tcgen05.ld below needs all 32 lanes
+            const bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.wait_limit_ns,
+                                              kStatusTimeoutEpilogue, p.status);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
             int tm, tn;
             tile_coords(tile, m_tiles, n_tiles, tm, tn);
@@ -250,37 +252,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ---------------------------------------------------------- host side ---
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(ptr);
-    }();
-    return fn;
-}
-
-// 2D e4m3 matrix [rows, K] with K contiguous; box = box_rows x 128 bytes.
-bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t rows, int64_t K, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
@@ -288,16 +259,18 @@ uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
 cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
                                const float *sa, const float *sb, const uint16_t *bias,
                                uint16_t *D, cudaStream_t s, const char **why) {
-    static bool attr_done = false;
-    if (!attr_done) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(gemm_f8_tensor_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        attr_done[dev] = true;
     }
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, A, M, K, BM) || !make_tmap(&tb, B, N, K, BN)) {
+    if (!make_tmap_k128(&ta, A, M, K, BM) || !make_tmap_k128(&tb, B, N, K, BN)) {
         *why = "cuTensorMapEncodeTiled failed";
         return cudaErrorInvalidValue;
     }

@@ -1,0 +1,118 @@
+"""GPU parity of the block-scaled FP8 GEMMs (1x128 activation/gradient tiles,
+128x128 weight tiles; the TE "recipe=block" of the NeMo SALMAutomodel page)
+against the oracle's per-block fp64 GEMM, through the C ABI.  Operands and
+scales come from the oracle's block quantisers, so only the GEMM is tested
+here (the quantisers have their own bit-exact tests)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import bf16_out
+
+import scaled_linear_layers_gb300 as fp8
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def check(got, ref, bound):
+    ok = oracle.gemm_tolerance_ok(got, ref, bound)
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outside tolerance; first {np.argwhere(~ok)[:3]}"
+
+
+SHAPES = [(128, 128, 128), (256, 384, 512), (384, 256, 1024), (1024, 512, 768)]
+
+
+def operands(M, N, K, seed):
+    x = synth.normal_with_outliers_bf16((M, K), 1.0, seed, "x")
+    w = synth.normal_with_outliers_bf16((N, K), 1.0, seed, "w")
+    g = synth.normal_with_outliers_bf16((M, N), 1.0, seed, "g")
+    return x, w, g
+
+
+def all_entries(R, C):
+    ii, jj = np.meshgrid(np.arange(R), np.arange(C), indexing="ij")
+    return ii.ravel(), jj.ravel()
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_block_fprop(shape):
+    M, N, K = shape
+    x, w, _ = operands(M, N, K, 1)
+    xq, xs, _ = oracle.quantize_rowtiles(x, 128)
+    wq, ws, _ = oracle.quantize_sqtiles(w, 128)
+    y = bf16_out(M, N)
+    fp8.fp8_linear_fprop(dev(xq), dev(xs), dev(wq), dev(ws), M, N, K, fp8.BLOCK, None, y)
+    ii, jj = all_entries(M, N)
+    _, ref, bound = oracle.gemm_block_entries(xq, wq, xs, ws, 128, ii, jj)
+    check(y.float().cpu().numpy().ravel(), ref, bound)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_block_dgrad(shape):
+    M, N, K = shape
+    _, w, g = operands(M, N, K, 2)
+    gq, gs, _ = oracle.quantize_rowtiles(g, 128)
+    wq, ws, _ = oracle.quantize_sqtiles(w, 128)
+    wqt = oracle.transpose_u8(wq)
+    dx = bf16_out(M, K)
+    fp8.fp8_linear_dgrad(dev(gq), dev(gs), dev(wqt), dev(ws), M, N, K, fp8.BLOCK, dx)
+    ii, jj = all_entries(M, K)
+    # B = Wqᵀ [K, N]: its 128x128 tile grid is the transpose of W's
+    _, ref, bound = oracle.gemm_block_entries(gq, wqt, gs, np.ascontiguousarray(ws.T), 128, ii, jj)
+    check(dx.float().cpu().numpy().ravel(), ref, bound)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_block_wgrad(shape):
+    M, N, K = shape
+    x, _, g = operands(M, N, K, 3)
+    gqt, gst, _ = oracle.quantize_coltiles_t(g, 128)   # [N, M], scales [N, M/128]
+    xqt, xst, _ = oracle.quantize_coltiles_t(x, 128)   # [K, M], scales [K, M/128]
+    dw = bf16_out(N, K)
+    fp8.fp8_linear_wgrad(dev(gqt), dev(gst), dev(xqt), dev(xst), M, N, K, fp8.BLOCK, dw)
+    ii, jj = all_entries(N, K)
+    _, ref, bound = oracle.gemm_block_entries(gqt, xqt, gst, xst, 1, ii, jj)
+    check(dw.float().cpu().numpy().ravel(), ref, bound)
+
+
+def test_block_equal_scales_match_tensorwise_gemm():
+    """With every tile scale equal, the block GEMM reduces to the tensorwise
+    one: both kernels must agree within the tolerance (and the oracle's two
+    GEMMs agree exactly, pinned on the CPU)."""
+    M, N, K = 256, 256, 512
+    rng = np.random.default_rng(4)
+    A = rng.integers(0, 0x7E, (M, K), dtype=np.uint8)
+    B = rng.integers(0, 0x7E, (N, K), dtype=np.uint8)
+    sa = np.full((M, K // 128), 0.03, np.float32)
+    sb = np.full((N // 128, K // 128), 0.5, np.float32)
+    y_blk = bf16_out(M, N)
+    fp8.fp8_linear_fprop(dev(A), dev(sa), dev(B), dev(sb), M, N, K, fp8.BLOCK, None, y_blk)
+    y_t = bf16_out(M, N)
+    fp8.fp8_linear_fprop(dev(A), dev(sa[:1, :1].ravel()), dev(B), dev(sb[:1, :1].ravel()), M, N, K,
+                         fp8.DELAYED, None, y_t)
+    _, ref, bound = oracle.gemm(A, B, np.float32(0.03), np.float32(0.5))
+    check(y_blk.float().cpu().numpy(), ref, bound)
+    check(y_t.float().cpu().numpy(), ref, bound)
+
+
+def test_block_full_size_sampled():
+    """The block workload's fprop shape (M=32768, K=N=8192) on sampled rows."""
+    M, N, K = 32768, 8192, 8192
+    rng = np.random.default_rng(5)
+    A = rng.integers(0, 0x7E, (M, K), dtype=np.uint8) | (rng.integers(0, 2, (M, K), dtype=np.uint8) << 7)
+    B = rng.integers(0, 0x7E, (N, K), dtype=np.uint8)
+    sa = rng.uniform(1e-3, 1e-1, (M, K // 128)).astype(np.float32)
+    sb = rng.uniform(1e-3, 1e-1, (N // 128, K // 128)).astype(np.float32)
+    y = bf16_out(M, N)
+    fp8.fp8_linear_fprop(dev(A), dev(sa), dev(B), dev(sb), M, N, K, fp8.BLOCK, None, y)
+    rows = rng.choice(M, 2, replace=False)
+    ii = np.concatenate([rng.integers(0, M, 2048), np.repeat(rows, N)])
+    jj = np.concatenate([rng.integers(0, N, 2048), np.tile(np.arange(N), 2)])
+    _, ref, bound = oracle.gemm_block_entries(A, B, sa, sb, 128, ii, jj)
+    check(y.float().cpu().numpy()[ii, jj], ref, bound)

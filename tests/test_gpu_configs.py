@@ -1,0 +1,314 @@
+"""End-to-end parity of the five workloads against the oracle, through the C ABI.
+
+1. one FP8 linear fprop, dynamic tensorwise scaling, X [64,256], W [256,256];
+2. one FP8 linear fwd+dgrad+wgrad under delayed scaling for 20 steps
+   (16-step weight amax history, X/G scales lagged one call) — all 20 steps at
+   512^3 with full comparison, and the first steps at the full 4096^3 size
+   with full quantised bytes / scales and sampled GEMM outputs;
+3. a transformer MLP block (tokens 16384, hidden 4096, FFN 14336), dynamic
+   scaling, every projection fwd+dgrad+wgrad, sampled outputs;
+4. a packed THD batch of 64 sequences (lengths 128..4096) zero-padded to a
+   multiple of 16: padded rows change no amax and no real output;
+5. the block-scaled recipe at M=32768, K=N=8192, inputs with 1% outliers x50.
+
+Bytes, amaxes and scales must be bit-exact; GEMM outputs within the stated
+tolerance |D - bf16(D_ref)| <= 1e-2 * s_A s_B sum|a||b| + 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import state as ost
+from helpers import dev_bf16, host_u8, f32, u8, bf16_out, first_diff
+
+import scaled_linear_layers_gb300 as fp8
+
+pytestmark = pytest.mark.gpu
+
+
+def f32bits(v):
+    return np.float32(v).view(np.uint32)
+
+
+def check_gemm(got_full, ref_tuple, ii=None, jj=None):
+    _, ref, bound = ref_tuple
+    got = got_full if ii is None else got_full[ii, jj]
+    ok = oracle.gemm_tolerance_ok(got, ref, bound)
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outside tolerance"
+
+
+def sample_entries(rng, R, C, n=2048, panels=2):
+    rows = rng.choice(R, panels, replace=False)
+    ii = np.concatenate([rng.integers(0, R, n), np.repeat(rows, C)])
+    jj = np.concatenate([rng.integers(0, C, n), np.tile(np.arange(C), panels)])
+    return ii, jj
+
+
+# ------------------------------------------------------------ workload 1 ---
+
+def test_config1_dynamic_fprop():
+    c = synth.CONFIG1
+    M, K, N = c["M"], c["K"], c["N"]
+    x = synth.normal_bf16((M, K), c["x_sigma"], c["seed"], "x")
+    w = synth.normal_bf16((N, K), c["w_sigma"], c["seed"], "w")
+    qx, qw = u8(M, K), u8(N, K)
+    sx, six, ax = f32(), f32(), f32()
+    sw, siw, aw = f32(), f32(), f32()
+    fp8.fp8_quantize(dev_bf16(x), fp8.DYNAMIC, sx, six, qx, ax)
+    fp8.fp8_quantize(dev_bf16(w), fp8.DYNAMIC, sw, siw, qw, aw)
+    y = bf16_out(M, N)
+    fp8.fp8_linear_fprop(qx, sx, qw, sw, M, N, K, fp8.DYNAMIC, None, y)
+    rx = oracle.quantize_dynamic(x)
+    rw = oracle.quantize_dynamic(w)
+    assert np.array_equal(host_u8(qx), rx[0]) and np.array_equal(host_u8(qw), rw[0])
+    assert sx.item() == rx[1] and sw.item() == rw[1]
+    check_gemm(y.float().cpu().numpy(), oracle.gemm(rx[0], rw[0], rx[1], rw[1]))
+
+
+# ------------------------------------------------------------ workload 2 ---
+
+class GpuDelayedLinear:
+    """The delayed-scaling call sequence of one training step through the C ABI."""
+
+    def __init__(self, M, N, K, w):
+        self.M, self.N, self.K = M, N, K
+        self.w = w
+        self.meta = fp8.Fp8Meta(16)
+        self.count = [0]
+        self.xq, self.xqt = u8(M, K), u8(K, M)
+        self.wq, self.wqt = u8(N, K), u8(K, N)
+        self.gq, self.gqt = u8(M, N), u8(N, M)
+        self.y, self.dx, self.dw = bf16_out(M, N), bf16_out(M, K), bf16_out(N, K)
+        self.ax, self.aw, self.ag = f32(), f32(), f32()
+
+    def step(self, x, g):
+        m, M, N, K = self.meta, self.M, self.N, self.K
+        fp8.fp8_state_step(self.count, 16, [m])
+        used = dict(x_scale=m.x_scale.item(), x_scale_inv=m.x_scale_inv.item(),
+                    w_scale=m.scale.item(), g_scale=m.g_scale.item())
+        fp8.fp8_quantize(x, fp8.DELAYED, None, m.x_scale_inv, self.xq, self.ax)
+        fp8.fp8_quantize_transpose(self.w, fp8.DELAYED, None, m.scale_inv, self.wq, self.wqt,
+                                   amax_out=self.aw)
+        fp8.fp8_linear_fprop(self.xq, m.x_scale, self.wq, m.scale, M, N, K, fp8.DELAYED, None,
+                             self.y)
+        fp8.fp8_meta_record(m, fp8.SLOT_W, self.aw)
+        fp8.fp8_meta_record(m, fp8.SLOT_X, self.ax)
+        fp8.fp8_quantize_transpose(g, fp8.DELAYED, None, m.g_scale_inv, self.gq, self.gqt,
+                                   amax_out=self.ag)
+        fp8.fp8_quantize_transpose(x, fp8.DELAYED, None, m.x_scale_inv, None, self.xqt)
+        used["x_scale_bwd"] = m.x_scale.item()
+        fp8.fp8_linear_dgrad(self.gq, m.g_scale, self.wqt, m.scale, M, N, K, fp8.DELAYED, self.dx)
+        fp8.fp8_linear_wgrad(self.gqt, m.g_scale, self.xqt, m.x_scale, M, N, K, fp8.DELAYED,
+                             self.dw)
+        fp8.fp8_meta_record(m, fp8.SLOT_G, self.ag)
+        fp8.fp8_check_device_status()
+        return used
+
+
+def run_delayed(M, N, K, steps, full_gemm, seed=0):
+    c = synth.CONFIG2
+    rng = np.random.default_rng(seed)
+    w = synth.normal_bf16((N, K), c["w_sigma"], seed, "w")
+    gpu = GpuDelayedLinear(M, N, K, dev_bf16(w))
+    st = ost.State(16)
+    meta = st.new_meta()
+    for t in range(steps):
+        x = synth.normal_bf16((M, K), c["x_sigma"], seed, "x", t)
+        g = synth.normal_bf16((M, N), c["g_sigma"], seed, "g", t)
+        used = gpu.step(dev_bf16(x), dev_bf16(g))
+        if full_gemm:
+            entries = None
+        else:
+            entries = dict(y=sample_entries(rng, M, N), dx=sample_entries(rng, M, K),
+                           dw=sample_entries(rng, N, K))
+        ref = ost.delayed_training_step(st, meta, x, w, g, entries)
+        f, b = ref["fwd"], ref["bwd"]
+        # scales used by this step, bit for bit
+        assert f32bits(used["x_scale"]) == f32bits(f["used"]["x_scale"]), t
+        assert f32bits(used["w_scale"]) == f32bits(f["used"]["w_scale"]), t
+        assert f32bits(used["g_scale"]) == f32bits(b["used"]["g_scale"]), t
+        assert f32bits(used["x_scale_bwd"]) == f32bits(b["used"]["x_scale"]), t
+        # bytes and amaxes
+        assert np.array_equal(host_u8(gpu.xq), f["xq"]), first_diff(host_u8(gpu.xq), f["xq"])
+        assert np.array_equal(host_u8(gpu.wq), f["wq"])
+        assert np.array_equal(host_u8(gpu.gq), b["gq"])
+        assert np.array_equal(host_u8(gpu.xqt), b["xq_bwd"].T)
+        assert f32bits(gpu.ax.item()) == f32bits(f["amax_x"])
+        assert f32bits(gpu.aw.item()) == f32bits(f["amax_w"])
+        assert f32bits(gpu.ag.item()) == f32bits(b["amax_g"])
+        # state after the step
+        snap = ref["meta"]
+        blk = gpu.meta.block.cpu().numpy()
+        assert np.array_equal(blk[8:].view(np.uint32), snap["amax_history"].view(np.uint32))
+        assert gpu.meta.idx == snap["idx"]
+        for k, i in (("scale", 0), ("scale_inv", 1), ("x_scale", 2), ("x_scale_inv", 3),
+                     ("g_scale", 4), ("g_scale_inv", 5)):
+            assert f32bits(blk[i]) == f32bits(snap[k]), (t, k)
+        # GEMMs
+        for name, out in (("y", gpu.y), ("dx", gpu.dx), ("dw", gpu.dw)):
+            got = out.float().cpu().numpy()
+            src = f if name == "y" else b
+            if full_gemm:
+                check_gemm(got, src[name])
+            else:
+                ii, jj = entries[name]
+                check_gemm(got, src[name], ii, jj)
+    return st
+
+
+def test_config2_delayed_20_steps_small():
+    st = run_delayed(512, 512, 512, steps=20, full_gemm=True)
+    assert st.step_count == 20
+
+
+def test_config2_delayed_full_size_first_steps():
+    run_delayed(4096, 4096, 4096, steps=2, full_gemm=False)
+
+
+# ------------------------------------------------------------ workload 3 ---
+
+def dynamic_linear_gpu(x, w, g):
+    """Dynamic tensorwise fwd+dgrad+wgrad of one projection on the GPU."""
+    M, K = x.shape
+    N = w.shape[0]
+    res = {}
+    for name, t in (("x", x), ("w", w), ("g", g)):
+        r, c = t.shape
+        q, qt = u8(r, c), u8(c, r)
+        s, si, a = f32(), f32(), f32()
+        fp8.fp8_quantize_transpose(t, fp8.DYNAMIC, s, si, q, qt, amax_out=a)
+        res[name] = (q, qt, s, a)
+    y, dx, dw = bf16_out(M, N), bf16_out(M, K), bf16_out(N, K)
+    X, W, G = res["x"], res["w"], res["g"]
+    fp8.fp8_linear_fprop(X[0], X[2], W[0], W[2], M, N, K, fp8.DYNAMIC, None, y)
+    fp8.fp8_linear_dgrad(G[0], G[2], W[1], W[2], M, N, K, fp8.DYNAMIC, dx)
+    fp8.fp8_linear_wgrad(G[1], G[2], X[1], X[2], M, N, K, fp8.DYNAMIC, dw)
+    fp8.fp8_check_device_status()
+    return res, y, dx, dw
+
+
+def check_dynamic_projection(xh, wh, gh, res, y, dx, dw, rng, sample_rows=8):
+    refq = {}
+    for name, h in (("x", xh), ("w", wh), ("g", gh)):
+        q, qt, s, a = res[name]
+        amax = oracle.amax(h)
+        rs, rsi = oracle.scale_from_amax(amax)
+        assert f32bits(a.item()) == f32bits(amax) and f32bits(s.item()) == f32bits(rs)
+        rows = rng.choice(h.shape[0], sample_rows, replace=False)
+        rq, _ = oracle.quantize(np.ascontiguousarray(h[rows]), rsi)
+        assert np.array_equal(host_u8(q[torch.from_numpy(rows).cuda()]), rq)
+        cols = rng.choice(h.shape[1], sample_rows, replace=False)
+        rqt, _ = oracle.quantize(np.ascontiguousarray(h[:, cols].T), rsi)
+        assert np.array_equal(host_u8(qt[torch.from_numpy(cols).cuda()]), rqt)
+        refq[name] = (host_u8(q), rs)
+    X, W, G = refq["x"], refq["w"], refq["g"]
+    M, K = xh.shape
+    N = wh.shape[0]
+    ii, jj = sample_entries(rng, M, N, 1024, 1)
+    check_gemm(y.float().cpu().numpy(), oracle.gemm_entries(X[0], W[0], X[1], W[1], ii, jj), ii, jj)
+    ii, jj = sample_entries(rng, M, K, 1024, 1)
+    check_gemm(dx.float().cpu().numpy(),
+               oracle.gemm_entries(G[0], oracle.transpose_u8(W[0]), G[1], W[1], ii, jj), ii, jj)
+    ii, jj = sample_entries(rng, N, K, 1024, 1)
+    check_gemm(dw.float().cpu().numpy(),
+               oracle.gemm_entries(oracle.transpose_u8(G[0]), oracle.transpose_u8(X[0]), G[1],
+                                   X[1], ii, jj), ii, jj)
+
+
+@pytest.mark.parametrize("proj", ["gate_up", "down"])
+def test_config3_mlp_projection(proj):
+    c = synth.CONFIG3
+    M, H, F = c["M"], c["hidden"], c["ffn"]
+    K, N = (H, 2 * F) if proj == "gate_up" else (F, H)
+    seed = c["seed"] + (0 if proj == "gate_up" else 1)
+    xh = synth.normal_bf16((M, K), c["x_sigma"], seed, "x")
+    wh = synth.normal_bf16((N, K), c["w_sigma"], seed, "w")
+    gh = synth.normal_bf16((M, N), c["g_sigma"], seed, "g")
+    res, y, dx, dw = dynamic_linear_gpu(dev_bf16(xh), dev_bf16(wh), dev_bf16(gh))
+    check_dynamic_projection(xh, wh, gh, res, y, dx, dw, np.random.default_rng(seed))
+
+
+# ------------------------------------------------------------ workload 4 ---
+
+def test_config4_thd_padding():
+    c = synth.CONFIG4
+    lengths = synth.thd_lengths(c["seed"], c["n_seq"], c["lo"], c["hi"])
+    T = int(lengths.sum())
+    K, N = c["K"], c["N"]
+    xh = synth.normal_bf16((T, K), c["x_sigma"], c["seed"], "x")
+    wh = synth.normal_bf16((N, K), c["w_sigma"], c["seed"], "w")
+    Tp = fp8.fp8_padded_rows(T, c["multiple"])
+    assert Tp % 16 == 0 and Tp - T < 16
+    gh = synth.normal_bf16((Tp, N), c["g_sigma"], c["seed"], "g")
+    gh[T:] = 0  # gradients of pad tokens are zero
+    xp = bf16_out(Tp, K)
+    assert fp8.fp8_pad_tokens(dev_bf16(xh), 16, xp) == Tp
+    res, y, dx, dw = dynamic_linear_gpu(xp, dev_bf16(wh), dev_bf16(gh))
+    # padded rows do not change amax; the scale is the unpadded tensor's
+    assert f32bits(res["x"][3].item()) == f32bits(oracle.amax(xh))
+    # pad rows of the quantised input, of Y and of dX are zero
+    assert not host_u8(res["x"][0][T:]).any()
+    assert not (y[T:].float() != 0).any().item() and not (dx[T:].float() != 0).any().item()
+    xph = np.concatenate([xh, np.zeros((Tp - T, K), np.uint16)])
+    check_dynamic_projection(xph, wh, gh, res, y, dx, dw, np.random.default_rng(4))
+    # dW over the padded batch equals dW over the real tokens (sampled)
+    rng = np.random.default_rng(5)
+    gq = host_u8(res["g"][0])[:T]
+    xq = host_u8(res["x"][0])[:T]
+    ii, jj = sample_entries(rng, N, K, 512, 1)
+    ref = oracle.gemm_entries(oracle.transpose_u8(gq), oracle.transpose_u8(xq),
+                              res["g"][2].item(), res["x"][2].item(), ii, jj)
+    check_gemm(dw.float().cpu().numpy(), ref, ii, jj)
+
+
+# ------------------------------------------------------------ workload 5 ---
+
+def test_config5_block_recipe_full_size():
+    c = synth.CONFIG5
+    M, K, N = c["M"], c["K"], c["N"]
+    rng = np.random.default_rng(c["seed"])
+    xh = synth.normal_with_outliers_bf16((M, K), c["sigma"], c["seed"], "x", p=c["p"], factor=c["factor"])
+    wh = synth.normal_with_outliers_bf16((N, K), c["sigma"], c["seed"], "w", p=c["p"], factor=c["factor"])
+    gh = synth.normal_with_outliers_bf16((M, N), c["sigma"], c["seed"], "g", p=c["p"], factor=c["factor"])
+    x, w, g = dev_bf16(xh), dev_bf16(wh), dev_bf16(gh)
+    # X: 1x128 rows for fprop and 128x1 columns (transposed) for wgrad
+    xq, xqt = u8(M, K), u8(K, M)
+    xs, xsi, xst, xsit = f32(M, K // 128), f32(M, K // 128), f32(K, M // 128), f32(K, M // 128)
+    fp8.fp8_quantize_transpose(x, fp8.BLOCK, xs, xsi, xq, xqt, xst, xsit)
+    wq, wqt = u8(N, K), u8(K, N)
+    ws, wsi = f32(N // 128, K // 128), f32(N // 128, K // 128)
+    fp8.fp8_quantize_transpose(w, fp8.BLOCK_2D, ws, wsi, wq, wqt)
+    gq, gqt = u8(M, N), u8(N, M)
+    gs, gsi, gst, gsit = f32(M, N // 128), f32(M, N // 128), f32(N, M // 128), f32(N, M // 128)
+    fp8.fp8_quantize_transpose(g, fp8.BLOCK, gs, gsi, gq, gqt, gst, gsit)
+    y, dx, dw = bf16_out(M, N), bf16_out(M, K), bf16_out(N, K)
+    fp8.fp8_linear_fprop(xq, xs, wq, ws, M, N, K, fp8.BLOCK, None, y)
+    fp8.fp8_linear_dgrad(gq, gs, wqt, ws, M, N, K, fp8.BLOCK, dx)
+    fp8.fp8_linear_wgrad(gqt, gst, xqt, xst, M, N, K, fp8.BLOCK, dw)
+    fp8.fp8_check_device_status()
+    # quantisers on sampled row / column blocks against the oracle
+    rows = rng.choice(M // 128, 2, replace=False) * 128
+    for r0 in rows:
+        blk = np.ascontiguousarray(xh[r0:r0 + 128])
+        q_ref, s_ref, _ = oracle.quantize_rowtiles(blk, 128)
+        assert np.array_equal(host_u8(xq[r0:r0 + 128]), q_ref)
+        assert np.array_equal(xs[r0:r0 + 128].cpu().numpy(), s_ref)
+        qt_ref, st_ref, _ = oracle.quantize_coltiles_t(blk, 128)
+        assert np.array_equal(host_u8(xqt[:, r0:r0 + 128]), qt_ref)
+        assert np.array_equal(xst[:, r0 // 128].cpu().numpy(), st_ref[:, 0])
+    wq_ref, ws_ref, _ = oracle.quantize_sqtiles(wh, 128)
+    assert np.array_equal(host_u8(wq), wq_ref) and np.array_equal(ws.cpu().numpy(), ws_ref)
+    # GEMMs on sampled entries, with the GPU's (verified) operands
+    xqh, gqh, xqth, gqth = host_u8(xq), host_u8(gq), host_u8(xqt), host_u8(gqt)
+    xsh, gsh, xsth, gsth = xs.cpu().numpy(), gs.cpu().numpy(), xst.cpu().numpy(), gst.cpu().numpy()
+    ii, jj = sample_entries(rng, M, N, 1024, 1)
+    check_gemm(y.float().cpu().numpy(),
+               oracle.gemm_block_entries(xqh, wq_ref, xsh, ws_ref, 128, ii, jj), ii, jj)
+    ii, jj = sample_entries(rng, M, K, 1024, 1)
+    check_gemm(dx.float().cpu().numpy(),
+               oracle.gemm_block_entries(gqh, host_u8(wqt), gsh, np.ascontiguousarray(ws_ref.T),
+                                         128, ii, jj), ii, jj)
+    ii, jj = sample_entries(rng, N, K, 1024, 1)
+    check_gemm(dw.float().cpu().numpy(),
+               oracle.gemm_block_entries(gqth, xqth, gsth, xsth, 1, ii, jj), ii, jj)
