@@ -18,6 +18,8 @@
 // drains its own MMAs and frees its TMEM before returning.
 #include <cuda.h>
 
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -26,13 +28,23 @@ namespace fp8 {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
-constexpr int A_STAGE = BM * BK, B_STAGE = BN * BK, STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int BM = 128, BK = 128;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int GROUP_M = 8;
-constexpr uint32_t IDESC = idesc_f8_f32(BM, BN);
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+
+// Per-N-tile configuration: the B box is BN rows, the ring holds as many
+// stages as fit in shared memory (at most 6).
+template <int BN>
+struct TileCfg {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "N tile");
+    static constexpr int A_STAGE = BM * BK, B_STAGE = BN * BK, STAGE_BYTES = A_STAGE + B_STAGE;
+    static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - 1024 - 256) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr uint32_t IDESC = idesc_f8_f32(BM, BN);
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+};
 
 struct GemmArgs {
     int M, N, K;
@@ -45,23 +57,18 @@ struct GemmArgs {
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &tm, int &tn) {
-    const int group = GROUP_M * n_tiles;
-    const int gid = tile / group;
-    const int first_m = gid * GROUP_M;
-    const int gsz = min(m_tiles - first_m, GROUP_M);
-    const int in = tile - gid * group;
-    tm = first_m + in % gsz;
-    tn = in / gsz;
+    grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
 
+template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_f8_tensor_kernel(const __grid_constant__ CUtensorMap tma_a,
                           const __grid_constant__ CUtensorMap tma_b, const GemmArgs p) {
+    using C = TileCfg<BN>;
+    constexpr int STAGES = C::STAGES, A_STAGE = C::A_STAGE, B_STAGE = C::B_STAGE;
+    constexpr int STAGE_BYTES = C::STAGE_BYTES;
+    constexpr uint32_t IDESC = C::IDESC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -241,6 +248,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    __syncwarp();  // lanes that skipped a role wait here for their warp's lane 0
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -256,16 +264,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
 
-cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
-                               const float *sa, const float *sb, const uint16_t *bias,
-                               uint16_t *D, cudaStream_t s, const char **why) {
+namespace {
+
+template <int BN>
+cudaError_t launch_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                      const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
+                      cudaStream_t s, const char **why) {
+    using C = TileCfg<BN>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_f8_tensor_kernel,
+        cudaError_t e = cudaFuncSetAttribute(gemm_f8_tensor_kernel<BN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
+                                             (int)C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
@@ -287,8 +299,59 @@ cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, in
     args.status = device_status_word();
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
-    gemm_f8_tensor_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, args);
+    gemm_f8_tensor_kernel<BN><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, args);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+// N-tile choice: a tile's time is modelled as proportional to the operand
+// bytes it streams per contraction block, 128*(BM + BN), and the kernel's time
+// as that times the number of waves of tiles over the SMs.  Picks the BN with
+// the lowest modelled time (ties: the larger tile).
+int choose_bn(int64_t M, int64_t N, int sms) {
+    static const int cand[] = {256, 224, 192, 160, 128};
+    int best = 256;
+    double best_cost = 1e30;
+    for (int bn : cand) {
+        const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + sms - 1) / sms;
+        const double cost = (double)waves * (BM + bn);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+// FP8LINEAR_GEMM_BN (256/224/192/160/128) overrides the choice: the tests use
+// it to run every tile shape on the same inputs.
+static int forced_bn() {
+    const char *e = getenv("FP8LINEAR_GEMM_BN");
+    return e ? atoi(e) : 0;
+}
+
+cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                               const float *sa, const float *sb, const uint16_t *bias,
+                               uint16_t *D, cudaStream_t s, const char **why) {
+    const int f = forced_bn();
+    // 2-SM pairs for problems with at least one wave of 256-row tiles;
+    // FP8LINEAR_GEMM_PAIR=0/1 forces the choice (tests run both kernels).
+    const char *pe = getenv("FP8LINEAR_GEMM_PAIR");
+    const int pair_mode = pe ? atoi(pe) : -1;
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    const bool use_pair =
+        pair_mode == 1 || (pair_mode != 0 && M >= 256 && pair_tiles >= num_sms() / 2);
+    if (use_pair) return launch_gemm_pair(A, B, M, N, K, sa, sb, bias, D, f >= 128 ? f : 0, s, why);
+    const int bn = f ? f : choose_bn(M, N, num_sms());
+    switch (bn) {
+    case 224: return launch_bn<224>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    case 192: return launch_bn<192>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    case 160: return launch_bn<160>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    case 128: return launch_bn<128>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    default: return launch_bn<256>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    }
 }
 
 }  // namespace fp8

@@ -44,23 +44,13 @@ struct BlockArgs {
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &tm, int &tn) {
-    const int group = GROUP_M * n_tiles;
-    const int gid = tile / group;
-    const int first_m = gid * GROUP_M;
-    const int gsz = min(m_tiles - first_m, GROUP_M);
-    const int in = tile - gid * group;
-    tm = first_m + in % gsz;
-    tn = in / gsz;
+    grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
 }
 
 __device__ __forceinline__ void epi_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
 
 template <bool kPerRowB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -263,6 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    __syncwarp();  // lanes that skipped a role wait here for their warp's lane 0
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

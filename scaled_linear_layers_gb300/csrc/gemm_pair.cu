@@ -1,0 +1,330 @@
+// Scaled FP8 GEMM with 2-SM MMAs (tcgen05 cta_group::2) for large problems.
+//
+//   D[M,N] = bf16( s_A * s_B * sum_k A[m,k] * B[n,k] (+ bias[n]) )
+//
+// A cluster of two CTAs on neighbouring SMs owns a 256 x BN output tile.  CTA
+// r (0 = leader, 1 = peer) loads rows r*128..+127 of the tile's A panel and
+// rows r*BN/2..+BN/2-1 of its B panel into its own shared memory; one thread
+// of the leader issues M=256 x N=BN x K=32 MMAs that read both CTAs' shared
+// memory and write rows 0..127 of the accumulator to the leader's TMEM and
+// rows 128..255 to the peer's.  Each SM therefore streams 128 x (128 + BN/2)
+// operand bytes per 128-deep contraction block instead of 128 x (128 + BN),
+// which is what limits the one-CTA kernel.
+//
+// Synchronisation: both CTAs' TMA loads complete on the leader's `full`
+// barrier (which expects the bytes of both); the leader's MMA commits arrive
+// on `empty` and `tfull` in both CTAs at once (multicast); both CTAs'
+// epilogue warps arrive on the leader's `tempty`.  Every wait is bounded; the
+// CTAs of a pair meet at cluster barriers after set-up and before teardown.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tmap.h"
+
+namespace fp8 {
+
+extern uint64_t g_wait_limit_ns;
+
+namespace {
+
+constexpr int BK = 128;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int GROUP_M = 4;  // 4 pair-rows of 256 = 1024 rows per raster group
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+
+template <int BN>
+struct PairCfg {
+    static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "N tile");
+    static constexpr int BNH = BN / 2;  // B rows held by each CTA
+    static constexpr int A_STAGE = 128 * BK, B_STAGE = BNH * BK;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;  // per CTA
+    static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - 1024 - 256) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr uint32_t IDESC = idesc_f8_f32(256, BN);
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+};
+
+struct PairArgs {
+    int M, N, K;
+    const float *sa, *sb;
+    const uint16_t *bias;
+    uint16_t *d;
+    int64_t ldd;
+    uint64_t wait_limit_ns;
+    unsigned int *status;
+};
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_f8_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
+                        const __grid_constant__ CUtensorMap tma_b, const PairArgs p) {
+    using C = PairCfg<BN>;
+    constexpr int STAGES = C::STAGES, A_STAGE = C::A_STAGE, B_STAGE = C::B_STAGE;
+    constexpr int BNH = C::BNH;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_STAGE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t *full = bars;                // [STAGES] (leader's counts both CTAs' bytes)
+    uint64_t *empty = bars + STAGES;      // [STAGES]
+    uint64_t *tfull = bars + 2 * STAGES;  // [2]
+    uint64_t *tempty = tfull + 2;         // [2] (leader's counts 8 epilogue warps)
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int m_tiles = (p.M + 255) / 256, n_tiles = (p.N + BN - 1) / BN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int nk = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // barriers of both CTAs initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                int tm, tn;
+                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+                const int arow = tm * 256 + (int)rank * 128;
+                const int brow = tn * BN + (int)rank * BNH;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns,
+                                           kStatusTimeoutTma, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                    const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
+                    tma_load_2d_pair(sA + stage * A_STAGE, &tma_a, leader_full, kb * BK, arow);
+                    tma_load_2d_pair(sB + stage * B_STAGE, &tma_b, leader_full, kb * BK, brow);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && rank == 0) {
+                // the leader's `full` barriers count both CTAs' copies: wait
+                // (bounded) for the last STAGES issues to land before teardown
+                for (int s = 0; s < STAGES; ++s) {
+                    stage = stage == 0 ? STAGES - 1 : stage - 1;
+                    if (stage == STAGES - 1) phase ^= 1u;
+                    volatile int no_abort = 0;
+                    mbar_wait_bounded(&full[stage], phase, &no_abort, 10000000ull,
+                                      kStatusTimeoutTma, p.status);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------- MMA issuer (leader)
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p.wait_limit_ns,
+                                       kStatusTimeoutMma, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.wait_limit_ns,
+                                           kStatusTimeoutMma, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
+                    const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_f8_pair(d_tmem, smem_desc_sw128(a0 + 32 * k),
+                                    smem_desc_sw128(b0 + 32 * k), C::IDESC, (kb | k) != 0);
+                    mma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) mma_commit_pair(&tfull[acc], 0x3);
+            }
+            mma_commit_pair(drain, 0x1);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(drain, 0, &no_abort, p.wait_limit_ns, kStatusTimeoutMma, p.status);
+        }
+    } else {
+        // ---------------------------------------------- epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const float s = __fmul_rn(*p.sa, *p.sb);
+        int it = 0;
+        for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            const bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.wait_limit_ns,
+                                              kStatusTimeoutEpilogue, p.status);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            int tm, tn;
+            grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+            const int row = tm * 256 + (int)rank * 128 + quarter * 32 + lane;
+            uint16_t *drow = p.d + (int64_t)row * p.ldd;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                       (uint32_t)(acc * BN + c * 32),
+                                   r);
+                tmem_ld_wait();
+                const int col = tn * BN + c * 32;
+                if (row < p.M && col < p.N) {
+                    uint32_t packed[16];
+                    if (p.bias != nullptr) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float b0 = __uint_as_float((uint32_t)p.bias[col + 2 * j] << 16);
+                            const float b1 =
+                                __uint_as_float((uint32_t)p.bias[col + 2 * j + 1] << 16);
+                            packed[j] =
+                                pack_bf16x2(__fadd_rn(__fmul_rn(__uint_as_float(r[2 * j]), s), b0),
+                                            __fadd_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), s), b1));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            packed[j] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * j]), s),
+                                                    __fmul_rn(__uint_as_float(r[2 * j + 1]), s));
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(drow + col);
+                    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    if (col + 16 < p.N) {
+                        dst[2] = make_uint4(packed[8], packed[9], packed[10], packed[11]);
+                        dst[3] = make_uint4(packed[12], packed[13], packed[14], packed[15]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        }
+    }
+
+    __syncwarp();  // lanes that skipped a role wait here for their warp's lane 0
+    tc_fence_before();
+    cluster_sync_all();  // the peer's smem/TMEM stay alive until the leader's MMAs drained
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int BN>
+cudaError_t launch_pair_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                           const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
+                           cudaStream_t s, const char **why) {
+    using C = PairCfg<BN>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_f8_pair_kernel<BN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    CUtensorMap ta, tb;
+    if (!make_tmap_k128(&ta, A, M, K, 128) || !make_tmap_k128(&tb, B, N, K, C::BNH)) {
+        *why = "cuTensorMapEncodeTiled failed";
+        return cudaErrorInvalidValue;
+    }
+    PairArgs args;
+    args.M = (int)M;
+    args.N = (int)N;
+    args.K = (int)K;
+    args.sa = sa;
+    args.sb = sb;
+    args.bias = bias;
+    args.d = D;
+    args.ldd = N;
+    args.wait_limit_ns = g_wait_limit_ns;
+    args.status = device_status_word();
+    const int64_t tiles = ((M + 255) / 256) * ((N + BN - 1) / BN);
+    const int64_t pairs = num_sms() / 2;
+    const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
+    gemm_f8_pair_kernel<BN><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Same cost model as the one-CTA chooser, per SM of a pair: waves of 256 x BN
+// tiles over the pairs times the bytes each SM streams per block, 128 + BN/2.
+int choose_pair_bn(int64_t M, int64_t N, int pairs) {
+    static const int cand[] = {256, 224, 192, 160, 128};
+    int best = 256;
+    double best_cost = 1e30;
+    for (int bn : cand) {
+        const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + pairs - 1) / pairs;
+        const double cost = (double)waves * (128 + bn / 2);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+cudaError_t launch_gemm_pair(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                             const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
+                             int bn, cudaStream_t s, const char **why) {
+    switch (bn ? bn : choose_pair_bn(M, N, num_sms() / 2)) {
+    case 224: return launch_pair_bn<224>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    case 192: return launch_pair_bn<192>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    case 160: return launch_pair_bn<160>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    case 128: return launch_pair_bn<128>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    default: return launch_pair_bn<256>(A, B, M, N, K, sa, sb, bias, D, s, why);
+    }
+}
+
+}  // namespace fp8

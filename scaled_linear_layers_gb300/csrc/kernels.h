@@ -34,6 +34,12 @@ cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, in
                                const float *sa, const float *sb, const uint16_t *bias,
                                uint16_t *D, cudaStream_t s, const char **why);
 
+// The 2-SM (CTA pair) kernel behind launch_gemm_tensor for large problems;
+// bn = 0 lets it choose the N tile.
+cudaError_t launch_gemm_pair(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                             const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
+                             int bn, cudaStream_t s, const char **why);
+
 // Block-scaled variant: the contraction is split into 128-blocks; A's block
 // scales are sa[i * sa_ld + kb]; B's are sb[(j / b_rows_per_scale) *
 // sb_row_stride + kb * sb_k_stride].

@@ -64,6 +64,50 @@ def test_gemm_random_codes_within_tolerance(shape, which):
     assert np.max(np.abs(got - ref) / (bound + 1e-30)) < 1e-2
 
 
+@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
+@pytest.mark.parametrize("which", ["fprop", "wgrad"])
+def test_gemm_every_tile_width(bn, which, monkeypatch):
+    """Each N-tile variant of the one-CTA kernel on shapes with ragged M/N/K tails."""
+    monkeypatch.setenv("FP8LINEAR_GEMM_PAIR", "0")
+    monkeypatch.setenv("FP8LINEAR_GEMM_BN", str(bn))
+    rng = np.random.default_rng(bn)
+    for M, N, K in [(400, 1008, 272), (128, 224, 128), (1152, 480, 640)]:
+        A = random_codes(rng, (M, K))
+        B = random_codes(rng, (N, K))
+        got = run_tensor_gemm(A, B, 0.05, 0.002, which=which)
+        _, ref, bound = oracle.gemm(A, B, np.float32(0.05), np.float32(0.002))
+        ok = oracle.gemm_tolerance_ok(got, ref, bound)
+        assert ok.all(), f"BN={bn} {(M, N, K)}: {(~ok).sum()} bad"
+
+
+@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
+@pytest.mark.parametrize("which", ["fprop", "dgrad", "wgrad"])
+def test_gemm_pair_kernel_every_tile_width(bn, which, monkeypatch):
+    """The 2-SM (CTA pair) kernel, forced on, on shapes with ragged tails,
+    including M smaller than the pair's 256 rows and a single-pair grid."""
+    monkeypatch.setenv("FP8LINEAR_GEMM_PAIR", "1")
+    monkeypatch.setenv("FP8LINEAR_GEMM_BN", str(bn))
+    rng = np.random.default_rng(bn + 7)
+    for M, N, K in [(400, 1008, 272), (128, 224, 128), (1152, 480, 640), (2048, 2048, 1024)]:
+        A = random_codes(rng, (M, K))
+        B = random_codes(rng, (N, K))
+        got = run_tensor_gemm(A, B, 0.05, 0.002, which=which)
+        _, ref, bound = oracle.gemm(A, B, np.float32(0.05), np.float32(0.002))
+        ok = oracle.gemm_tolerance_ok(got, ref, bound)
+        assert ok.all(), f"pair BN={bn} {(M, N, K)}: {(~ok).sum()} bad"
+
+
+def test_gemm_pair_kernel_bias(monkeypatch):
+    monkeypatch.setenv("FP8LINEAR_GEMM_PAIR", "1")
+    rng = np.random.default_rng(3)
+    A = random_codes(rng, (512, 512))
+    B = random_codes(rng, (384, 512))
+    bias = synth.normal_bf16((384,), 1.0, seed=4, tensor="bias")
+    got = run_tensor_gemm(A, B, 0.01, 0.02, bias=bias)
+    _, ref, bound = oracle.gemm(A, B, np.float32(0.01), np.float32(0.02), bias)
+    assert oracle.gemm_tolerance_ok(got, ref, bound).all()
+
+
 def test_gemm_exact_on_integer_operands():
     """Values in -16..16 with K=256: every partial sum is an integer below
     2^16, exact in fp32, and the results fit bf16's 8 bits only when small;
@@ -89,10 +133,12 @@ def test_gemm_bias():
     assert oracle.gemm_tolerance_ok(got, ref, bound).all()
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (16384, 4096, 4096)])
-def test_gemm_full_size_sampled(shape):
+def test_gemm_full_size_sampled(shape, pair, monkeypatch):
     """Full-size GEMM in the benchmark's launch configuration; 4096 sampled
-    entries plus 4 whole row panels against the oracle."""
+    entries plus 4 whole row panels against the oracle, for both kernels."""
+    monkeypatch.setenv("FP8LINEAR_GEMM_PAIR", pair)
     M, N, K = shape
     rng = np.random.default_rng(M + K)
     x = synth.normal_bf16((M, K), 1.0, seed=1, tensor="x")
