@@ -133,80 +133,55 @@ class ClockSampler:
 
 # --------------------------------------------------------------- GPU arm ---
 
+SEGMENTS = ["quant_x_fwd", "quant_t_w", "gemm_fprop", "meta_fwd", "quant_t_g", "quant_t_x_bwd",
+            "gemm_dgrad", "gemm_wgrad", "meta_bwd"]
+
+
 class Step:
-    """Device buffers and the C-ABI call sequence of one delayed-scaling step."""
+    """One delayed-scaling training step = one native call
+    (fp8_linear_step_delayed), with optional per-segment events."""
 
     def __init__(self, fp8, torch, dev, x_sets, g_sets, w):
-        self.fp8, self.torch, self.dev = fp8, torch, dev
-        u8 = dict(dtype=torch.uint8, device=dev)
-        bf = dict(dtype=torch.bfloat16, device=dev)
-        f32 = dict(dtype=torch.float32, device=dev)
+        self.fp8, self.torch = fp8, torch
         self.x_sets, self.g_sets, self.w = x_sets, g_sets, w
-        self.xq = torch.empty((M, K), **u8)
-        self.xqt = torch.empty((K, M), **u8)
-        self.wq = torch.empty((N, K), **u8)
-        self.wqt = torch.empty((K, N), **u8)
-        self.gq = torch.empty((M, N), **u8)
-        self.gqt = torch.empty((N, M), **u8)
-        self.y = torch.empty((M, N), **bf)
-        self.dx = torch.empty((M, K), **bf)
-        self.dw = torch.empty((N, K), **bf)
-        self.amax = torch.zeros(4, **f32)
+        self.io = fp8.LinearStep(M, N, K, device=dev)
         self.meta = fp8.Fp8Meta(16, device=dev)
         self.count = [0]
         self.launches = 0
-        self.events = None
+        self.events = None  # per-step event lists of the timed region
+        self.pool = []      # events created (and recorded once) ahead of it
 
-    def _ev(self, name):
-        if self.events is not None:
-            e = self.torch.cuda.Event(enable_timing=True)
-            e.record()
-            self.events.append((name, e))
+    def prepare_events(self, steps):
+        """Create the timed region's events up front so the region itself
+        only passes their handles to the native call."""
+        self.pool = []
+        for _ in range(steps):
+            ev = [self.torch.cuda.Event(enable_timing=True) for _ in range(len(SEGMENTS) + 1)]
+            for e in ev:
+                e.record()
+            self.pool.append(ev)
+        self.pool.reverse()
+        self.events = []
 
     def run(self, t, x=None, g=None):
-        fp8, m = self.fp8, self.meta
         x = self.x_sets[t % len(self.x_sets)] if x is None else x
         g = self.g_sets[t % len(self.g_sets)] if g is None else g
-        a_x, a_w, a_g = self.amax[0:1], self.amax[1:2], self.amax[2:3]
-        before = self.count[0]
-        fp8.fp8_state_step(self.count, 16, [m])
-        refreshed = self.count[0] % 16 == 0
-        self._ev("quant_x_fwd")
-        fp8.fp8_quantize(x, fp8.DELAYED, None, m.x_scale_inv, self.xq, a_x)
-        self._ev("quant_t_w")
-        fp8.fp8_quantize_transpose(self.w, fp8.DELAYED, None, m.scale_inv, self.wq, self.wqt,
-                                   amax_out=a_w)
-        self._ev("gemm_fprop")
-        fp8.fp8_linear_fprop(self.xq, m.x_scale, self.wq, m.scale, M, N, K, fp8.DELAYED, None,
-                             self.y)
-        self._ev("meta")
-        fp8.fp8_meta_record(m, fp8.SLOT_W, a_w)
-        fp8.fp8_meta_record(m, fp8.SLOT_X, a_x)
-        self._ev("quant_t_g")
-        fp8.fp8_quantize_transpose(g, fp8.DELAYED, None, m.g_scale_inv, self.gq, self.gqt,
-                                   amax_out=a_g)
-        self._ev("quant_t_x_bwd")
-        fp8.fp8_quantize_transpose(x, fp8.DELAYED, None, m.x_scale_inv, None, self.xqt)
-        self._ev("gemm_dgrad")
-        fp8.fp8_linear_dgrad(self.gq, m.g_scale, self.wqt, m.scale, M, N, K, fp8.DELAYED, self.dx)
-        self._ev("gemm_wgrad")
-        fp8.fp8_linear_wgrad(self.gqt, m.g_scale, self.xqt, m.x_scale, M, N, K, fp8.DELAYED,
-                             self.dw)
-        self._ev("meta")
-        fp8.fp8_meta_record(m, fp8.SLOT_G, a_g)
-        self._ev("end")
-        # kernels: 4 quantisers + 3 GEMMs + 3 meta updates (+1 refresh)
-        self.launches += 10 + (1 if refreshed else 0)
-        assert self.count[0] == before + 1
+        self.io.set_inputs(x, self.w, g)
+        ev = None
+        if self.events is not None and self.pool:
+            ev = self.pool.pop()
+            self.events.append(ev)
+        self.fp8.fp8_linear_step_delayed(self.meta, self.count, self.io, events=ev)
+        # kernels: 4 quantisers + 3 GEMMs + 3 state updates (+1 refresh)
+        self.launches += 10 + (1 if self.count[0] % 16 == 0 else 0)
 
 
-def kernel_times(events):
-    """Average ms per launch of each named segment, from consecutive events."""
-    acc = {}
-    for (name, e0), (_, e1) in zip(events, events[1:]):
-        if name == "end":
-            continue
-        acc.setdefault(name, []).append(e0.elapsed_time(e1))
+def kernel_times(steps_events):
+    """Average ms per launch of each segment over the timed steps."""
+    acc = {k: [] for k in SEGMENTS}
+    for ev in steps_events:
+        for i, name in enumerate(SEGMENTS):
+            acc[name].append(ev[i].elapsed_time(ev[i + 1]))
     return {k: sum(v) / len(v) for k, v in acc.items()}
 
 
@@ -243,8 +218,9 @@ def gpu_arm(args, rank, world):
     barrier()
 
     # --- device-resident timed region
+    step.prepare_events(args.steps)
+    torch.cuda.synchronize()
     step.launches = 0
-    step.events = []
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -281,9 +257,9 @@ def gpu_arm(args, rank, world):
         x_buf.copy_(xp[t % 4], non_blocking=True)
         g_buf.copy_(gp[t % 4], non_blocking=True)
         step.run(t, x_buf, g_buf)
-        outs[0].copy_(step.y, non_blocking=True)
-        outs[1].copy_(step.dx, non_blocking=True)
-        outs[2].copy_(step.dw, non_blocking=True)
+        outs[0].copy_(step.io.y, non_blocking=True)
+        outs[1].copy_(step.io.dx, non_blocking=True)
+        outs[2].copy_(step.io.dw, non_blocking=True)
     e1.record()
     barrier()
     ms_e2e = e0.elapsed_time(e1)

@@ -195,6 +195,52 @@ fp8_status fp8_state_step(int64_t *step_count, int32_t interval, fp8_meta *metas
                           cudaStream_t s);
 
 /* ------------------------------------------------------------------------ */
+/* One training step of one linear, delayed scaling (composite)              */
+/* ------------------------------------------------------------------------ */
+/* Caller-owned device buffers of one step.  x, w, y, xq, wq, wqt, amax are
+ * required; g, gq, gqt, xqt, dx, dw may all be NULL for a forward-only step;
+ * bias is optional. */
+typedef struct {
+    const uint16_t *x;    /* [M,K] bf16 activations (input)                   */
+    const uint16_t *w;    /* [N,K] bf16 weight (input)                        */
+    const uint16_t *g;    /* [M,N] bf16 upstream gradient (input, nullable)   */
+    const uint16_t *bias; /* [N] bf16 (input, nullable)                       */
+    uint8_t *xq;          /* [M,K] e4m3, X with the lagged x scale            */
+    uint8_t *xqt;         /* [K,M] e4m3, Xᵀ with the x scale of this step     */
+    uint8_t *wq;          /* [N,K] e4m3                                       */
+    uint8_t *wqt;         /* [K,N] e4m3                                       */
+    uint8_t *gq;          /* [M,N] e4m3                                       */
+    uint8_t *gqt;         /* [N,M] e4m3                                       */
+    float *amax;          /* [3] amax of x, w, g of this step (output)        */
+    uint16_t *y;          /* [M,N] bf16 output                                */
+    uint16_t *dx;         /* [M,K] bf16 input gradient (nullable)             */
+    uint16_t *dw;         /* [N,K] bf16 weight gradient, overwritten (nullable) */
+} fp8_linear_step_io;
+
+/* Number of events fp8_linear_step_delayed records when given an array. */
+#define FP8_STEP_NEVENTS 10
+
+/* The AstrAI page's training step for one linear (fp8_autocast entry, then
+ * fp8_linear_forward, then fp8_linear_backward), as one call that enqueues
+ * every kernel on `s`:
+ *   fp8_state_step (refresh every m->interval steps);
+ *   X -> xq with x_scale_inv (amax[0]); W -> wq, wqt with scale_inv (amax[1]);
+ *   y = fprop(xq, x_scale, wq, scale, bias);
+ *   record amax[1] in the history; lag-update the x scale from amax[0];
+ *   if g: G -> gq, gqt with g_scale_inv (amax[2]); X -> xqt with the updated
+ *   x_scale_inv; dx = dgrad(gq, g_scale, wqt, scale); dw = wgrad(gqt,
+ *   g_scale, xqt, x_scale); lag-update the g scale from amax[2].
+ * The backward reuses the forward's Wqᵀ: the page quantises w again with the
+ * same scale_inv, which gives the same bytes.  `events` (nullable) receives
+ * FP8_STEP_NEVENTS cudaEventRecord calls at the segment boundaries (before
+ * each of: X, W, fprop, forward state update, G, Xᵀ, dgrad, wgrad, backward
+ * state update; and at the end).  Argument checks as for the single calls;
+ * the first failing call's status is returned and later work is not enqueued. */
+fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_linear_step_io *io,
+                                   int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
+                                   cudaStream_t s);
+
+/* ------------------------------------------------------------------------ */
 /* Token padding                                                             */
 /* ------------------------------------------------------------------------ */
 

@@ -24,6 +24,7 @@ __all__ = [
     "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_meta_init", "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
+    "fp8_linear_step_delayed", "LinearStep",
     "Fp8Error", "DELAYED", "DYNAMIC", "BLOCK", "BLOCK_2D", "SLOT_W", "SLOT_X", "SLOT_G",
     "library_path",
 ]
@@ -169,6 +170,56 @@ def fp8_state_step(step_count: list, interval: int, metas, stream=None):
     step_count[0] = cnt.value
     for i, m in enumerate(metas):
         m.c = arr[i]
+
+
+class LinearStep:
+    """Buffers of fp8_linear_step_delayed for one linear: the C io struct
+    built once from torch tensors (the caller keeps them alive), so a step
+    is a single C call.  ``set_inputs`` swaps the x / g / w pointers."""
+
+    def __init__(self, M, N, K, device="cuda", backward=True, bias=None):
+        u8 = dict(dtype=torch.uint8, device=device)
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.M, self.N, self.K = M, N, K
+        self.xq, self.wq, self.wqt = (torch.empty((M, K), **u8), torch.empty((N, K), **u8),
+                                      torch.empty((K, N), **u8))
+        self.amax = torch.zeros(3, dtype=torch.float32, device=device)
+        self.y = torch.empty((M, N), **bf)
+        self.bias = bias
+        if backward:
+            self.xqt, self.gq, self.gqt = (torch.empty((K, M), **u8), torch.empty((M, N), **u8),
+                                           torch.empty((N, M), **u8))
+            self.dx, self.dw = torch.empty((M, K), **bf), torch.empty((N, K), **bf)
+        else:
+            self.xqt = self.gq = self.gqt = self.dx = self.dw = None
+        self.io = _lib.fp8_linear_step_io()
+        for name in ("xq", "xqt", "wq", "wqt", "gq", "gqt", "amax", "y", "dx", "dw", "bias"):
+            t = getattr(self, name)
+            setattr(self.io, name, None if t is None else t.data_ptr())
+
+    def set_inputs(self, x, w, g=None):
+        for t in (x, w) + ((g,) if g is not None else ()):
+            _bf16(t)
+        assert tuple(x.shape) == (self.M, self.K) and tuple(w.shape) == (self.N, self.K)
+        self.io.x, self.io.w = x.data_ptr(), w.data_ptr()
+        if g is not None:
+            assert tuple(g.shape) == (self.M, self.N) and self.gq is not None
+        self.io.g = None if g is None else g.data_ptr()
+
+
+def fp8_linear_step_delayed(meta: Fp8Meta, step_count: list, step: LinearStep, events=None,
+                            stream=None):
+    """One delayed-scaling training step (see the C header).  ``events`` is
+    None or a list of FP8_STEP_NEVENTS recorded torch.cuda.Event objects."""
+    cnt = ctypes.c_int64(step_count[0])
+    ev = None
+    if events is not None:
+        arr = (ctypes.c_void_p * _lib.FP8_STEP_NEVENTS)(*[e.cuda_event for e in events])
+        ev = ctypes.cast(arr, ctypes.c_void_p)
+    _check(_LIB.fp8_linear_step_delayed(ctypes.byref(meta.c), ctypes.byref(cnt),
+                                        ctypes.byref(step.io), step.M, step.N, step.K, ev,
+                                        _stream(stream)))
+    step_count[0] = cnt.value
 
 
 def fp8_padded_rows(rows: int, multiple: int = 16) -> int:

@@ -35,6 +35,14 @@ class fp8_meta(ctypes.Structure):
     _fields_ = [("dev", ctypes.c_void_p), ("interval", ctypes.c_int32), ("idx", ctypes.c_int32)]
 
 
+class fp8_linear_step_io(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("x", "w", "g", "bias", "xq", "xqt", "wq", "wqt", "gq", "gqt", "amax", "y", "dx",
+                 "dw")]
+
+
+FP8_STEP_NEVENTS = 10
+
 P, I64, I32, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
 S = ctypes.c_int  # fp8_status / enums
 
@@ -49,6 +57,8 @@ SIGNATURES = {
     "fp8_meta_record": (S, [ctypes.POINTER(fp8_meta), S, P, P]),
     "fp8_meta_refresh": (S, [ctypes.POINTER(fp8_meta), P]),
     "fp8_state_step": (S, [ctypes.POINTER(I64), I32, ctypes.POINTER(fp8_meta), I32, P]),
+    "fp8_linear_step_delayed": (S, [ctypes.POINTER(fp8_meta), ctypes.POINTER(I64),
+                                    ctypes.POINTER(fp8_linear_step_io), I64, I64, I64, P, P]),
     "fp8_padded_rows": (I64, [I64, I64]),
     "fp8_pad_tokens": (S, [P, I64, I64, I64, P, ctypes.POINTER(I64), P]),
     "fp8_check_device_status": (S, [P]),

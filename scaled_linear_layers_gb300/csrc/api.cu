@@ -352,6 +352,64 @@ fp8_status fp8_state_step(int64_t *step_count, int32_t interval, fp8_meta *metas
     return FP8_OK;
 }
 
+fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_linear_step_io *io,
+                                   int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
+                                   cudaStream_t s) {
+    const char *who = "fp8_linear_step_delayed";
+    FP8_NEED(m, who);
+    FP8_NEED(m->dev, who);
+    FP8_NEED(step_count, who);
+    FP8_NEED(io, who);
+    FP8_NEED(io->amax, who);
+    const bool bwd = io->g != nullptr;
+    if (bwd) {
+        FP8_NEED(io->gq, who);
+        FP8_NEED(io->gqt, who);
+        FP8_NEED(io->xqt, who);
+    }
+    int ev = 0;
+    auto mark = [&]() -> fp8_status {
+        if (events == nullptr) return FP8_OK;
+        return cuda_status(cudaEventRecord(events[ev++], s), who);
+    };
+    float *d = m->dev;
+    FP8_TRY(fp8_state_step(step_count, m->interval, m, 1, s));
+    FP8_TRY(mark());
+    FP8_TRY(fp8_quantize(io->x, M, K, FP8_RECIPE_DELAYED, nullptr, d + FP8_META_X_SCALE_INV, io->xq,
+                         io->amax + 0, s));
+    FP8_TRY(mark());
+    FP8_TRY(fp8_quantize_transpose(io->w, N, K, FP8_RECIPE_DELAYED, nullptr, d + FP8_META_SCALE_INV,
+                                   io->wq, io->wqt, nullptr, nullptr, io->amax + 1, s));
+    FP8_TRY(mark());
+    FP8_TRY(fp8_linear_fprop(io->xq, d + FP8_META_X_SCALE, io->wq, d + FP8_META_SCALE, M, N, K,
+                             FP8_RECIPE_DELAYED, io->bias, io->y, s));
+    FP8_TRY(mark());
+    FP8_TRY(fp8_meta_record(m, FP8_SLOT_W, io->amax + 1, s));
+    FP8_TRY(fp8_meta_record(m, FP8_SLOT_X, io->amax + 0, s));
+    if (bwd) {
+        FP8_TRY(mark());
+        FP8_TRY(fp8_quantize_transpose(io->g, M, N, FP8_RECIPE_DELAYED, nullptr,
+                                       d + FP8_META_G_SCALE_INV, io->gq, io->gqt, nullptr, nullptr,
+                                       io->amax + 2, s));
+        FP8_TRY(mark());
+        FP8_TRY(fp8_quantize_transpose(io->x, M, K, FP8_RECIPE_DELAYED, nullptr,
+                                       d + FP8_META_X_SCALE_INV, nullptr, io->xqt, nullptr, nullptr,
+                                       nullptr, s));
+        FP8_TRY(mark());
+        if (io->dx != nullptr)
+            FP8_TRY(fp8_linear_dgrad(io->gq, d + FP8_META_G_SCALE, io->wqt, d + FP8_META_SCALE, M,
+                                     N, K, FP8_RECIPE_DELAYED, io->dx, s));
+        FP8_TRY(mark());
+        if (io->dw != nullptr)
+            FP8_TRY(fp8_linear_wgrad(io->gqt, d + FP8_META_G_SCALE, io->xqt, d + FP8_META_X_SCALE,
+                                     M, N, K, FP8_RECIPE_DELAYED, io->dw, s));
+        FP8_TRY(mark());
+        FP8_TRY(fp8_meta_record(m, FP8_SLOT_G, io->amax + 2, s));
+    }
+    while (events != nullptr && ev < FP8_STEP_NEVENTS) FP8_TRY(mark());
+    return FP8_OK;
+}
+
 int64_t fp8_padded_rows(int64_t rows, int64_t multiple) {
     if (rows < 0 || multiple < 1) return -1;
     return (rows + multiple - 1) / multiple * multiple;

@@ -28,17 +28,23 @@ extern uint64_t g_wait_limit_ns;
 
 namespace {
 
-constexpr int BK = 128;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int GROUP_M = 4;  // 4 pair-rows of 256 = 1024 rows per raster group
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
+// A stage holds KSUB 128-byte-wide boxes of each operand (contraction depth
+// 128*KSUB): narrower N tiles take two boxes per stage so each barrier round
+// trip covers 8 MMAs (measured: +7% at 4096^3 for N=224, a loss at N=256
+// where only three 64 KB stages would fit).
 template <int BN>
 struct PairCfg {
     static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "N tile");
+    static constexpr int KSUB = BN < 256 ? 2 : 1;
+    static constexpr int BK = 128 * KSUB;
     static constexpr int BNH = BN / 2;  // B rows held by each CTA
-    static constexpr int A_STAGE = 128 * BK, B_STAGE = BNH * BK;
+    static constexpr int A_SUB = 128 * 128, B_SUB = BNH * 128;  // one 128-byte box
+    static constexpr int A_STAGE = A_SUB * KSUB, B_STAGE = B_SUB * KSUB;
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;  // per CTA
     static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - 1024 - 256) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
@@ -62,7 +68,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tma_b, const PairArgs p) {
     using C = PairCfg<BN>;
     constexpr int STAGES = C::STAGES, A_STAGE = C::A_STAGE, B_STAGE = C::B_STAGE;
-    constexpr int BNH = C::BNH;
+    constexpr int BNH = C::BNH, BK = C::BK, KSUB = C::KSUB;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -128,8 +134,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     }
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
                     const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(sA + stage * A_STAGE, &tma_a, leader_full, kb * BK, arow);
-                    tma_load_2d_pair(sB + stage * B_STAGE, &tma_b, leader_full, kb * BK, brow);
+#pragma unroll
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        tma_load_2d_pair(sA + stage * A_STAGE + ks * C::A_SUB, &tma_a, leader_full,
+                                         kb * BK + 128 * ks, arow);
+                        tma_load_2d_pair(sB + stage * B_STAGE + ks * C::B_SUB, &tma_b, leader_full,
+                                         kb * BK + 128 * ks, brow);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -175,9 +186,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
                     const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        mma_f8_pair(d_tmem, smem_desc_sw128(a0 + 32 * k),
-                                    smem_desc_sw128(b0 + 32 * k), C::IDESC, (kb | k) != 0);
+                    for (int ks = 0; ks < KSUB; ++ks)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_f8_pair(d_tmem, smem_desc_sw128(a0 + ks * C::A_SUB + 32 * k),
+                                        smem_desc_sw128(b0 + ks * C::B_SUB + 32 * k), C::IDESC,
+                                        (kb | ks | k) != 0);
                     mma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) {
                         stage = 0;

@@ -166,6 +166,68 @@ def test_config2_delayed_full_size_first_steps():
     run_delayed(4096, 4096, 4096, steps=2, full_gemm=False)
 
 
+def test_composite_step_matches_oracle_20_steps():
+    """fp8_linear_step_delayed (one native call per training step) against
+    the oracle's state machine: all 20 steps at 256x384x512, full compare."""
+    c = synth.CONFIG2
+    M, N, K = 256, 384, 512
+    w = synth.normal_bf16((N, K), c["w_sigma"], 7, "w")
+    wd = dev_bf16(w)
+    step = fp8.LinearStep(M, N, K)
+    meta = fp8.Fp8Meta(16)
+    count = [0]
+    st = ost.State(16)
+    om = st.new_meta()
+    for t in range(20):
+        x = synth.normal_bf16((M, K), c["x_sigma"], 7, "x", t)
+        g = synth.normal_bf16((M, N), c["g_sigma"], 7, "g", t)
+        xd, gd = dev_bf16(x), dev_bf16(g)
+        step.set_inputs(xd, wd, gd)
+        fp8.fp8_linear_step_delayed(meta, count, step)
+        fp8.fp8_check_device_status()
+        ref = ost.delayed_training_step(st, om, x, w, g)
+        f, b = ref["fwd"], ref["bwd"]
+        assert count[0] == st.step_count == t + 1
+        assert np.array_equal(host_u8(step.xq), f["xq"]) and np.array_equal(host_u8(step.wq), f["wq"])
+        assert np.array_equal(host_u8(step.wqt), f["wq"].T)
+        assert np.array_equal(host_u8(step.gq), b["gq"]) and np.array_equal(host_u8(step.gqt), b["gq"].T)
+        assert np.array_equal(host_u8(step.xqt), b["xq_bwd"].T)
+        am = step.amax.cpu().numpy()
+        assert [f32bits(v) for v in am] == [f32bits(f["amax_x"]), f32bits(f["amax_w"]),
+                                            f32bits(b["amax_g"])]
+        blk = meta.block.cpu().numpy()
+        snap = ref["meta"]
+        assert np.array_equal(blk[8:].view(np.uint32), snap["amax_history"].view(np.uint32))
+        for k, i in (("scale", 0), ("scale_inv", 1), ("x_scale", 2), ("x_scale_inv", 3),
+                     ("g_scale", 4), ("g_scale_inv", 5)):
+            assert f32bits(blk[i]) == f32bits(snap[k]), (t, k)
+        check_gemm(step.y.float().cpu().numpy(), f["y"])
+        check_gemm(step.dx.float().cpu().numpy(), b["dx"])
+        check_gemm(step.dw.float().cpu().numpy(), b["dw"])
+
+
+def test_composite_step_forward_only_and_events():
+    M, N, K = 128, 256, 128
+    x = synth.normal_bf16((M, K), 1.0, 8, "x")
+    w = synth.normal_bf16((N, K), 0.02, 8, "w")
+    step = fp8.LinearStep(M, N, K, backward=False)
+    meta = fp8.Fp8Meta(16)
+    count = [0]
+    step.set_inputs(dev_bf16(x), dev_bf16(w))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    for e in ev:
+        e.record()
+    fp8.fp8_linear_step_delayed(meta, count, step, events=ev)
+    torch.cuda.synchronize()
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(9))
+    st = ost.State(16)
+    om = st.new_meta()
+    st.step()
+    f = ost.linear_forward(om, x, w)
+    check_gemm(step.y.float().cpu().numpy(), f["y"])
+    assert meta.idx == 1 and count[0] == 1
+
+
 # ------------------------------------------------------------ workload 3 ---
 
 def dynamic_linear_gpu(x, w, g):
