@@ -218,24 +218,27 @@ typedef struct {
 } fp8_linear_step_io;
 
 /* Number of events fp8_linear_step_delayed records when given an array. */
-#define FP8_STEP_NEVENTS 10
+#define FP8_STEP_NEVENTS 8
 
 /* The AstrAI page's training step for one linear (fp8_autocast entry, then
  * fp8_linear_forward, then fp8_linear_backward), as one call that enqueues
  * every kernel on `s`:
- *   fp8_state_step (refresh every m->interval steps);
- *   X -> xq with x_scale_inv (amax[0]); W -> wq, wqt with scale_inv (amax[1]);
+ *   fp8_state_step (refresh every m->interval steps); amax[0..2] cleared;
+ *   X -> xq with x_scale_inv (amax[0]) and W -> wq, wqt with scale_inv
+ *   (amax[1]), one launch;
  *   y = fprop(xq, x_scale, wq, scale, bias);
- *   record amax[1] in the history; lag-update the x scale from amax[0];
- *   if g: G -> gq, gqt with g_scale_inv (amax[2]); X -> xqt with the updated
- *   x_scale_inv; dx = dgrad(gq, g_scale, wqt, scale); dw = wgrad(gqt,
- *   g_scale, xqt, x_scale); lag-update the g scale from amax[2].
- * The backward reuses the forward's Wqᵀ: the page quantises w again with the
- * same scale_inv, which gives the same bytes.  `events` (nullable) receives
- * FP8_STEP_NEVENTS cudaEventRecord calls at the segment boundaries (before
- * each of: X, W, fprop, forward state update, G, Xᵀ, dgrad, wgrad, backward
- * state update; and at the end).  Argument checks as for the single calls;
- * the first failing call's status is returned and later work is not enqueued. */
+ *   history[idx] = amax[1] and the lag update of the x scale from amax[0],
+ *   one launch;
+ *   if g: G -> gq, gqt with g_scale_inv (amax[2]) and X -> xqt with the
+ *   updated x_scale_inv, one launch; dx = dgrad(gq, g_scale, wqt, scale);
+ *   dw = wgrad(gqt, g_scale, xqt, x_scale); lag update of the g scale.
+ * Results are those of the single calls in that order.  The backward reuses
+ * the forward's Wqᵀ: the page quantises w again with the same scale_inv,
+ * which gives the same bytes.  M, N, K multiples of 16.  `events` (nullable)
+ * receives FP8_STEP_NEVENTS cudaEventRecord calls at the segment boundaries
+ * (before: the forward quantisation, fprop, the forward state update, the
+ * backward quantisation, dgrad, wgrad, the backward state update; and at the
+ * end).  Argument checks happen before anything is enqueued. */
 fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_linear_step_io *io,
                                    int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
                                    cudaStream_t s);

@@ -41,7 +41,7 @@ class fp8_linear_step_io(ctypes.Structure):
                  "dw")]
 
 
-FP8_STEP_NEVENTS = 10
+FP8_STEP_NEVENTS = 8
 
 P, I64, I32, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
 S = ctypes.c_int  # fp8_status / enums

@@ -360,13 +360,34 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     FP8_NEED(m->dev, who);
     FP8_NEED(step_count, who);
     FP8_NEED(io, who);
-    FP8_NEED(io->amax, who);
+    if (M <= 0 || N <= 0 || K <= 0 || M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: bad shape [M=%lld, N=%lld, K=%lld]", who, (long long)M,
+                    (long long)N, (long long)K);
+    FP8_TRY(check_dim16(who, "M", M, 16));
+    FP8_TRY(check_dim16(who, "N", N, 16));
+    FP8_TRY(check_dim16(who, "K", K, 16));
+    if (m->interval < 1 || m->idx < 0 || m->idx >= m->interval)
+        return fail(FP8_ERR_SHAPE, "%s: corrupt meta", who);
     const bool bwd = io->g != nullptr;
+    FP8_NEED(io->x, who);
+    FP8_NEED(io->w, who);
+    FP8_NEED(io->xq, who);
+    FP8_NEED(io->wq, who);
+    FP8_NEED(io->wqt, who);
+    FP8_NEED(io->amax, who);
+    FP8_NEED(io->y, who);
     if (bwd) {
         FP8_NEED(io->gq, who);
         FP8_NEED(io->gqt, who);
         FP8_NEED(io->xqt, who);
     }
+    const void *ptrs[] = {io->x, io->w, io->g, io->bias, io->xq, io->xqt, io->wq, io->wqt,
+                          io->gq, io->gqt, io->y, io->dx, io->dw};
+    for (const void *p : ptrs)
+        if (p != nullptr && !aligned16(p))
+            return fail(FP8_ERR_ALIGNMENT, "%s: a buffer is not 16-byte aligned", who);
+    FP8_TRY(check_device(who));
+
     int ev = 0;
     auto mark = [&]() -> fp8_status {
         if (events == nullptr) return FP8_OK;
@@ -374,27 +395,25 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     };
     float *d = m->dev;
     FP8_TRY(fp8_state_step(step_count, m->interval, m, 1, s));
+    FP8_TRY(cuda_status(cudaMemsetAsync(io->amax, 0, 3 * sizeof(float), s), who));
+    // forward: X (lagged x scale, q only) and W (q and qt) in one launch
     FP8_TRY(mark());
-    FP8_TRY(fp8_quantize(io->x, M, K, FP8_RECIPE_DELAYED, nullptr, d + FP8_META_X_SCALE_INV, io->xq,
-                         io->amax + 0, s));
-    FP8_TRY(mark());
-    FP8_TRY(fp8_quantize_transpose(io->w, N, K, FP8_RECIPE_DELAYED, nullptr, d + FP8_META_SCALE_INV,
-                                   io->wq, io->wqt, nullptr, nullptr, io->amax + 1, s));
+    DelayedQuantJob jx{io->x, M, K, d + FP8_META_X_SCALE_INV, io->xq, nullptr, io->amax + 0};
+    DelayedQuantJob jw{io->w, N, K, d + FP8_META_SCALE_INV, io->wq, io->wqt, io->amax + 1};
+    FP8_TRY(cuda_status(launch_quantize_delayed_pair(jx, jw, s), who));
     FP8_TRY(mark());
     FP8_TRY(fp8_linear_fprop(io->xq, d + FP8_META_X_SCALE, io->wq, d + FP8_META_SCALE, M, N, K,
                              FP8_RECIPE_DELAYED, io->bias, io->y, s));
+    // record(amax_w) and the lag update of the x scale, one launch
     FP8_TRY(mark());
-    FP8_TRY(fp8_meta_record(m, FP8_SLOT_W, io->amax + 1, s));
-    FP8_TRY(fp8_meta_record(m, FP8_SLOT_X, io->amax + 0, s));
+    FP8_TRY(cuda_status(launch_meta_fwd(d, m->idx, io->amax + 0, io->amax + 1, s), who));
+    m->idx = (m->idx + 1) % m->interval;
     if (bwd) {
+        // backward: G (q and qt) and X again, transposed, with the updated scale
         FP8_TRY(mark());
-        FP8_TRY(fp8_quantize_transpose(io->g, M, N, FP8_RECIPE_DELAYED, nullptr,
-                                       d + FP8_META_G_SCALE_INV, io->gq, io->gqt, nullptr, nullptr,
-                                       io->amax + 2, s));
-        FP8_TRY(mark());
-        FP8_TRY(fp8_quantize_transpose(io->x, M, K, FP8_RECIPE_DELAYED, nullptr,
-                                       d + FP8_META_X_SCALE_INV, nullptr, io->xqt, nullptr, nullptr,
-                                       nullptr, s));
+        DelayedQuantJob jg{io->g, M, N, d + FP8_META_G_SCALE_INV, io->gq, io->gqt, io->amax + 2};
+        DelayedQuantJob jxt{io->x, M, K, d + FP8_META_X_SCALE_INV, nullptr, io->xqt, nullptr};
+        FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s), who));
         FP8_TRY(mark());
         if (io->dx != nullptr)
             FP8_TRY(fp8_linear_dgrad(io->gq, d + FP8_META_G_SCALE, io->wqt, d + FP8_META_SCALE, M,

@@ -24,6 +24,22 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
                                       float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
                                       float *scale_t, float *scale_inv_t, float *amax_out,
                                       cudaStream_t s);
+// Two delayed-scaling quantisations in one launch (q and/or qt per tensor,
+// rows and cols multiples of 16).  amax_out, when given, must already be
+// zero: this launcher does not clear it.
+struct DelayedQuantJob {
+    const uint16_t *x;
+    int64_t rows, cols;
+    const float *scale_inv;
+    uint8_t *q, *qt;
+    float *amax_out;
+};
+cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const DelayedQuantJob &b,
+                                         cudaStream_t s);
+// Forward state update in one launch: history[idx] = *amax_w, then the lag
+// update of the x scale from *amax_x.
+cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const float *amax_w,
+                            cudaStream_t s);
 cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,
                             uint16_t *out, cudaStream_t s);
 

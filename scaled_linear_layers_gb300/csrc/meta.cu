@@ -26,6 +26,14 @@ __global__ void meta_lag_kernel(float *scale, float *scale_inv, const float *ama
     *scale_inv = si;
 }
 
+__global__ void meta_fwd_kernel(float *dev, int idx, const float *amax_x, const float *amax_w) {
+    dev[FP8_META_HISTORY + idx] = *amax_w;
+    float s, si;
+    scales_from_amax(*amax_x, s, si);
+    dev[FP8_META_X_SCALE] = s;
+    dev[FP8_META_X_SCALE_INV] = si;
+}
+
 __global__ void meta_refresh_kernel(float *dev, int interval) {
     const float *h = dev + FP8_META_HISTORY;
     float m = h[0];
@@ -86,6 +94,12 @@ cudaError_t launch_meta_copy(float *dst, const float *src, cudaStream_t s) {
 
 cudaError_t launch_meta_lag(float *scale, float *scale_inv, const float *amax, cudaStream_t s) {
     meta_lag_kernel<<<1, 1, 0, s>>>(scale, scale_inv, amax);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const float *amax_w,
+                            cudaStream_t s) {
+    meta_fwd_kernel<<<1, 1, 0, s>>>(dev, idx, amax_x, amax_w);
     return cudaGetLastError();
 }
 

@@ -208,21 +208,46 @@ __global__ void __launch_bounds__(256)
 //                   (scale_t/scale_inv_t [C, R/128]).
 enum QtMode { kTensorDelayed = 0, kTensorDynamic = 1, kTile2D = 2, kRowCol = 3 };
 
+// One launch may cover two tensors (a "job" each, same mode): the first
+// job's tiles take blocks 0..tiles-1, the second's the rest.  A step issues
+// its independent quantisations in one launch this way, halving the launch
+// ramps of these short, HBM-bound kernels.
+struct QtJob {
+    const uint16_t *x;
+    int R, C, tiles_x, tiles;
+    const float *scale_src;
+    uint8_t *q, *qt;
+    float *amax_out, *scale, *scale_inv, *scale_t, *scale_inv_t;
+};
+struct QtJobs {
+    QtJob job[2];
+};
+
 template <int kMode>
-__global__ void __launch_bounds__(256)
-    quantize_transpose_kernel(const uint16_t *__restrict__ x, int R, int C,
-                              const float *__restrict__ scale_src, uint8_t *__restrict__ q,
-                              uint8_t *__restrict__ qt, float *__restrict__ amax_out,
-                              float *__restrict__ scale, float *__restrict__ scale_inv,
-                              float *__restrict__ scale_t, float *__restrict__ scale_inv_t) {
+__global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jobs) {
     __shared__ uint32_t tile[128 * 32];
     __shared__ uint32_t red[8];
     __shared__ uint32_t colmax[8][128];
     __shared__ float col_si[128];
     __shared__ float tile_si;
 
+    const bool second = (int)blockIdx.x >= jobs.job[0].tiles;
+    const QtJob J = second ? jobs.job[1] : jobs.job[0];
+    const int tile_id = (int)blockIdx.x - (second ? jobs.job[0].tiles : 0);
+    const int bx = tile_id % J.tiles_x, by = tile_id / J.tiles_x;
+    const uint16_t *__restrict__ x = J.x;
+    const int R = J.R, C = J.C;
+    const float *__restrict__ scale_src = J.scale_src;
+    uint8_t *__restrict__ q = J.q;
+    uint8_t *__restrict__ qt = J.qt;
+    float *__restrict__ amax_out = J.amax_out;
+    float *__restrict__ scale = J.scale;
+    float *__restrict__ scale_inv = J.scale_inv;
+    float *__restrict__ scale_t = J.scale_t;
+    float *__restrict__ scale_inv_t = J.scale_inv_t;
+
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int r0 = blockIdx.y * 128, c0 = blockIdx.x * 128;
+    const int r0 = by * 128, c0 = bx * 128;
     const int chunk = t & 15, rsub = t >> 4;
     const int gc = c0 + chunk * 8;
 
@@ -238,7 +263,7 @@ __global__ void __launch_bounds__(256)
     if (kMode == kTensorDynamic) {
         float s;
         scales_from_amax(*scale_src, s, si_all);
-        if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+        if (bx == 0 && by == 0 && t == 0) {
             *scale = s;
             *scale_inv = si_all;
         }
@@ -258,7 +283,7 @@ __global__ void __launch_bounds__(256)
             row_si[i] = si;
             const int gr = r0 + rsub + 16 * i;
             if (chunk == 0 && gr < R && scale != nullptr) {
-                const int64_t idx = (int64_t)gr * (C >> 7) + blockIdx.x;
+                const int64_t idx = (int64_t)gr * (C >> 7) + bx;
                 scale[idx] = s;
                 scale_inv[idx] = si;
             }
@@ -292,7 +317,7 @@ __global__ void __launch_bounds__(256)
             scales_from_amax(__uint_as_float(m << 16), s, si);
             col_si[t] = si;
             if (c0 + t < C) {
-                const int64_t idx = (int64_t)(c0 + t) * (R >> 7) + blockIdx.y;
+                const int64_t idx = (int64_t)(c0 + t) * (R >> 7) + by;
                 scale_t[idx] = s;
                 scale_inv_t[idx] = si;
             }
@@ -317,7 +342,7 @@ __global__ void __launch_bounds__(256)
             if (t == 0) {
                 float s, si;
                 scales_from_amax(__uint_as_float(m << 16), s, si);
-                const int64_t idx = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+                const int64_t idx = (int64_t)by * J.tiles_x + bx;
                 scale[idx] = s;
                 scale_inv[idx] = si;
                 tile_si = si;
@@ -457,6 +482,38 @@ cudaError_t launch_quantize_rowtiles(const uint16_t *x, int64_t rows, int64_t co
     return cudaGetLastError();
 }
 
+static QtJob make_job(const uint16_t *x, int64_t rows, int64_t cols, const float *src,
+                      float *scale, float *scale_inv, uint8_t *q, uint8_t *qt, float *scale_t,
+                      float *scale_inv_t, float *amax_k) {
+    QtJob j;
+    j.x = x;
+    j.R = (int)rows;
+    j.C = (int)cols;
+    j.tiles_x = (int)((cols + 127) / 128);
+    j.tiles = rows * cols == 0 ? 0 : j.tiles_x * (int)((rows + 127) / 128);
+    j.scale_src = src;
+    j.q = q;
+    j.qt = qt;
+    j.amax_out = amax_k;
+    j.scale = scale;
+    j.scale_inv = scale_inv;
+    j.scale_t = scale_t;
+    j.scale_inv_t = scale_inv_t;
+    return j;
+}
+
+static cudaError_t launch_jobs(int mode, const QtJobs &jobs, cudaStream_t s) {
+    const int grid = jobs.job[0].tiles + jobs.job[1].tiles;
+    if (grid == 0) return cudaSuccess;
+    switch (mode) {
+    case kTensorDelayed: quantize_transpose_kernel<kTensorDelayed><<<grid, 256, 0, s>>>(jobs); break;
+    case kTensorDynamic: quantize_transpose_kernel<kTensorDynamic><<<grid, 256, 0, s>>>(jobs); break;
+    case kTile2D: quantize_transpose_kernel<kTile2D><<<grid, 256, 0, s>>>(jobs); break;
+    default: quantize_transpose_kernel<kRowCol><<<grid, 256, 0, s>>>(jobs); break;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, int mode,
                                       float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
                                       float *scale_t, float *scale_inv_t, float *amax_out,
@@ -471,28 +528,22 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
             return e;
         if (mode == kTensorDelayed) src = scale_inv;
     }
-    if (rows == 0 || cols == 0) return cudaSuccess;
-    dim3 grid((unsigned)((cols + 127) / 128), (unsigned)((rows + 127) / 128));
-    float *amax_k = mode == kTensorDynamic ? nullptr : amax_out;
-    switch (mode) {
-    case kTensorDelayed:
-        quantize_transpose_kernel<kTensorDelayed><<<grid, 256, 0, s>>>(
-            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
-        break;
-    case kTensorDynamic:
-        quantize_transpose_kernel<kTensorDynamic><<<grid, 256, 0, s>>>(
-            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
-        break;
-    case kTile2D:
-        quantize_transpose_kernel<kTile2D><<<grid, 256, 0, s>>>(
-            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
-        break;
-    default:
-        quantize_transpose_kernel<kRowCol><<<grid, 256, 0, s>>>(
-            x, (int)rows, (int)cols, src, q, qt, amax_k, scale, scale_inv, scale_t, scale_inv_t);
-        break;
-    }
-    return cudaGetLastError();
+    QtJobs jobs;
+    jobs.job[0] = make_job(x, rows, cols, src, scale, scale_inv, q, qt, scale_t, scale_inv_t,
+                           mode == kTensorDynamic ? nullptr : amax_out);
+    jobs.job[1] = jobs.job[0];
+    jobs.job[1].tiles = 0;
+    return launch_jobs(mode, jobs, s);
+}
+
+cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const DelayedQuantJob &b,
+                                         cudaStream_t s) {
+    QtJobs jobs;
+    jobs.job[0] = make_job(a.x, a.rows, a.cols, a.scale_inv, nullptr, nullptr, a.q, a.qt, nullptr,
+                           nullptr, a.amax_out);
+    jobs.job[1] = make_job(b.x, b.rows, b.cols, b.scale_inv, nullptr, nullptr, b.q, b.qt, nullptr,
+                           nullptr, b.amax_out);
+    return launch_jobs(kTensorDelayed, jobs, s);
 }
 
 cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,

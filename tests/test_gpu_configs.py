@@ -214,12 +214,12 @@ def test_composite_step_forward_only_and_events():
     meta = fp8.Fp8Meta(16)
     count = [0]
     step.set_inputs(dev_bf16(x), dev_bf16(w))
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
     for e in ev:
         e.record()
     fp8.fp8_linear_step_delayed(meta, count, step, events=ev)
     torch.cuda.synchronize()
-    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(9))
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(7))
     st = ost.State(16)
     om = st.new_meta()
     st.step()
