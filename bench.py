@@ -340,8 +340,8 @@ def gpu_arm(args, rank, world):
         "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 3),
-                     "traffic": profile_traffic("gemm_fp8_tensor_4096.md"),
-                     "kernel": "gemm_f8_tensor_kernel (mean of fprop/dgrad/wgrad launches)",
+                     "traffic": profile_traffic("gemm_fp8_pair_4096.md"),
+                     "kernel": "gemm_f8_pair_kernel (2-SM tcgen05; mean of the fprop/dgrad/wgrad launches)",
                      "peak_source": f"{peaks['src']} bf16 burst {peaks['bf16']} TFLOP/s x 2 (fp8:bf16 nominal)"},
         "kernels": kernels,
         "e2e": {"value": round(STEP_FLOP * world / (ms_e2e_step * 1e-3) / 1e12, 2),
