@@ -35,6 +35,7 @@
 #ifndef FP8LINEAR_H
 #define FP8LINEAR_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -113,6 +114,27 @@ fp8_status fp8_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols,
                                   float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
                                   float *scale_t, float *scale_inv_t, float *amax_out,
                                   cudaStream_t s);
+
+/* Bytes of workspace fp8_quantize_fused_dynamic needs (16 KiB). */
+size_t fp8_quantize_fused_workspace_bytes(void);
+
+/* Current (dynamic) tensorwise scaling of x [rows, cols] in ONE launch, with
+ * the results of fp8_quantize_transpose(..., FP8_RECIPE_DYNAMIC, ...): amax_out
+ * = amax(x), scale/scale_inv from it, q [rows, cols] (nullable) and qt
+ * [cols, rows] (nullable; not both NULL).  A persistent grid computes the amax,
+ * meets at a grid-wide barrier and then casts, re-reading x from L2 when it
+ * fits there (3 instead of 5 HBM bytes per element when only q is written).
+ * rows % 16 == 0 and cols % 16 == 0.
+ * workspace: caller-owned device memory of fp8_quantize_fused_workspace_bytes()
+ * bytes, 16-byte aligned, set to zero once before its first use; each call
+ * leaves it ready for the next.  Calls that may overlap on the GPU (other
+ * streams) need separate workspaces.  After FP8_ERR_TIMEOUT from
+ * fp8_check_device_status, zero the workspace again.
+ * Source: SpecForge "Add training.fp8_linear" page (dynamic tensorwise
+ * scaling); AstrAI fp8_state.py _update_delayed_scale (the scale rule). */
+fp8_status fp8_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols, float *scale,
+                                      float *scale_inv, uint8_t *q, uint8_t *qt, float *amax_out,
+                                      void *workspace, cudaStream_t s);
 
 /* ------------------------------------------------------------------------ */
 /* Scaled FP8 GEMMs (tcgen05, fp32 accumulation in tensor memory, bf16 out)  */

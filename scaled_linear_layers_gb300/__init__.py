@@ -24,7 +24,8 @@ __all__ = [
     "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_meta_init", "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
-    "fp8_linear_step_delayed", "LinearStep",
+    "fp8_linear_step_delayed", "LinearStep", "fp8_quantize_fused_dynamic",
+    "fp8_quantize_fused_workspace_bytes",
     "Fp8Error", "DELAYED", "DYNAMIC", "BLOCK", "BLOCK_2D", "SLOT_W", "SLOT_X", "SLOT_G",
     "library_path",
 ]
@@ -85,6 +86,21 @@ def fp8_quantize_transpose(x, recipe, scale, scale_inv, q, qt, scale_t=None, sca
     _check(_LIB.fp8_quantize_transpose(_ptr(x), x.shape[0], x.shape[1], recipe, _ptr(scale),
                                        _ptr(scale_inv), _ptr(_u8(q)), _ptr(_u8(qt)), _ptr(scale_t),
                                        _ptr(scale_inv_t), _ptr(amax_out), _stream(stream)))
+
+
+def fp8_quantize_fused_workspace_bytes() -> int:
+    return int(_LIB.fp8_quantize_fused_workspace_bytes())
+
+
+def fp8_quantize_fused_dynamic(x, scale, scale_inv, q, qt, amax_out, workspace, stream=None):
+    """Current scaling in one launch; ``workspace`` is a zeroed device tensor
+    of fp8_quantize_fused_workspace_bytes() bytes (reusable across calls)."""
+    _bf16(x)
+    assert x.dim() == 2
+    assert workspace.numel() * workspace.element_size() >= fp8_quantize_fused_workspace_bytes()
+    _check(_LIB.fp8_quantize_fused_dynamic(_ptr(x), x.shape[0], x.shape[1], _ptr(scale),
+                                           _ptr(scale_inv), _ptr(_u8(q)), _ptr(_u8(qt)),
+                                           _ptr(amax_out), _ptr(workspace), _stream(stream)))
 
 
 def fp8_linear_fprop(xq, x_scale, wq, w_scale, M, N, K, recipe, bias, y, stream=None):

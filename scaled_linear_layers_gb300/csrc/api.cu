@@ -213,6 +213,35 @@ fp8_status fp8_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols,
                        who);
 }
 
+size_t fp8_quantize_fused_workspace_bytes(void) { return kFusedWorkspaceBytes; }
+
+fp8_status fp8_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols, float *scale,
+                                      float *scale_inv, uint8_t *q, uint8_t *qt, float *amax_out,
+                                      void *workspace, cudaStream_t s) {
+    const char *who = "fp8_quantize_fused_dynamic";
+    if (rows < 0 || cols < 0 || rows > 0x7FFFFFFF || cols > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: bad shape [%lld, %lld]", who, (long long)rows,
+                    (long long)cols);
+    FP8_TRY(check_dim16(who, "rows", rows, 16));
+    FP8_TRY(check_dim16(who, "cols", cols, 16));
+    if (rows * cols > 0) {
+        FP8_NEED(x, who);
+        if (q == nullptr && qt == nullptr) return fail(FP8_ERR_NULL, "%s: q and qt are both NULL", who);
+    }
+    FP8_NEED(scale, who);
+    FP8_NEED(scale_inv, who);
+    FP8_NEED(amax_out, who);
+    FP8_NEED(workspace, who);
+    FP8_ALIGN(x, who);
+    FP8_ALIGN(q, who);
+    FP8_ALIGN(qt, who);
+    FP8_ALIGN(workspace, who);
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_quantize_fused_dynamic(x, rows, cols, scale, scale_inv, q, qt, amax_out,
+                                                     static_cast<unsigned int *>(workspace), s),
+                       who);
+}
+
 static fp8_status gemm_common(const char *who, const uint8_t *A, const float *sa, const uint8_t *B,
                               const float *sb, int64_t M, int64_t N, int64_t K, fp8_recipe r,
                               uint16_t *D, const char *mname, const char *nname, const char *kname) {
@@ -463,10 +492,11 @@ fp8_status fp8_check_device_status(cudaStream_t s) {
     e = read_and_clear_device_status(&v);
     if (e != cudaSuccess) return cuda_status(e, who);
     if (v == 0) return FP8_OK;
-    return fail(FP8_ERR_TIMEOUT, "%s: a bounded wait ran out (status bits 0x%x: %s%s%s%s)", who, v,
+    return fail(FP8_ERR_TIMEOUT, "%s: a bounded wait ran out (status bits 0x%x: %s%s%s%s%s)", who, v,
                 (v & kStatusTimeoutTma) ? "tma " : "", (v & kStatusTimeoutMma) ? "mma " : "",
                 (v & kStatusTimeoutEpilogue) ? "epilogue " : "",
-                (v & kStatusTimeoutSelftest) ? "selftest" : "");
+                (v & kStatusTimeoutSelftest) ? "selftest " : "",
+                (v & kStatusTimeoutBarrier) ? "grid-barrier" : "");
 }
 
 fp8_status fp8_selftest_wait_timeout(uint32_t timeout_us, cudaStream_t s) {

@@ -18,7 +18,12 @@ enum : unsigned int {
     kStatusTimeoutMma = 2u,
     kStatusTimeoutEpilogue = 4u,
     kStatusTimeoutSelftest = 8u,
+    kStatusTimeoutBarrier = 16u,
 };
+
+// Bytes of the workspace of the single-launch dynamic quantiser: barrier
+// words and one partial amax per CTA of its persistent grid.
+constexpr size_t kFusedWorkspaceBytes = 16384;
 
 // Default limit of one bounded wait, in nanoseconds of %globaltimer.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s

@@ -40,6 +40,11 @@ cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const Delayed
 // update of the x scale from *amax_x.
 cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const float *amax_w,
                             cudaStream_t s);
+// Current scaling in one cooperative launch (see quantize_fused.cu);
+// workspace: kFusedWorkspaceBytes, zero before its first use.
+cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols,
+                                          float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
+                                          float *amax_out, unsigned int *workspace, cudaStream_t s);
 cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,
                             uint16_t *out, cudaStream_t s);
 

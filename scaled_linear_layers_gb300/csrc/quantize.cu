@@ -8,42 +8,10 @@
 // cvt.rn.satfinite.e4m3x2.f32 after one IEEE fp32 multiply by scale_inv.
 #include "common.cuh"
 #include "kernels.h"
+#include "qtile.cuh"
 
 namespace fp8 {
 
-namespace {
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v) {
-    return max(max(absmax_bits2(v.x), absmax_bits2(v.y)), max(absmax_bits2(v.z), absmax_bits2(v.w)));
-}
-
-// Block-wide max of a per-thread bf16-magnitude bit pattern; result valid in
-// thread 0.  `red` holds one word per warp.
-__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
-    v = __reduce_max_sync(0xFFFFFFFFu, v);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t m = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, red[w]);
-        v = m;
-    }
-    return v;
-}
-
-// amax bits (a bf16 magnitude pattern) -> fp32 bits of the same value.
-__device__ __forceinline__ unsigned int bf16bits_to_f32bits(uint32_t b) { return b << 16; }
-
-}  // namespace
 
 // ------------------------------------------------------------------ amax ---
 
@@ -252,11 +220,7 @@ __global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jo
     const int gc = c0 + chunk * 8;
 
     uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int gr = r0 + rsub + 16 * i;
-        v[i] = (gr < R && gc < C) ? ldg_nc_v4(x + (int64_t)gr * C + gc) : make_uint4(0, 0, 0, 0);
-    }
+    tile_load(x, R, C, r0, c0, v);
 
     float si_all = 0.f;
     if (kMode == kTensorDelayed) si_all = *scale_src;
@@ -388,33 +352,7 @@ __global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jo
     if (qt == nullptr) return;  // 2D-tile quantisation without the transpose
     __syncthreads();
 
-    // transposed read-back
-    const int a = lane & 7, b = lane >> 3;
-    const int w = 4 * warp + b;
-    uint32_t wv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) wv[i] = tile[(16 * a + i) * 32 + (w ^ (4 * a))];
-    uint32_t col[4][4];  // col[j][k]: rows 16a+4k..+3 of column 4w+j
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t x0 = wv[4 * k], x1 = wv[4 * k + 1], x2 = wv[4 * k + 2], x3 = wv[4 * k + 3];
-        const uint32_t p0 = __byte_perm(x0, x1, 0x5140), p1 = __byte_perm(x0, x1, 0x7362);
-        const uint32_t p2 = __byte_perm(x2, x3, 0x5140), p3 = __byte_perm(x2, x3, 0x7362);
-        col[0][k] = __byte_perm(p0, p2, 0x5410);
-        col[1][k] = __byte_perm(p0, p2, 0x7632);
-        col[2][k] = __byte_perm(p1, p3, 0x5410);
-        col[3][k] = __byte_perm(p1, p3, 0x7632);
-    }
-    const int gr = r0 + 16 * a;
-    if (gr < R) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int gcc = c0 + 4 * w + j;
-            if (gcc < C)
-                *reinterpret_cast<uint4 *>(qt + (int64_t)gcc * R + gr) =
-                    make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
-        }
-    }
+    tile_transpose_store(tile, qt, R, C, r0, c0);
 }
 
 // --------------------------------------------------------------- padding ---
