@@ -136,6 +136,28 @@ fp8_status fp8_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t c
                                       float *scale_inv, uint8_t *q, uint8_t *qt, float *amax_out,
                                       void *workspace, cudaStream_t s);
 
+/* fp8_quantize_fused_dynamic without a workspace argument, for callers that
+ * cannot allocate device memory: a host framework that owns every byte of the
+ * device in a pre-planned pool and forbids libraries from allocating, or a
+ * plain C caller with no allocator of its own that must not pull in
+ * cudaMalloc and the synchronisation it implies.  The source pages have no
+ * counterpart to this call; it exists only for such callers.
+ * Same arguments (minus the workspace) and results as
+ * fp8_quantize_fused_dynamic.  Its scratch is a 4 KiB array in the library's
+ * own static device memory (barrier words plus one partial amax for each of
+ * at most 1008 CTAs), which every GPU that loads the library keeps until the
+ * process exits; the call returns FP8_ERR_UNSUPPORTED if this GPU's
+ * persistent grid would need more slots than that.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress), so make
+ * that first call before any stream capture.  Every call clears the barrier
+ * words on `s`, and all calls share the one array, so calls that may overlap
+ * on the GPU (other streams, other host threads) race: issue them in one
+ * stream order.  Nothing here calls cudaMalloc, cudaFree or any allocating
+ * routine. */
+fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, int64_t cols,
+                                              float *scale, float *scale_inv, uint8_t *q,
+                                              uint8_t *qt, float *amax_out, cudaStream_t s);
+
 /* ------------------------------------------------------------------------ */
 /* Scaled FP8 GEMMs (tcgen05, fp32 accumulation in tensor memory, bf16 out)  */
 /* ------------------------------------------------------------------------ */

@@ -25,7 +25,7 @@ __all__ = [
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
     "fp8_linear_step_delayed", "LinearStep", "fp8_quantize_fused_dynamic",
-    "fp8_quantize_fused_workspace_bytes",
+    "fp8_quantize_fused_workspace_bytes", "fp8_quantize_fused_dynamic_noalloc",
     "Fp8Error", "DELAYED", "DYNAMIC", "BLOCK", "BLOCK_2D", "SLOT_W", "SLOT_X", "SLOT_G",
     "library_path",
 ]
@@ -101,6 +101,17 @@ def fp8_quantize_fused_dynamic(x, scale, scale_inv, q, qt, amax_out, workspace, 
     _check(_LIB.fp8_quantize_fused_dynamic(_ptr(x), x.shape[0], x.shape[1], _ptr(scale),
                                            _ptr(scale_inv), _ptr(_u8(q)), _ptr(_u8(qt)),
                                            _ptr(amax_out), _ptr(workspace), _stream(stream)))
+
+
+def fp8_quantize_fused_dynamic_noalloc(x, scale, scale_inv, q, qt, amax_out, stream=None):
+    """fp8_quantize_fused_dynamic with the library's static scratch instead of
+    a workspace, for callers that cannot allocate device memory (see the C
+    header).  Calls share that scratch: keep them in one stream order."""
+    _bf16(x)
+    assert x.dim() == 2
+    _check(_LIB.fp8_quantize_fused_dynamic_noalloc(_ptr(x), x.shape[0], x.shape[1], _ptr(scale),
+                                                   _ptr(scale_inv), _ptr(_u8(q)), _ptr(_u8(qt)),
+                                                   _ptr(amax_out), _stream(stream)))
 
 
 def fp8_linear_fprop(xq, x_scale, wq, w_scale, M, N, K, recipe, bias, y, stream=None):

@@ -52,6 +52,7 @@ SIGNATURES = {
     "fp8_quantize_transpose": (S, [P, I64, I64, S, P, P, P, P, P, P, P, P]),
     "fp8_quantize_fused_workspace_bytes": (ctypes.c_size_t, []),
     "fp8_quantize_fused_dynamic": (S, [P, I64, I64, P, P, P, P, P, P, P]),
+    "fp8_quantize_fused_dynamic_noalloc": (S, [P, I64, I64, P, P, P, P, P, P]),
     "fp8_linear_fprop": (S, [P, P, P, P, I64, I64, I64, S, P, P, P]),
     "fp8_linear_dgrad": (S, [P, P, P, P, I64, I64, I64, S, P, P]),
     "fp8_linear_wgrad": (S, [P, P, P, P, I64, I64, I64, S, P, P]),

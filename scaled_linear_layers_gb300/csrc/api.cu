@@ -242,6 +242,34 @@ fp8_status fp8_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t c
                        who);
 }
 
+fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, int64_t cols,
+                                              float *scale, float *scale_inv, uint8_t *q,
+                                              uint8_t *qt, float *amax_out, cudaStream_t s) {
+    const char *who = "fp8_quantize_fused_dynamic_noalloc";
+    if (rows < 0 || cols < 0 || rows > 0x7FFFFFFF || cols > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: bad shape [%lld, %lld]", who, (long long)rows,
+                    (long long)cols);
+    FP8_TRY(check_dim16(who, "rows", rows, 16));
+    FP8_TRY(check_dim16(who, "cols", cols, 16));
+    if (rows * cols > 0) {
+        FP8_NEED(x, who);
+        if (q == nullptr && qt == nullptr) return fail(FP8_ERR_NULL, "%s: q and qt are both NULL", who);
+    }
+    FP8_NEED(scale, who);
+    FP8_NEED(scale_inv, who);
+    FP8_NEED(amax_out, who);
+    FP8_ALIGN(x, who);
+    FP8_ALIGN(q, who);
+    FP8_ALIGN(qt, who);
+    FP8_TRY(check_device(who));
+    const char *why = nullptr;
+    cudaError_t e = launch_quantize_fused_dynamic_noalloc(x, rows, cols, scale, scale_inv, q, qt,
+                                                          amax_out, s, &why);
+    if (e == cudaErrorInvalidValue && why != nullptr)
+        return fail(FP8_ERR_UNSUPPORTED, "%s: %s", who, why);
+    return cuda_status(e, who, why);
+}
+
 static fp8_status gemm_common(const char *who, const uint8_t *A, const float *sa, const uint8_t *B,
                               const float *sb, int64_t M, int64_t N, int64_t K, fp8_recipe r,
                               uint16_t *D, const char *mname, const char *nname, const char *kname) {

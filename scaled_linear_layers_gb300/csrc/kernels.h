@@ -45,6 +45,11 @@ cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const floa
 cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols,
                                           float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
                                           float *amax_out, unsigned int *workspace, cudaStream_t s);
+// The same with a static scratch array instead of a workspace (no allocation).
+cudaError_t launch_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, int64_t cols,
+                                                  float *scale, float *scale_inv, uint8_t *q,
+                                                  uint8_t *qt, float *amax_out, cudaStream_t s,
+                                                  const char **why);
 cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,
                             uint16_t *out, cudaStream_t s);
 

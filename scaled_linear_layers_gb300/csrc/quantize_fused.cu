@@ -118,6 +118,13 @@ __global__ void __launch_bounds__(256) quantize_fused_dynamic_kernel(const Fused
     }
 }
 
+// Scratch of the allocation-free entry point (fp8_quantize_fused_dynamic_noalloc):
+// the barrier words and one partial amax for each of at most
+// kStaticMaxGrid CTAs, 4 KiB that every GPU loading the library keeps until
+// the process exits.  All calls of that entry point share it.
+constexpr int kStaticMaxGrid = 1008;
+static __device__ __align__(256) unsigned int g_noalloc_scratch[kWsHeader + kStaticMaxGrid];
+
 }  // namespace
 
 cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols,
@@ -153,6 +160,72 @@ cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64
     if (grid > a.tiles) grid = a.tiles;
     if (grid > kMaxGrid) grid = kMaxGrid;
     if (grid < 1) grid = 1;
+    void *args[] = {&a};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(quantize_fused_dynamic_kernel),
+                                       dim3((unsigned)grid), dim3(256), args, 0, s);
+}
+
+// The same kernel with its scratch in g_noalloc_scratch instead of a caller
+// workspace.  In host code the array's name is only a stand-in for the device
+// object, so its device address is looked up with cudaGetSymbolAddress once
+// per device (with that device current) on the first call there.  Returns
+// cudaErrorInvalidValue with *why set when the grid this GPU would run needs
+// more partial slots than the array holds.
+cudaError_t launch_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, int64_t cols,
+                                                  float *scale, float *scale_inv, uint8_t *q,
+                                                  uint8_t *qt, float *amax_out, cudaStream_t s,
+                                                  const char **why) {
+    static unsigned int *scratch_addr[64] = {};
+    static int occ_cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) {
+        *why = "device index out of range";
+        return cudaErrorInvalidDevice;
+    }
+    if (scratch_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            *why = "cudaGetSymbolAddress of the static scratch failed";
+            return e;
+        }
+        scratch_addr[dev] = static_cast<unsigned int *>(ptr);
+    }
+    if (occ_cache[dev] == 0) {
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_fused_dynamic_kernel, 256, 0);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        occ_cache[dev] = occ;
+    }
+    FusedArgs a;
+    a.x = x;
+    a.R = (int)rows;
+    a.C = (int)cols;
+    a.tiles_x = (int)((cols + 127) / 128);
+    a.tiles = rows * cols == 0 ? 0 : a.tiles_x * (int)((rows + 127) / 128);
+    a.scale = scale;
+    a.scale_inv = scale_inv;
+    a.amax_out = amax_out;
+    a.q = q;
+    a.qt = qt;
+    a.ws = scratch_addr[dev];
+    a.wait_limit_ns = g_wait_limit_ns;
+    a.status = device_status_word();
+    int64_t grid = (int64_t)num_sms() * occ_cache[dev];
+    if (grid > a.tiles) grid = a.tiles;
+    if (grid < 1) grid = 1;
+    if (grid > kStaticMaxGrid) {
+        *why = "this GPU's persistent grid needs more partial slots than the static scratch "
+               "holds (1008)";
+        return cudaErrorInvalidValue;
+    }
+    // the arrival count must start at zero; a previous call that timed out
+    // may have left it otherwise (a memset, not an allocation)
+    e = cudaMemsetAsync(a.ws, 0, 2 * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
     void *args[] = {&a};
     return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(quantize_fused_dynamic_kernel),
                                        dim3((unsigned)grid), dim3(256), args, 0, s);
