@@ -449,6 +449,258 @@ def cpu_baseline_for_gpu_line(steps: int = 2):
             "cpu_seconds": round(spent_total, 2), "ms_per_step_extrapolated": round(ms_step, 1)}
 
 
+
+# ------------------------------------------------- the other workloads ---
+# `--workload mlp|thd|block|sweep` measures the remaining configurations
+# (one JSON line each; the default line above is the headline workload).
+# Inputs are drawn on the device from a seeded torch generator with the
+# configurations' shapes and distributions (parity of the same paths on
+# host-generated inputs is in tests/test_gpu_configs.py).
+
+def _timed(torch, fn, steps, warmup):
+    for t in range(warmup):
+        fn(t)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(steps):
+        fn(warmup + t)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per step
+
+
+def _seeded_normal(torch, shape, sigma, seed, dev, outliers=None):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * sigma
+    if outliers is not None:
+        p, factor = outliers
+        hit = torch.rand(shape, generator=g, device=dev) < p
+        x = torch.where(hit, x * factor, x)
+    return x.to(torch.bfloat16)
+
+
+class _DynLinear:
+    """fwd + dgrad + wgrad of one projection under current scaling: every
+    operand through the single-launch dynamic quantiser (q and qt)."""
+
+    def __init__(self, fp8, torch, dev, M, N, K, x, w, g):
+        self.fp8, self.M, self.N, self.K = fp8, M, N, K
+        self.x, self.w, self.g = x, w, g
+        u8 = dict(dtype=torch.uint8, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.q = {n: (torch.empty((r, c), **u8), torch.empty((c, r), **u8))
+                  for n, (r, c) in (("x", (M, K)), ("w", (N, K)), ("g", (M, N)))}
+        self.sc = torch.empty(12, dtype=torch.float32, device=dev)
+        self.ws = [torch.zeros(fp8.fp8_quantize_fused_workspace_bytes() // 4, dtype=torch.int32,
+                               device=dev) for _ in range(3)]
+        self.y, self.dx, self.dw = (torch.empty((M, N), **bf), torch.empty((M, K), **bf),
+                                    torch.empty((N, K), **bf))
+
+    def run(self):
+        fp8, sc = self.fp8, self.sc
+        for i, (n, t) in enumerate((("x", self.x), ("w", self.w), ("g", self.g))):
+            fp8.fp8_quantize_fused_dynamic(t, sc[4 * i:4 * i + 1], sc[4 * i + 1:4 * i + 2],
+                                           self.q[n][0], self.q[n][1], sc[4 * i + 2:4 * i + 3],
+                                           self.ws[i])
+        M, N, K = self.M, self.N, self.K
+        sx, sw, sg = sc[0:1], sc[4:5], sc[8:9]
+        fp8.fp8_linear_fprop(self.q["x"][0], sx, self.q["w"][0], sw, M, N, K, fp8.DYNAMIC, None,
+                             self.y)
+        fp8.fp8_linear_dgrad(self.q["g"][0], sg, self.q["w"][1], sw, M, N, K, fp8.DYNAMIC, self.dx)
+        fp8.fp8_linear_wgrad(self.q["g"][1], sg, self.q["x"][1], sx, M, N, K, fp8.DYNAMIC, self.dw)
+
+
+def _gemm_line(metric_name, value_tflops, ms, flop, workload, extra, peaks):
+    fp8_peak = peaks["bf16"] * FP8_PER_BF16
+    return {"metric": metric_name, "value": round(value_tflops, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "flop_per_step": flop, "higher_is_better": True,
+            "frac_of_fp8_peak": round(value_tflops / fp8_peak, 3),
+            "fp8_peak": round(fp8_peak, 1), "data": "synthetic (seeded, on device)",
+            "config": {"workload": workload, **extra}}
+
+
+def workload_mlp(args):
+    import torch
+    import scaled_linear_layers_gb300 as fp8
+    c = synth.CONFIG3
+    dev = torch.device("cuda", 0)
+    M, H, F = c["M"], c["hidden"], c["ffn"]
+    projs = []
+    for i, (K, N) in enumerate(((H, 2 * F), (F, H))):
+        x = _seeded_normal(torch, (M, K), c["x_sigma"], 10 * i + 1, dev)
+        w = _seeded_normal(torch, (N, K), c["w_sigma"], 10 * i + 2, dev)
+        g = _seeded_normal(torch, (M, N), c["g_sigma"], 10 * i + 3, dev)
+        projs.append(_DynLinear(fp8, torch, dev, M, N, K, x, w, g))
+    flop = sum(6.0 * p.M * p.N * p.K for p in projs)
+    ms = _timed(torch, lambda t: [p.run() for p in projs], args.steps, args.warmup)
+    fp8.fp8_check_device_status()
+    return _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
+                      "transformer MLP block, tokens 16384, hidden 4096, FFN 14336 (gate/up "
+                      "4096->28672, down 14336->4096), dynamic scaling, fwd+dgrad+wgrad",
+                      {"M": M, "hidden": H, "ffn": F, "recipe": "dynamic"}, load_peaks())
+
+
+def workload_thd(args):
+    import torch
+    import scaled_linear_layers_gb300 as fp8
+    c = synth.CONFIG4
+    dev = torch.device("cuda", 0)
+    lengths = synth.thd_lengths(c["seed"], c["n_seq"], c["lo"], c["hi"])
+    T = int(lengths.sum())
+    Tp = fp8.fp8_padded_rows(T, c["multiple"])
+    K, N = c["K"], c["N"]
+    x = _seeded_normal(torch, (T, K), c["x_sigma"], 41, dev)
+    w = _seeded_normal(torch, (N, K), c["w_sigma"], 42, dev)
+    g = _seeded_normal(torch, (Tp, N), c["g_sigma"], 43, dev)
+    g[T:] = 0
+    xp = torch.empty((Tp, K), dtype=torch.bfloat16, device=dev)
+    lin = _DynLinear(fp8, torch, dev, Tp, N, K, xp, w, g)
+
+    def step(t):
+        fp8.fp8_pad_tokens(x, c["multiple"], xp)
+        lin.run()
+    flop = 6.0 * Tp * N * K
+    ms = _timed(torch, step, args.steps, args.warmup)
+    fp8.fp8_check_device_status()
+    return _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
+                      "packed THD batch, 64 sequences of 128..4096 tokens, zero-padded to a "
+                      "multiple of 16, linear 4096->4096, dynamic scaling, pad + fwd+dgrad+wgrad",
+                      {"tokens": T, "padded_tokens": Tp, "K": K, "N": N, "recipe": "dynamic"},
+                      load_peaks())
+
+
+def workload_block(args):
+    import torch
+    import scaled_linear_layers_gb300 as fp8
+    c = synth.CONFIG5
+    dev = torch.device("cuda", 0)
+    M, K, N = c["M"], c["K"], c["N"]
+    out = (c["p"], c["factor"])
+    x = _seeded_normal(torch, (M, K), c["sigma"], 51, dev, out)
+    w = _seeded_normal(torch, (N, K), c["sigma"], 52, dev, out)
+    g = _seeded_normal(torch, (M, N), c["sigma"], 53, dev, out)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    xq, xqt, wq, wqt, gq, gqt = (torch.empty((M, K), **u8), torch.empty((K, M), **u8),
+                                 torch.empty((N, K), **u8), torch.empty((K, N), **u8),
+                                 torch.empty((M, N), **u8), torch.empty((N, M), **u8))
+    xs, xsi, xst, xsit = (torch.empty((M, K // 128), **f32), torch.empty((M, K // 128), **f32),
+                          torch.empty((M // 128, K), **f32), torch.empty((M // 128, K), **f32))
+    ws, wsi = torch.empty((N // 128, K // 128), **f32), torch.empty((N // 128, K // 128), **f32)
+    gs, gsi, gst, gsit = (torch.empty((M, N // 128), **f32), torch.empty((M, N // 128), **f32),
+                          torch.empty((M // 128, N), **f32), torch.empty((M // 128, N), **f32))
+    y, dx, dw = (torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                 torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                 torch.empty((N, K), dtype=torch.bfloat16, device=dev))
+    ev = {}
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        ev.setdefault(name, []).append(e)
+
+    def step(t):
+        mark("quant")
+        fp8.fp8_quantize_transpose(x, fp8.BLOCK, xs, xsi, xq, xqt, xst, xsit)
+        fp8.fp8_quantize_transpose(w, fp8.BLOCK_2D, ws, wsi, wq, wqt)
+        fp8.fp8_quantize_transpose(g, fp8.BLOCK, gs, gsi, gq, gqt, gst, gsit)
+        mark("fprop")
+        fp8.fp8_linear_fprop(xq, xs, wq, ws, M, N, K, fp8.BLOCK, None, y)
+        mark("dgrad")
+        fp8.fp8_linear_dgrad(gq, gs, wqt, ws, M, N, K, fp8.BLOCK, dx)
+        mark("wgrad")
+        fp8.fp8_linear_wgrad(gqt, gst, xqt, xst, M, N, K, fp8.BLOCK, dw)
+        mark("end")
+    flop = 6.0 * M * N * K
+    ms = _timed(torch, step, args.steps, args.warmup)
+    fp8.fp8_check_device_status()
+    names = ["quant", "fprop", "dgrad", "wgrad", "end"]
+    seg = {n: statistics.mean(a.elapsed_time(b) for a, b in
+                              zip(ev[n][args.warmup:], ev[names[i + 1]][args.warmup:]))
+           for i, n in enumerate(names[:-1])}
+    line = _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
+                      "block-scaled recipe (1x128 activation/gradient tiles, 128x128 weight "
+                      "tiles), M=32768, K=N=8192, 1% outliers x50, fwd+dgrad+wgrad",
+                      {"M": M, "N": N, "K": K, "recipe": "block"}, load_peaks())
+    gflop = 2.0 * M * N * K
+    qbytes = 4 * M * K + 4 * N * K + 4 * M * N + 16 * (M * K + M * N) // 128 + 8 * (N * K) // (128 * 128)
+    line["kernels"] = {k: {"us": round(seg[k] * 1e3, 1),
+                           "tflops": round(gflop / (seg[k] * 1e-3) / 1e12, 1)}
+                       for k in ("fprop", "dgrad", "wgrad")}
+    line["kernels"]["quant_block_x_w_g"] = {"us": round(seg["quant"] * 1e3, 1),
+                                            "gbs": round(qbytes / (seg["quant"] * 1e-3) / 1e9, 1)}
+    return line
+
+
+def workload_sweep(args):
+    """Quantise-only sweep, n = 2^20 .. 2^30 bf16 elements ([n/4096, 4096]),
+    each kernel replayed from a CUDA graph of 20 launches (no host gaps)."""
+    import torch
+    import scaled_linear_layers_gb300 as fp8
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    rows_out = []
+    for lg in range(20, 31, 2):
+        n = 1 << lg
+        R, C = n // 4096, 4096
+        nbuf = 2 if n >= (1 << 26) else 8
+        xs = [_seeded_normal(torch, (R, C), 1.0, 60 + i, dev) for i in range(nbuf)]
+        q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+        qt = torch.empty((C, R), dtype=torch.uint8, device=dev)
+        sc = torch.ones(8, dtype=torch.float32, device=dev)
+        bs = torch.empty((R, C // 128), dtype=torch.float32, device=dev)
+        bsi = torch.empty((R, C // 128), dtype=torch.float32, device=dev)
+        ws = torch.zeros(fp8.fp8_quantize_fused_workspace_bytes() // 4, dtype=torch.int32, device=dev)
+        s, si, a = sc[0:1], sc[1:2], sc[2:3]
+        si.fill_(100.0)
+        cases = {
+            "amax": (2, lambda i: fp8.fp8_amax(xs[i % nbuf], a)),
+            "quantize_delayed": (3, lambda i: fp8.fp8_quantize(xs[i % nbuf], fp8.DELAYED, None, si, q, a)),
+            "quantize_dynamic_2pass": (5, lambda i: fp8.fp8_quantize(xs[i % nbuf], fp8.DYNAMIC, s, sc[3:4], q, a)),
+            "quantize_dynamic_fused": (3, lambda i: fp8.fp8_quantize_fused_dynamic(xs[i % nbuf], s, sc[3:4], q, None, a, ws)),
+            "cast_transpose_delayed": (4, lambda i: fp8.fp8_quantize_transpose(xs[i % nbuf], fp8.DELAYED, None, si, q, qt, amax_out=a)),
+            "block_1x128": (3, lambda i: fp8.fp8_quantize(xs[i % nbuf], fp8.BLOCK, bs, bsi, q, None)),
+        }
+        row = {"n": n}
+        for name, (bpe, fn) in cases.items():
+            reps = 20
+            try:
+                g = torch.cuda.CUDAGraph()
+                fn(0)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g):
+                    for i in range(reps):
+                        fn(i)
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                t = e0.elapsed_time(e1) / reps * 1e-3
+                mode = "graph"
+            except Exception:  # a launch form the capture does not take: time it plainly
+                torch.cuda.synchronize()
+                t = _timed(torch, fn, reps, 3) * 1e-3
+                mode = "stream"
+            gbs = bpe * n / t / 1e9
+            row[name] = {"us": round(t * 1e6, 2), "gbs": round(gbs, 1),
+                         "frac_hbm": round(gbs / peaks["hbm"], 3),
+                         "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 3), "timing": mode}
+        rows_out.append(row)
+        del xs
+        torch.cuda.empty_cache()
+    fp8.fp8_check_device_status()
+    best = max(r["cast_transpose_delayed"]["gbs"] for r in rows_out)
+    return {"metric": "quantize GB/s (algorithmic bytes) vs HBM", "value": best, "unit": "GB/s",
+            "higher_is_better": True, "data": "synthetic (seeded, on device)",
+            "config": {"workload": "quantise-only sweep, 2^20..2^30 bf16 elements, [n/4096, 4096]"},
+            "hbm_peak_measured": peaks["hbm"], "sweep": rows_out}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,11 +708,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="linear4096",
+                    choices=["linear4096", "mlp", "thd", "block", "sweep"])
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.workload != "linear4096":
+        if rank != 0:
+            return
+        fn = {"mlp": workload_mlp, "thd": workload_thd, "block": workload_block,
+              "sweep": workload_sweep}[args.workload]
+        print(json.dumps(fn(args)), flush=True)
+        return
     if args.impl == "reference":
         line = reference_arm(args, rank, world)
     else:

@@ -103,8 +103,10 @@ fp8_status fp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, fp8_recip
  *   DELAYED / DYNAMIC: scale, scale_inv, amax_out as for fp8_quantize;
  *            scale_t / scale_inv_t unused (may be NULL).
  *   BLOCK:   q uses 1x128 row tiles (scale/scale_inv [rows, cols/128]); qt uses
- *            128x1 column tiles, i.e. 1x128 tiles of its own rows
- *            (scale_t/scale_inv_t [cols, rows/128]).  q and its scales may be NULL
+ *            128x1 column tiles, i.e. 1x128 tiles of its own rows; their scales
+ *            scale_t/scale_inv_t are [rows/128, cols]: entry [b, c] is the
+ *            scale of column c over rows 128b..128b+127 (qt row c, contraction
+ *            block b), contiguous over c.  q and its scales may be NULL
  *            together when only qt is wanted (wgrad operands).
  *   BLOCK_2D: 128x128 tiles; scale/scale_inv [rows/128, cols/128] serve both q
  *            and qt; scale_t/scale_inv_t unused.
@@ -188,7 +190,7 @@ fp8_status fp8_linear_dgrad(const uint8_t *gq, const float *g_scale,
 
 /* dw [N,K] = bf16( g_scale·x_scale · gqt[N,M] · xqt[K,M]ᵀ ), gqt = Gqᵀ,
  * xqt = Xqᵀ.  The result overwrites dw (no accumulation into a main grad).
- * BLOCK: g_scale [N, M/128] and x_scale [K, M/128] are the column-tile scales
+ * BLOCK: g_scale [M/128, N] and x_scale [M/128, K] are the column-tile scales
  * that fp8_quantize_transpose writes to scale_t. */
 fp8_status fp8_linear_wgrad(const uint8_t *gqt, const float *g_scale,
                             const uint8_t *xqt, const float *x_scale,

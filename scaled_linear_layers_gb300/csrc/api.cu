@@ -304,9 +304,8 @@ fp8_status fp8_linear_fprop(const uint8_t *xq, const float *x_scale, const uint8
     if (r == FP8_RECIPE_BLOCK) {
         if (bias != nullptr) return fail(FP8_ERR_UNSUPPORTED, "%s: bias with the block recipe", who);
         // A = Xq [M,K], scales [M, K/128]; B = Wq [N,K], 128x128 grid [N/128, K/128]
-        return cuda_status(launch_gemm_block(xq, wq, M, N, K, x_scale, K / 128, w_scale, K / 128, 1,
-                                             128, y, s, &why),
-                           who, why);
+        const BlockScales sc{x_scale, K / 128, 1, w_scale, K / 128, 1, 128};
+        return cuda_status(launch_gemm_block(xq, wq, M, N, K, sc, y, s, &why), who, why);
     }
     FP8_ALIGN(bias, who);
     return cuda_status(launch_gemm_tensor(xq, wq, M, N, K, x_scale, w_scale, bias, y, s, &why), who,
@@ -323,9 +322,8 @@ fp8_status fp8_linear_dgrad(const uint8_t *gq, const float *g_scale, const uint8
     if (r == FP8_RECIPE_BLOCK) {
         // A = Gq [M,N], scales [M, N/128]; B = Wqᵀ [K,N]: the scale of B row k,
         // contraction block nb is W's grid entry [nb, k/128].
-        return cuda_status(launch_gemm_block(gq, wqt, M, K, N, g_scale, N / 128, w_scale, 1,
-                                             K / 128, 128, dx, s, &why),
-                           who, why);
+        const BlockScales sc{g_scale, N / 128, 1, w_scale, 1, K / 128, 128};
+        return cuda_status(launch_gemm_block(gq, wqt, M, K, N, sc, dx, s, &why), who, why);
     }
     return cuda_status(launch_gemm_tensor(gq, wqt, M, K, N, g_scale, w_scale, nullptr, dx, s, &why),
                        who, why);
@@ -339,10 +337,10 @@ fp8_status fp8_linear_wgrad(const uint8_t *gqt, const float *g_scale, const uint
     FP8_TRY(gemm_common(who, gqt, g_scale, xqt, x_scale, M, N, K, r, dw, "M", "N", "K"));
     const char *why = nullptr;
     if (r == FP8_RECIPE_BLOCK) {
-        // A = Gqᵀ [N,M], scales [N, M/128]; B = Xqᵀ [K,M], scales [K, M/128]
-        return cuda_status(launch_gemm_block(gqt, xqt, N, K, M, g_scale, M / 128, x_scale, M / 128,
-                                             1, 1, dw, s, &why),
-                           who, why);
+        // A = Gqᵀ [N,M] and B = Xqᵀ [K,M]; their column-tile scales are
+        // [M/128, N] and [M/128, K] (block-major)
+        const BlockScales sc{g_scale, 1, N, x_scale, 1, K, 1};
+        return cuda_status(launch_gemm_block(gqt, xqt, N, K, M, sc, dw, s, &why), who, why);
     }
     return cuda_status(launch_gemm_tensor(gqt, xqt, N, K, M, g_scale, x_scale, nullptr, dw, s, &why),
                        who, why);

@@ -66,13 +66,19 @@ cudaError_t launch_gemm_pair(const uint8_t *A, const uint8_t *B, int64_t M, int6
                              const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
                              int bn, cudaStream_t s, const char **why);
 
-// Block-scaled variant: the contraction is split into 128-blocks; A's block
-// scales are sa[i * sa_ld + kb]; B's are sb[(j / b_rows_per_scale) *
-// sb_row_stride + kb * sb_k_stride].
+// Block-scaled variant: the contraction is split into 128-blocks; A's scale
+// of (row i, block kb) is sa[i * sa_row + kb * sa_k]; B's scale of (row j,
+// block kb) is sb[(j / b_rows) * sb_row + kb * sb_k], b_rows = 1 (per-row
+// scales) or 128 (128x128 weight tiles).
+struct BlockScales {
+    const float *sa;
+    int64_t sa_row, sa_k;
+    const float *sb;
+    int64_t sb_row, sb_k;
+    int b_rows;
+};
 cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
-                              const float *sa, int64_t sa_ld, const float *sb,
-                              int64_t sb_row_stride, int64_t sb_k_stride, int b_rows_per_scale,
-                              uint16_t *D, cudaStream_t s, const char **why);
+                              const BlockScales &sc, uint16_t *D, cudaStream_t s, const char **why);
 
 cudaError_t launch_meta_init(float *dev, int interval, cudaStream_t s);
 cudaError_t launch_meta_copy(float *dst, const float *src, cudaStream_t s);

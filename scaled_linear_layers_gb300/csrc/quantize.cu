@@ -173,7 +173,9 @@ __global__ void __launch_bounds__(256)
 //                   (scale grid [R/128, C/128]), used for q and qt.
 //   kRowCol:        q uses 1x128 row-tile scales (scale/scale_inv
 //                   [R, C/128]); qt uses 128x1 column-tile scales
-//                   (scale_t/scale_inv_t [C, R/128]).
+//                   (scale_t/scale_inv_t [R/128, C]: one row of scales per
+//                   128-row block, contiguous over the columns, which is the
+//                   order the block GEMM reads them in).
 enum QtMode { kTensorDelayed = 0, kTensorDynamic = 1, kTile2D = 2, kRowCol = 3 };
 
 // One launch may cover two tensors (a "job" each, same mode): the first
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jo
             scales_from_amax(__uint_as_float(m << 16), s, si);
             col_si[t] = si;
             if (c0 + t < C) {
-                const int64_t idx = (int64_t)(c0 + t) * (R >> 7) + by;
+                const int64_t idx = (int64_t)by * C + (c0 + t);  // [R/128, C]
                 scale_t[idx] = s;
                 scale_inv_t[idx] = si;
             }

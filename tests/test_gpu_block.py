@@ -25,7 +25,8 @@ def check(got, ref, bound):
     assert ok.all(), f"{(~ok).sum()} of {ok.size} outside tolerance; first {np.argwhere(~ok)[:3]}"
 
 
-SHAPES = [(128, 128, 128), (256, 384, 512), (384, 256, 1024), (1024, 512, 768)]
+SHAPES = [(128, 128, 128), (256, 384, 512), (384, 256, 1024), (1024, 512, 768),
+          (640, 1152, 384)]
 
 
 def operands(M, N, K, seed):
@@ -75,7 +76,9 @@ def test_block_wgrad(shape):
     gqt, gst, _ = oracle.quantize_coltiles_t(g, 128)   # [N, M], scales [N, M/128]
     xqt, xst, _ = oracle.quantize_coltiles_t(x, 128)   # [K, M], scales [K, M/128]
     dw = bf16_out(N, K)
-    fp8.fp8_linear_wgrad(dev(gqt), dev(gst), dev(xqt), dev(xst), M, N, K, fp8.BLOCK, dw)
+    # the library takes column-tile scales block-major: [M/128, N] and [M/128, K]
+    fp8.fp8_linear_wgrad(dev(gqt), dev(np.ascontiguousarray(gst.T)), dev(xqt),
+                         dev(np.ascontiguousarray(xst.T)), M, N, K, fp8.BLOCK, dw)
     ii, jj = all_entries(N, K)
     _, ref, bound = oracle.gemm_block_entries(gqt, xqt, gst, xst, 1, ii, jj)
     check(dw.float().cpu().numpy().ravel(), ref, bound)

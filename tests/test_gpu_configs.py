@@ -336,13 +336,13 @@ def test_config5_block_recipe_full_size():
     x, w, g = dev_bf16(xh), dev_bf16(wh), dev_bf16(gh)
     # X: 1x128 rows for fprop and 128x1 columns (transposed) for wgrad
     xq, xqt = u8(M, K), u8(K, M)
-    xs, xsi, xst, xsit = f32(M, K // 128), f32(M, K // 128), f32(K, M // 128), f32(K, M // 128)
+    xs, xsi, xst, xsit = f32(M, K // 128), f32(M, K // 128), f32(M // 128, K), f32(M // 128, K)
     fp8.fp8_quantize_transpose(x, fp8.BLOCK, xs, xsi, xq, xqt, xst, xsit)
     wq, wqt = u8(N, K), u8(K, N)
     ws, wsi = f32(N // 128, K // 128), f32(N // 128, K // 128)
     fp8.fp8_quantize_transpose(w, fp8.BLOCK_2D, ws, wsi, wq, wqt)
     gq, gqt = u8(M, N), u8(N, M)
-    gs, gsi, gst, gsit = f32(M, N // 128), f32(M, N // 128), f32(N, M // 128), f32(N, M // 128)
+    gs, gsi, gst, gsit = f32(M, N // 128), f32(M, N // 128), f32(M // 128, N), f32(M // 128, N)
     fp8.fp8_quantize_transpose(g, fp8.BLOCK, gs, gsi, gq, gqt, gst, gsit)
     y, dx, dw = bf16_out(M, N), bf16_out(M, K), bf16_out(N, K)
     fp8.fp8_linear_fprop(xq, xs, wq, ws, M, N, K, fp8.BLOCK, None, y)
@@ -358,12 +358,14 @@ def test_config5_block_recipe_full_size():
         assert np.array_equal(xs[r0:r0 + 128].cpu().numpy(), s_ref)
         qt_ref, st_ref, _ = oracle.quantize_coltiles_t(blk, 128)
         assert np.array_equal(host_u8(xqt[:, r0:r0 + 128]), qt_ref)
-        assert np.array_equal(xst[:, r0 // 128].cpu().numpy(), st_ref[:, 0])
+        assert np.array_equal(xst[r0 // 128].cpu().numpy(), st_ref[:, 0])
     wq_ref, ws_ref, _ = oracle.quantize_sqtiles(wh, 128)
     assert np.array_equal(host_u8(wq), wq_ref) and np.array_equal(ws.cpu().numpy(), ws_ref)
     # GEMMs on sampled entries, with the GPU's (verified) operands
     xqh, gqh, xqth, gqth = host_u8(xq), host_u8(gq), host_u8(xqt), host_u8(gqt)
-    xsh, gsh, xsth, gsth = xs.cpu().numpy(), gs.cpu().numpy(), xst.cpu().numpy(), gst.cpu().numpy()
+    # the oracle takes column-tile scales as [rows of the operand, blocks]
+    xsh, gsh = xs.cpu().numpy(), gs.cpu().numpy()
+    xsth, gsth = np.ascontiguousarray(xst.cpu().numpy().T), np.ascontiguousarray(gst.cpu().numpy().T)
     ii, jj = sample_entries(rng, M, N, 1024, 1)
     check_gemm(y.float().cpu().numpy(),
                oracle.gemm_block_entries(xqh, wq_ref, xsh, ws_ref, 128, ii, jj), ii, jj)

@@ -142,7 +142,7 @@ def test_quantize_transpose_block_rowcol(shape):
     x = synth.normal_with_outliers_bf16(shape, 1.0, seed=C, tensor="g")
     q, qt = u8(R, C), u8(C, R)
     s, si = f32(R, C // 128), f32(R, C // 128)
-    st, sit = f32(C, R // 128), f32(C, R // 128)
+    st, sit = f32(R // 128, C), f32(R // 128, C)  # block-major column-tile scales
     a = f32()
     fp8.fp8_quantize_transpose(dev_bf16(x), fp8.BLOCK, s, si, q, qt, st, sit, a)
     ref_q, ref_s, ref_si = oracle.quantize_rowtiles(x, 128)
@@ -150,7 +150,7 @@ def test_quantize_transpose_block_rowcol(shape):
     assert np.array_equal(host_u8(q), ref_q), first_diff(host_u8(q), ref_q)
     assert np.array_equal(s.cpu().numpy(), ref_s) and np.array_equal(si.cpu().numpy(), ref_si)
     assert np.array_equal(host_u8(qt), ref_qt), first_diff(host_u8(qt), ref_qt)
-    assert np.array_equal(st.cpu().numpy(), ref_st) and np.array_equal(sit.cpu().numpy(), ref_sit)
+    assert np.array_equal(st.cpu().numpy(), ref_st.T) and np.array_equal(sit.cpu().numpy(), ref_sit.T)
     assert amax_bits(a.item()) == amax_bits(oracle.amax(x))
 
 
