@@ -3,17 +3,19 @@
 //
 //   D[i,j] = bf16( sum_kb sA(i,kb) * sB(j,kb) * sum_{k in block kb} A[i,k] B[j,k] )
 //
-// A CTA pair (2-SM tcgen05, as in the tensorwise pair kernel) owns a 256 x 256
-// output tile; each 128-deep contraction block is one pipeline stage.  The
-// leader's MMAs write that block's partial product (fresh accumulation) into
-// one of two 256-column TMEM slots of both CTAs; in each CTA the epilogue
-// warps (8, or 16 with per-row B scales; 2 or 4 per TMEM lane quarter) read
-// the partial back 16 (or 8) columns at a time, release the slot, and fold it into
-// fp32 register accumulators with the two block scales using packed fp32x2
-// FMAs.  B's scale
-// is one value per 128-row tile (weights) or one per row (wgrad's Xᵀ operand,
-// staged per warp through shared memory from a layout contiguous over rows).
-// Every wait is bounded, as in the other GEMM kernels.
+// One persistent CTA per SM owns 128 x 128 output tiles; each 128-deep
+// contraction block is one stage of a TMA ring.  The MMA warp writes that
+// block's partial product (fresh accumulation) into one of four 128-column
+// TMEM slots, so it can run three blocks ahead of the promotion; eight
+// epilogue warps (two per TMEM lane quarter, 64 columns each) read a partial
+// back in one round trip, hand the slot back and fold it into fp32 register
+// accumulators with the two block scales using packed fp32x2 FMAs.  B's scale
+// is one value per 128-row tile (weights) or one per row (wgrad's Xᵀ operand:
+// each warp stages its 64 scales of the next block into shared memory with
+// cp.async, from a layout contiguous over rows).  Every handshake is local to
+// the SM: a CTA-pair version of this kernel measured at half the speed, the
+// per-block slot hand-back across two SMs costing more than the slack.  Every
+// wait is bounded, as in the other GEMM kernels.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -26,24 +28,17 @@ extern uint64_t g_wait_limit_ns;
 
 namespace {
 
-constexpr int BN = 256, BNH = 128, BK = 128, STAGES = 6, SLOTS = 2;
-constexpr int A_STAGE = 128 * BK, B_STAGE = BNH * BK, STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int BM = 128, BN = 128, BK = 128, STAGES = 6, SLOTS = 4;
+constexpr int A_STAGE = BM * BK, B_STAGE = BN * BK, STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
+constexpr int COLS = 64;  // accumulator columns per epilogue thread
 constexpr uint32_t TMEM_COLS = SLOTS * BN;  // 512
-constexpr int GROUP_M = 4;
-constexpr uint32_t IDESC = idesc_f8_f32(256, BN);
-
-// Epilogue shape: per-tile B scales need one fp32 factor per block and fit 8
-// warps (128 accumulator columns per thread); per-row B scales need a factor
-// per column and use 16 warps (64 columns per thread) to stay in registers.
-template <bool kPerRowB>
-struct EpiCfg {
-    static constexpr int WARPS = kPerRowB ? 16 : 8;
-    static constexpr int THREADS = 64 + WARPS * 32;
-    static constexpr int COLS = 4 * BN / WARPS;  // accumulator columns per thread
-    static constexpr int SBUF_FLOATS = WARPS * 2 * COLS;  // per-warp double buffers
-    static constexpr size_t SMEM_BYTES =
-        1024 + (size_t)STAGES * STAGE_BYTES + SBUF_FLOATS * sizeof(float) + 256;
-};
+constexpr int GROUP_M = 8;
+constexpr uint32_t IDESC = idesc_f8_f32(BM, BN);
+constexpr int SBUF_FLOATS = EPI_WARPS * 2 * COLS;  // per-warp double-buffered B-row scales
+constexpr size_t SMEM_BYTES =
+    1024 + (size_t)STAGES * STAGE_BYTES + SBUF_FLOATS * sizeof(float) + 256;
 
 struct BlockArgs {
     int M, N, K;
@@ -78,30 +73,26 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 }
 
 template <bool kPerRowB>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_f8_block_kernel(const __grid_constant__ CUtensorMap tma_a,
                          const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
-    using E = EpiCfg<kPerRowB>;
-    constexpr int EPI_WARPS = E::WARPS, COLS = E::COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_STAGE;
     float *sbuf = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf + E::SBUF_FLOATS);
-    uint64_t *full = bars;                // [STAGES] (leader's counts both CTAs' bytes)
-    uint64_t *empty = bars + STAGES;      // [STAGES]
-    uint64_t *sfull = bars + 2 * STAGES;  // [SLOTS] MMA -> epilogues of both CTAs
-    uint64_t *sempty = sfull + SLOTS;     // [SLOTS] (leader's counts both CTAs' epilogue warps)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf + SBUF_FLOATS);
+    uint64_t *full = bars;                // [STAGES] TMA -> MMA
+    uint64_t *empty = bars + STAGES;      // [STAGES] MMA -> TMA
+    uint64_t *sfull = bars + 2 * STAGES;  // [SLOTS] MMA -> epilogue
+    uint64_t *sempty = sfull + SLOTS;     // [SLOTS] epilogue -> MMA
     uint64_t *drain = sempty + SLOTS;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int m_tiles = (p.M + 255) / 256, n_tiles = (p.N + BN - 1) / BN;
+    const int m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN;
     const int num_tiles = m_tiles * n_tiles;
     const int nk = (p.K + BK - 1) / BK;
 
@@ -112,7 +103,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
         }
         for (int s = 0; s < SLOTS; ++s) {
             mbar_init(&sfull[s], 1);
-            mbar_init(&sempty[s], 2 * EPI_WARPS);
+            mbar_init(&sempty[s], EPI_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -121,11 +112,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
         tma_prefetch_desc(&tma_b);
     }
     if (warp == 1) {
-        tmem_alloc_pair(tmem_holder, TMEM_COLS);
-        tmem_relinquish_pair();
+        tmem_alloc(tmem_holder, TMEM_COLS);
+        tmem_relinquish();
     }
     tc_fence_before();
-    cluster_sync_all();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -135,28 +126,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int tm, tn;
                 grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
-                const int arow = tm * 256 + (int)rank * 128;
-                const int brow = tn * BN + (int)rank * BNH;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns,
                                            kStatusTimeoutTma, p.status)) {
                         ok = false;
                         break;
                     }
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
-                    const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(sA + stage * A_STAGE, &tma_a, leader_full, kb * BK, arow);
-                    tma_load_2d_pair(sB + stage * B_STAGE, &tma_b, leader_full, kb * BK, brow);
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_2d(sA + stage * A_STAGE, &tma_a, &full[stage], kb * BK, tm * BM);
+                    tma_load_2d(sB + stage * B_STAGE, &tma_b, &full[stage], kb * BK, tn * BN);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (!ok && rank == 0) {
+            if (!ok) {
                 for (int s = 0; s < STAGES; ++s) {
                     stage = stage == 0 ? STAGES - 1 : stage - 1;
                     if (stage == STAGES - 1) phase ^= 1u;
@@ -167,13 +155,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ------------------------------------------- MMA issuer (leader)
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
             int stage = 0;
             uint32_t phase = 0;
             uint32_t g = 0;  // contraction blocks issued so far (across tiles)
             bool ok = true;
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const uint32_t slot = g % SLOTS, sphase = (g / SLOTS) & 1u;
                     if (!mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag, p.wait_limit_ns,
@@ -189,37 +177,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
                     const uint32_t d_tmem = tmem_base + slot * BN;
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        mma_f8_pair(d_tmem, smem_desc_sw128(a0 + 32 * k),
-                                    smem_desc_sw128(b0 + 32 * k), IDESC, k != 0);
-                    mma_commit_pair(&empty[stage], 0x3);
-                    mma_commit_pair(&sfull[slot], 0x3);
+                        mma_f8(d_tmem, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k),
+                               IDESC, k != 0);
+                    mma_commit(&empty[stage]);
+                    mma_commit(&sfull[slot]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            mma_commit_pair(drain, 0x1);
+            mma_commit(drain);
             volatile int no_abort = 0;
             mbar_wait_bounded(drain, 0, &no_abort, p.wait_limit_ns, kStatusTimeoutMma, p.status);
         }
     } else {
-        // -------------------------------- epilogue (EPI_WARPS, both CTAs)
+        // ------------------------------------------------- epilogue (8 warps)
         const int quarter = warp & 3;
-        const int group = (warp - 2) >> 2;  // columns group*COLS .. +COLS-1 of the tile
+        const int group = (warp - 2) >> 2;  // columns group*64 .. +63 of the tile
         float *wbuf = sbuf + (warp - 2) * 2 * COLS;  // this warp's [2][COLS] B-row scales
-        constexpr int PER_LANE = COLS / 32;           // B-row scales each lane stages
+        constexpr int PER_LANE = COLS / 32;          // B-row scales each lane stages
         const BlockScales &sc = p.sc;
         bool ok = true;
         uint32_t g = 0;
-        for (int tile = pair; tile < num_tiles; tile += npairs) {
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int tm, tn;
             grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
-            const int row = tm * 256 + (int)rank * 128 + quarter * 32 + lane;
+            const int row = tm * BM + quarter * 32 + lane;
             const int j0 = tn * BN + group * COLS;  // first output column of this thread
             const float *sa_row = sc.sa + (int64_t)min(row, p.M - 1) * sc.sa_row;
-            // per-tile B: one scale per block for this thread's columns (which
-            // lie in one 128-row weight tile); per-row B: lane l stages rows
+            // per-tile B: one scale per block for this thread's columns (all in
+            // one 128-row weight tile); per-row B: lane l stages rows
             // j0 + PER_LANE*l .. of the block's scales
             const float *sb_ptr =
                 kPerRowB ? sc.sb + (int64_t)min(j0 + PER_LANE * lane, p.N - PER_LANE) * sc.sb_row
@@ -229,8 +217,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
             for (int j = 0; j < COLS / 2; ++j) acc[j] = 0ull;
             float sa_next = sa_row[0];
             float sb_next = kPerRowB ? 0.f : sb_ptr[0];
-            // per-row B: the block's scales go global -> shared by cp.async, one
-            // block ahead, into the warp's other buffer
             auto stage_scales = [&](int kbn) {
                 const float *src = sb_ptr + (int64_t)kbn * sc.sb_k;
                 float *dst = wbuf + (kbn & 1) * COLS + PER_LANE * lane;
@@ -262,36 +248,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + slot * BN +
                                        (uint32_t)(group * COLS);
+                // all of this warp's columns in one round trip, then the slot
+                // goes back before the math
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(taddr, r0);
+                tmem_ld_32x32b_x32(taddr + 32, r1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[slot]);
                 const uint64_t fsa = pack2(sa_cur, sa_cur);
                 const float f1 = sa_cur * sb_cur;
                 const uint64_t fts = pack2(f1, f1);
-                // CHUNK columns per TMEM load: 16, or 8 where registers are tight
-                constexpr int CHUNK = kPerRowB ? 8 : 16;
 #pragma unroll
-                for (int c = 0; c < COLS / CHUNK; ++c) {
-                    uint32_t r[CHUNK];
-                    if constexpr (CHUNK == 16)
-                        tmem_ld_32x32b_x16(taddr + CHUNK * c, r);
-                    else
-                        tmem_ld_32x32b_x8(taddr + CHUNK * c, r);
-                    tmem_ld_wait();
-                    if (c == COLS / CHUNK - 1) {  // the whole slot is in registers: hand it back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sempty[slot]), 0));
-                    }
-#pragma unroll
-                    for (int j = 0; j < CHUNK / 2; ++j) {
-                        const int a = (CHUNK / 2) * c + j;  // accumulator pair index
-                        const uint64_t pv =
-                            pack2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                        if (kPerRowB) {
-                            const float2 sb2 = *reinterpret_cast<const float2 *>(buf + 2 * a);
-                            const uint64_t f = mul2(pack2(sb2.x, sb2.y), fsa);
-                            acc[a] = fma2(pv, f, acc[a]);
-                        } else {
-                            acc[a] = fma2(pv, fts, acc[a]);
-                        }
+                for (int a = 0; a < COLS / 2; ++a) {
+                    const uint32_t lo = a < 16 ? r0[2 * a] : r1[2 * a - 32];
+                    const uint32_t hi = a < 16 ? r0[2 * a + 1] : r1[2 * a - 31];
+                    const uint64_t pv = pack2(__uint_as_float(lo), __uint_as_float(hi));
+                    if (kPerRowB) {
+                        const float2 sb2 = *reinterpret_cast<const float2 *>(buf + 2 * a);
+                        const uint64_t f = mul2(pack2(sb2.x, sb2.y), fsa);
+                        acc[a] = fma2(pv, f, acc[a]);
+                    } else {
+                        acc[a] = fma2(pv, fts, acc[a]);
                     }
                 }
             }
@@ -311,11 +290,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiCfg<kPerRowB>::TH
 
     __syncwarp();  // lanes that skipped a role wait here for their warp's lane 0
     tc_fence_before();
-    cluster_sync_all();  // the peer's smem/TMEM stay alive until the leader's MMAs drained
+    __syncthreads();
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -328,12 +307,11 @@ cudaError_t launch_block(const CUtensorMap &ta, const CUtensorMap &tb, const Blo
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(gemm_f8_block_kernel<kPerRowB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)EpiCfg<kPerRowB>::SMEM_BYTES);
+                                             (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    gemm_f8_block_kernel<kPerRowB>
-        <<<grid, EpiCfg<kPerRowB>::THREADS, EpiCfg<kPerRowB>::SMEM_BYTES, s>>>(ta, tb, args);
+    gemm_f8_block_kernel<kPerRowB><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, args);
     return cudaGetLastError();
 }
 
@@ -343,7 +321,7 @@ cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int
                               const BlockScales &sc, uint16_t *D, cudaStream_t s,
                               const char **why) {
     CUtensorMap ta, tb;
-    if (!make_tmap_k128(&ta, A, M, K, 128) || !make_tmap_k128(&tb, B, N, K, BNH)) {
+    if (!make_tmap_k128(&ta, A, M, K, BM) || !make_tmap_k128(&tb, B, N, K, BN)) {
         *why = "cuTensorMapEncodeTiled failed";
         return cudaErrorInvalidValue;
     }
@@ -356,9 +334,8 @@ cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int
     args.ldd = N;
     args.wait_limit_ns = g_wait_limit_ns;
     args.status = device_status_word();
-    const int64_t tiles = ((M + 255) / 256) * ((N + BN - 1) / BN);
-    const int64_t pairs = num_sms() / 2;
-    const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
     if (sc.b_rows == 1) return launch_block<true>(ta, tb, args, grid, s);
     if (sc.b_rows == 128) return launch_block<false>(ta, tb, args, grid, s);
     *why = "B scales must be per row or per 128-row tile";
