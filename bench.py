@@ -152,11 +152,15 @@ class Step:
         self.events = None  # per-step event lists of the timed region
         self.pool = []      # events created (and recorded once) ahead of it
 
-    def prepare_events(self, steps):
+    def prepare_events(self, steps, every):
         """Create the timed region's events up front so the region itself
-        only passes their handles to the native call."""
+        only passes their handles to the native call; steps without events
+        get None."""
         self.pool = []
-        for _ in range(steps):
+        for i in range(steps):
+            if i % every != 0:
+                self.pool.append(None)
+                continue
             ev = [self.torch.cuda.Event(enable_timing=True) for _ in range(len(SEGMENTS) + 1)]
             for e in ev:
                 e.record()
@@ -171,7 +175,8 @@ class Step:
         ev = None
         if self.events is not None and self.pool:
             ev = self.pool.pop()
-            self.events.append(ev)
+            if ev is not None:
+                self.events.append(ev)
         self.fp8.fp8_linear_step_delayed(self.meta, self.count, self.io, events=ev)
         # kernels: 2 quantiser launches + 3 GEMMs + 2 state updates (+1 refresh)
         self.launches += 7 + (1 if self.count[0] % 16 == 0 else 0)
@@ -219,7 +224,8 @@ def gpu_arm(args, rank, world):
     barrier()
 
     # --- device-resident timed region
-    step.prepare_events(args.steps)
+    if not args.no_kernel_events:
+        step.prepare_events(args.steps, max(1, args.event_every))
     torch.cuda.synchronize()
     step.launches = 0
     t_start = torch.cuda.Event(enable_timing=True)
@@ -235,7 +241,7 @@ def gpu_arm(args, rank, world):
         clocks = clk.summary(first)
     launches = step.launches
     ms_total = t_start.elapsed_time(t_end)
-    segs = kernel_times(step.events)
+    segs = kernel_times(step.events) if step.events else None
     step.events = None
     fp8.fp8_check_device_status()
 
@@ -307,17 +313,21 @@ def gpu_arm(args, rank, world):
 
     peaks = load_peaks()
     fp8_peak = peaks["bf16"] * FP8_PER_BF16
-    gemm_ms = statistics.mean(segs[k] for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"))
-    gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
     kernels = {}
-    for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"):
-        kernels[k] = {"us": round(segs[k] * 1e3, 2),
-                      "tflops": round(GEMM_FLOP / (segs[k] * 1e-3) / 1e12, 1)}
-    for k, b in QBYTES.items():
-        gbs = b / (segs[k] * 1e-3) / 1e9
-        kernels[k] = {"us": round(segs[k] * 1e3, 2), "gbs": round(gbs, 1),
-                      "frac_hbm": round(gbs / peaks["hbm"], 3),
-                      "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 3)}
+    gemm_tflops = None
+    if segs is not None:
+        gemm_ms = statistics.mean(segs[k] for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"))
+        gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
+        for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"):
+            kernels[k] = {"us": round(segs[k] * 1e3, 2),
+                          "tflops": round(GEMM_FLOP / (segs[k] * 1e-3) / 1e12, 1)}
+        for k, b in QBYTES.items():
+            gbs = b / (segs[k] * 1e-3) / 1e9
+            kernels[k] = {"us": round(segs[k] * 1e3, 2), "gbs": round(gbs, 1),
+                          "frac_hbm": round(gbs / peaks["hbm"], 3),
+                          "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 3)}
+        for k in ("meta_fwd", "meta_bwd"):
+            kernels[k] = {"us": round(segs[k] * 1e3, 2)}
     value = STEP_FLOP * world / (ms_step * 1e-3) / 1e12
     line = {
         "metric": METRIC,
@@ -337,9 +347,10 @@ def gpu_arm(args, rank, world):
                    "M": M, "N": N, "K": K, "recipe": "delayed", "input_sets": N_SETS,
                    "l2": "inputs rotate over 20 X/G sets (1.25 GiB) > 129 MB L2",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
+        "roofline": {"bound": "tensor",
+                     "achieved": None if gemm_tflops is None else round(gemm_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / fp8_peak, 3),
+                     "frac": None if gemm_tflops is None else round(gemm_tflops / fp8_peak, 3),
                      "traffic": profile_traffic("gemm_fp8_pair_4096.md"),
                      "kernel": "gemm_f8_pair_kernel (2-SM tcgen05; mean of the fprop/dgrad/wgrad launches)",
                      "peak_source": f"{peaks['src']} bf16 burst {peaks['bf16']} TFLOP/s x 2 (fp8:bf16 nominal)"},
@@ -348,6 +359,9 @@ def gpu_arm(args, rank, world):
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e_step, 4)},
         "gpu_launches": launches,
+        "kernel_timing": None if segs is None else
+        f"CUDA events at the kernel boundaries of every {max(1, args.event_every)}-th timed step "
+        "(an event between two kernels stops their programmatic overlap)",
         "clocks": clocks,
     }
     return line
@@ -708,6 +722,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernel-events", action="store_true",
+                    help="time the step without per-kernel events (no per-kernel breakdown)")
+    ap.add_argument("--event-every", type=int, default=10,
+                    help="record kernel-boundary events on every n-th timed step: an event "
+                         "between two kernels stops the second from overlapping the first")
     ap.add_argument("--workload", default="linear4096",
                     choices=["linear4096", "mlp", "thd", "block", "sweep"])
     args = ap.parse_args()

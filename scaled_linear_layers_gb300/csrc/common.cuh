@@ -34,6 +34,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel on the stream finishes.  It does
+// its set-up (barriers, TMEM, descriptors), then waits here before it touches
+// global memory, and lets the next kernel be scheduled right away.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait_prior() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_allow_next() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

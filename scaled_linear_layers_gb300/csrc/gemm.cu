@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    pdl_wait_prior();  // set-up done; the previous kernel's results are needed from here
+    pdl_allow_next();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -299,8 +301,7 @@ cudaError_t launch_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, 
     args.status = device_status_word();
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
-    gemm_f8_tensor_kernel<BN><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, args);
-    return cudaGetLastError();
+    return launch_pdl(gemm_f8_tensor_kernel<BN>, grid, NUM_THREADS, C::SMEM_BYTES, s, ta, tb, args);
 }
 
 }  // namespace

@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    pdl_wait_prior();  // set-up done; the previous kernel's results are needed from here
+    pdl_allow_next();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -311,8 +313,8 @@ cudaError_t launch_block(const CUtensorMap &ta, const CUtensorMap &tb, const Blo
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    gemm_f8_block_kernel<kPerRowB><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, args);
-    return cudaGetLastError();
+    return launch_pdl(gemm_f8_block_kernel<kPerRowB>, grid, NUM_THREADS, SMEM_BYTES, s, ta, tb,
+                      args);
 }
 
 }  // namespace

@@ -114,6 +114,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     cluster_sync_all();  // barriers of both CTAs initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    pdl_wait_prior();  // set-up done; the previous kernel's results are needed from here
+    pdl_allow_next();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -305,8 +307,7 @@ cudaError_t launch_pair_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_
     const int64_t tiles = ((M + 255) / 256) * ((N + BN - 1) / BN);
     const int64_t pairs = num_sms() / 2;
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    gemm_f8_pair_kernel<BN><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, args);
-    return cudaGetLastError();
+    return launch_pdl(gemm_f8_pair_kernel<BN>, grid, NUM_THREADS, C::SMEM_BYTES, s, ta, tb, args);
 }
 
 }  // namespace

@@ -13,13 +13,21 @@ namespace {
 __device__ unsigned int g_device_status = 0;
 
 __global__ void meta_init_kernel(float *dev, int interval) {
+    pdl_wait_prior();
+    pdl_allow_next();
     for (int i = threadIdx.x; i < FP8_META_HISTORY + interval; i += blockDim.x)
         dev[i] = (i == 6 || i == 7) ? 0.0f : 1.0f;
 }
 
-__global__ void meta_copy_kernel(float *dst, const float *src) { *dst = *src; }
+__global__ void meta_copy_kernel(float *dst, const float *src) {
+    pdl_wait_prior();
+    pdl_allow_next();
+    *dst = *src;
+}
 
 __global__ void meta_lag_kernel(float *scale, float *scale_inv, const float *amax) {
+    pdl_wait_prior();
+    pdl_allow_next();
     float s, si;
     scales_from_amax(*amax, s, si);
     *scale = s;
@@ -27,6 +35,8 @@ __global__ void meta_lag_kernel(float *scale, float *scale_inv, const float *ama
 }
 
 __global__ void meta_fwd_kernel(float *dev, int idx, const float *amax_x, const float *amax_w) {
+    pdl_wait_prior();
+    pdl_allow_next();
     dev[FP8_META_HISTORY + idx] = *amax_w;
     float s, si;
     scales_from_amax(*amax_x, s, si);
@@ -35,6 +45,8 @@ __global__ void meta_fwd_kernel(float *dev, int idx, const float *amax_x, const 
 }
 
 __global__ void meta_refresh_kernel(float *dev, int interval) {
+    pdl_wait_prior();
+    pdl_allow_next();
     const float *h = dev + FP8_META_HISTORY;
     float m = h[0];
     for (int i = 1; i < interval; ++i) {
@@ -83,29 +95,24 @@ cudaError_t read_and_clear_device_status(unsigned int *out) {
 }
 
 cudaError_t launch_meta_init(float *dev, int interval, cudaStream_t s) {
-    meta_init_kernel<<<1, 128, 0, s>>>(dev, interval);
-    return cudaGetLastError();
+    return launch_pdl(meta_init_kernel, 1, 128, 0, s, dev, interval);
 }
 
 cudaError_t launch_meta_copy(float *dst, const float *src, cudaStream_t s) {
-    meta_copy_kernel<<<1, 1, 0, s>>>(dst, src);
-    return cudaGetLastError();
+    return launch_pdl(meta_copy_kernel, 1, 1, 0, s, dst, src);
 }
 
 cudaError_t launch_meta_lag(float *scale, float *scale_inv, const float *amax, cudaStream_t s) {
-    meta_lag_kernel<<<1, 1, 0, s>>>(scale, scale_inv, amax);
-    return cudaGetLastError();
+    return launch_pdl(meta_lag_kernel, 1, 1, 0, s, scale, scale_inv, amax);
 }
 
 cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const float *amax_w,
                             cudaStream_t s) {
-    meta_fwd_kernel<<<1, 1, 0, s>>>(dev, idx, amax_x, amax_w);
-    return cudaGetLastError();
+    return launch_pdl(meta_fwd_kernel, 1, 1, 0, s, dev, idx, amax_x, amax_w);
 }
 
 cudaError_t launch_meta_refresh(float *dev, int interval, cudaStream_t s) {
-    meta_refresh_kernel<<<1, 1, 0, s>>>(dev, interval);
-    return cudaGetLastError();
+    return launch_pdl(meta_refresh_kernel, 1, 1, 0, s, dev, interval);
 }
 
 cudaError_t launch_selftest_wait(uint32_t timeout_us, cudaStream_t s) {

@@ -18,6 +18,8 @@ namespace fp8 {
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ x, int64_t n,
                                                    float *__restrict__ amax_out) {
     __shared__ uint32_t red[8];
+    pdl_wait_prior();
+    pdl_allow_next();
     uint32_t m = 0;
     const int64_t nvec = n >> 3;  // 8 bf16 per 16-byte vector
     const uint4 *xv = reinterpret_cast<const uint4 *>(x);
@@ -48,6 +50,8 @@ __global__ void __launch_bounds__(256)
                     uint8_t *__restrict__ q, float *__restrict__ amax_out,
                     float *__restrict__ scale_out, float *__restrict__ scale_inv_out) {
     __shared__ uint32_t red[8];
+    pdl_wait_prior();
+    pdl_allow_next();
     float si;
     if (kDynamic) {
         float s;
@@ -107,6 +111,8 @@ __global__ void __launch_bounds__(256)
                              uint8_t *__restrict__ q, float *__restrict__ scale,
                              float *__restrict__ scale_inv, float *__restrict__ amax_out) {
     __shared__ uint32_t red[8];
+    pdl_wait_prior();
+    pdl_allow_next();
     const int lane16 = threadIdx.x & 15;
     const int half = (threadIdx.x >> 4) & 1;
     const int64_t wg = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -200,6 +206,8 @@ __global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jo
     __shared__ uint32_t colmax[8][128];
     __shared__ float col_si[128];
     __shared__ float tile_si;
+    pdl_wait_prior();
+    pdl_allow_next();
 
     const bool second = (int)blockIdx.x >= jobs.job[0].tiles;
     const QtJob J = second ? jobs.job[1] : jobs.job[0];
@@ -362,6 +370,8 @@ __global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jo
 __global__ void __launch_bounds__(256) pad_rows_kernel_v16(const uint4 *__restrict__ x,
                                                            int64_t n_in, int64_t n_out,
                                                            uint4 *__restrict__ out) {
+    pdl_wait_prior();
+    pdl_allow_next();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_out; i += stride)
         out[i] = i < n_in ? ldg_nc_v4(x + i) : make_uint4(0, 0, 0, 0);
@@ -370,6 +380,8 @@ __global__ void __launch_bounds__(256) pad_rows_kernel_v16(const uint4 *__restri
 __global__ void __launch_bounds__(256) pad_rows_kernel_scalar(const uint16_t *__restrict__ x,
                                                               int64_t n_in, int64_t n_out,
                                                               uint16_t *__restrict__ out) {
+    pdl_wait_prior();
+    pdl_allow_next();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_out; i += stride)
         out[i] = i < n_in ? x[i] : (uint16_t)0;
@@ -388,8 +400,7 @@ static int grid_for(int64_t work_items, int per_block) {
 cudaError_t launch_amax(const uint16_t *x, int64_t n, float *amax_out, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
     if (e != cudaSuccess || n == 0) return e;
-    amax_kernel<<<grid_for((n >> 3) / 4 + 1, 256), 256, 0, s>>>(x, n, amax_out);
-    return cudaGetLastError();
+    return launch_pdl(amax_kernel, grid_for((n >> 3) / 4 + 1, 256), 256, 0, s, x, n, amax_out);
 }
 
 cudaError_t launch_quantize_tensor(const uint16_t *x, int64_t n, bool dynamic, float *scale,
@@ -399,12 +410,16 @@ cudaError_t launch_quantize_tensor(const uint16_t *x, int64_t n, bool dynamic, f
     const int grid = grid_for((n >> 4) / 2 + 1, 256);
     if (dynamic) {
         if ((e = launch_amax(x, n, amax_out, s)) != cudaSuccess) return e;
-        quantize_kernel<true><<<grid, 256, 0, s>>>(x, n, amax_out, q, nullptr, scale, scale_inv);
+        e = launch_pdl(quantize_kernel<true>, grid, 256, 0, s, x, n, (const float *)amax_out, q,
+                       (float *)nullptr, scale, scale_inv);
+        if (e != cudaSuccess) return e;
     } else {
         if (amax_out != nullptr && (e = cudaMemsetAsync(amax_out, 0, sizeof(float), s)) != cudaSuccess)
             return e;
         if (n == 0) return cudaSuccess;
-        quantize_kernel<false><<<grid, 256, 0, s>>>(x, n, scale_inv, q, amax_out, nullptr, nullptr);
+        e = launch_pdl(quantize_kernel<false>, grid, 256, 0, s, x, n, (const float *)scale_inv, q,
+                       amax_out, (float *)nullptr, (float *)nullptr);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -417,9 +432,8 @@ cudaError_t launch_quantize_rowtiles(const uint16_t *x, int64_t rows, int64_t co
         return e;
     const int64_t ntiles = rows * (cols / 128);
     if (ntiles == 0) return cudaSuccess;
-    quantize_rowtiles_kernel<<<grid_for(ntiles, 32), 256, 0, s>>>(x, ntiles, q, scale, scale_inv,
-                                                                  amax_out);
-    return cudaGetLastError();
+    return launch_pdl(quantize_rowtiles_kernel, grid_for(ntiles, 32), 256, 0, s, x, ntiles, q,
+                      scale, scale_inv, amax_out);
 }
 
 static QtJob make_job(const uint16_t *x, int64_t rows, int64_t cols, const float *src,
@@ -446,12 +460,11 @@ static cudaError_t launch_jobs(int mode, const QtJobs &jobs, cudaStream_t s) {
     const int grid = jobs.job[0].tiles + jobs.job[1].tiles;
     if (grid == 0) return cudaSuccess;
     switch (mode) {
-    case kTensorDelayed: quantize_transpose_kernel<kTensorDelayed><<<grid, 256, 0, s>>>(jobs); break;
-    case kTensorDynamic: quantize_transpose_kernel<kTensorDynamic><<<grid, 256, 0, s>>>(jobs); break;
-    case kTile2D: quantize_transpose_kernel<kTile2D><<<grid, 256, 0, s>>>(jobs); break;
-    default: quantize_transpose_kernel<kRowCol><<<grid, 256, 0, s>>>(jobs); break;
+    case kTensorDelayed: return launch_pdl(quantize_transpose_kernel<kTensorDelayed>, grid, 256, 0, s, jobs);
+    case kTensorDynamic: return launch_pdl(quantize_transpose_kernel<kTensorDynamic>, grid, 256, 0, s, jobs);
+    case kTile2D: return launch_pdl(quantize_transpose_kernel<kTile2D>, grid, 256, 0, s, jobs);
+    default: return launch_pdl(quantize_transpose_kernel<kRowCol>, grid, 256, 0, s, jobs);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, int mode,
@@ -491,12 +504,11 @@ cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64
     const int64_t n_in = rows * cols, n_out = padded * cols;
     if (n_out == 0) return cudaSuccess;
     if (cols % 8 == 0) {
-        pad_rows_kernel_v16<<<grid_for(n_out / 8, 256), 256, 0, s>>>(
-            reinterpret_cast<const uint4 *>(x), n_in / 8, n_out / 8, reinterpret_cast<uint4 *>(out));
-    } else {
-        pad_rows_kernel_scalar<<<grid_for(n_out, 256), 256, 0, s>>>(x, n_in, n_out, out);
+        return launch_pdl(pad_rows_kernel_v16, grid_for(n_out / 8, 256), 256, 0, s,
+                          reinterpret_cast<const uint4 *>(x), n_in / 8, n_out / 8,
+                          reinterpret_cast<uint4 *>(out));
     }
-    return cudaGetLastError();
+    return launch_pdl(pad_rows_kernel_scalar, grid_for(n_out, 256), 256, 0, s, x, n_in, n_out, out);
 }
 
 }  // namespace fp8
