@@ -204,12 +204,14 @@ fp8_status fp8_linear_wgrad(const uint8_t *gqt, const float *g_scale,
  *   [0] scale   [1] scale_inv      weight, from the amax-history window
  *   [2] x_scale [3] x_scale_inv    activation, lagged one call
  *   [4] g_scale [5] g_scale_inv    gradient, lagged one call
- *   [6..7] reserved
+ *   [6]     x scale used by the forward GEMM of the step in progress
+ *           (written by fp8_linear_step_delayed; otherwise unused)
+ *   [7]     reserved
  *   [8 .. 8+interval) amax_history ring
  * Source: AstrAI fp8_state.py FP8TensorMeta (all fields start at 1). */
 enum { FP8_META_SCALE = 0, FP8_META_SCALE_INV = 1, FP8_META_X_SCALE = 2,
        FP8_META_X_SCALE_INV = 3, FP8_META_G_SCALE = 4, FP8_META_G_SCALE_INV = 5,
-       FP8_META_HISTORY = 8 };
+       FP8_META_X_SCALE_FWD = 6, FP8_META_HISTORY = 8 };
 #define FP8_META_FLOATS(interval) (8 + (interval))
 
 typedef struct {
@@ -268,23 +270,31 @@ typedef struct {
 
 /* The AstrAI page's training step for one linear (fp8_autocast entry, then
  * fp8_linear_forward, then fp8_linear_backward), as one call that enqueues
- * every kernel on `s`:
+ * every kernel:
  *   fp8_state_step (refresh every m->interval steps); amax[0..2] cleared;
  *   X -> xq with x_scale_inv (amax[0]) and W -> wq, wqt with scale_inv
- *   (amax[1]), one launch;
- *   y = fprop(xq, x_scale, wq, scale, bias);
+ *   (amax[1]), one launch, which also copies x_scale to slot
+ *   FP8_META_X_SCALE_FWD;
+ *   y = fprop(xq, x scale of that slot, wq, scale, bias);
  *   history[idx] = amax[1] and the lag update of the x scale from amax[0],
  *   one launch;
  *   if g: G -> gq, gqt with g_scale_inv (amax[2]) and X -> xqt with the
  *   updated x_scale_inv, one launch; dx = dgrad(gq, g_scale, wqt, scale);
  *   dw = wgrad(gqt, g_scale, xqt, x_scale); lag update of the g scale.
- * Results are those of the single calls in that order.  The backward reuses
- * the forward's Wqᵀ: the page quantises w again with the same scale_inv,
- * which gives the same bytes.  M, N, K multiples of 16.  `events` (nullable)
- * receives FP8_STEP_NEVENTS cudaEventRecord calls at the segment boundaries
- * (before: the forward quantisation, fprop, the forward state update, the
- * backward quantisation, dgrad, wgrad, the backward state update; and at the
- * end).  Argument checks happen before anything is enqueued. */
+ * Results are those of the single calls in that order.  The forward state
+ * update and the backward quantisation do not depend on fprop, so they run on
+ * a second stream owned by the library (one per host thread and device),
+ * forked from and joined back into `s` with events: the memory-bound
+ * quantisation overlaps the compute-bound GEMM.  To the caller everything is
+ * ordered on `s` (work enqueued on `s` after this call sees all results).
+ * The backward reuses the forward's Wqᵀ: the page quantises w again with the
+ * same scale_inv, which gives the same bytes.  M, N, K multiples of 16.
+ * `events` (nullable) receives FP8_STEP_NEVENTS cudaEventRecord calls on the
+ * stream of each segment (before: the forward quantisation, fprop, the
+ * forward state update, the backward quantisation, dgrad, wgrad, the backward
+ * state update; and at the end); events between kernels stop their
+ * overlap, so the step runs slower while they are recorded.  Argument checks
+ * happen before anything is enqueued. */
 fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_linear_step_io *io,
                                    int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
                                    cudaStream_t s);

@@ -407,6 +407,34 @@ fp8_status fp8_state_step(int64_t *step_count, int32_t interval, fp8_meta *metas
     return FP8_OK;
 }
 
+namespace {
+
+// The second stream of fp8_linear_step_delayed and its fork/join events, one
+// set per host thread and device (created on first use, kept for the thread's
+// lifetime), so concurrent callers never share them.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream tl_side[kMaxDevices];
+
+fp8_status side_stream(const char *who, SideStream **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, who);
+    SideStream &ss = tl_side[dev];
+    if (ss.stream == nullptr) {
+        if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_status(e, who, "creating the step's second stream");
+    }
+    *out = &ss;
+    return FP8_OK;
+}
+
+}  // namespace
+
 fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_linear_step_io *io,
                                    int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
                                    cudaStream_t s) {
@@ -442,45 +470,64 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
         if (p != nullptr && !aligned16(p))
             return fail(FP8_ERR_ALIGNMENT, "%s: a buffer is not 16-byte aligned", who);
     FP8_TRY(check_device(who));
+    SideStream *side = nullptr;
+    FP8_TRY(side_stream(who, &side));
+    // with timing events everything stays on `s`, so consecutive events
+    // bracket one kernel each
+    const bool overlap = events == nullptr;
+    cudaStream_t s2 = overlap ? side->stream : s;
 
     int ev = 0;
-    auto mark = [&]() -> fp8_status {
+    auto mark = [&](cudaStream_t on) -> fp8_status {
         if (events == nullptr) return FP8_OK;
-        return cuda_status(cudaEventRecord(events[ev++], s), who);
+        return cuda_status(cudaEventRecord(events[ev++], on), who);
     };
     float *d = m->dev;
     FP8_TRY(fp8_state_step(step_count, m->interval, m, 1, s));
     FP8_TRY(cuda_status(cudaMemsetAsync(io->amax, 0, 3 * sizeof(float), s), who));
-    // forward: X (lagged x scale, q only) and W (q and qt) in one launch
-    FP8_TRY(mark());
+    // forward: X (lagged x scale, q only) and W (q and qt) in one launch,
+    // which also keeps the x scale fprop must use
+    FP8_TRY(mark(s));
     DelayedQuantJob jx{io->x, M, K, d + FP8_META_X_SCALE_INV, io->xq, nullptr, io->amax + 0};
     DelayedQuantJob jw{io->w, N, K, d + FP8_META_SCALE_INV, io->wq, io->wqt, io->amax + 1};
-    FP8_TRY(cuda_status(launch_quantize_delayed_pair(jx, jw, s), who));
-    FP8_TRY(mark());
-    FP8_TRY(fp8_linear_fprop(io->xq, d + FP8_META_X_SCALE, io->wq, d + FP8_META_SCALE, M, N, K,
-                             FP8_RECIPE_DELAYED, io->bias, io->y, s));
+    FP8_TRY(cuda_status(launch_quantize_delayed_pair(jx, jw, s, d + FP8_META_X_SCALE,
+                                                     d + FP8_META_X_SCALE_FWD),
+                        who));
+    if (overlap) {  // fork: the state update and the backward quantisation
+        FP8_TRY(cuda_status(cudaEventRecord(side->fork, s), who));
+        FP8_TRY(cuda_status(cudaStreamWaitEvent(s2, side->fork, 0), who));
+    }
+    FP8_TRY(mark(s));
+    FP8_TRY(fp8_linear_fprop(io->xq, d + FP8_META_X_SCALE_FWD, io->wq, d + FP8_META_SCALE, M, N,
+                             K, FP8_RECIPE_DELAYED, io->bias, io->y, s));
     // record(amax_w) and the lag update of the x scale, one launch
-    FP8_TRY(mark());
-    FP8_TRY(cuda_status(launch_meta_fwd(d, m->idx, io->amax + 0, io->amax + 1, s), who));
+    FP8_TRY(mark(s2));
+    FP8_TRY(cuda_status(launch_meta_fwd(d, m->idx, io->amax + 0, io->amax + 1, s2), who));
     m->idx = (m->idx + 1) % m->interval;
     if (bwd) {
         // backward: G (q and qt) and X again, transposed, with the updated scale
-        FP8_TRY(mark());
+        FP8_TRY(mark(s2));
         DelayedQuantJob jg{io->g, M, N, d + FP8_META_G_SCALE_INV, io->gq, io->gqt, io->amax + 2};
         DelayedQuantJob jxt{io->x, M, K, d + FP8_META_X_SCALE_INV, nullptr, io->xqt, nullptr};
-        FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s), who));
-        FP8_TRY(mark());
+        FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s2), who));
+    }
+    if (overlap) {  // join
+        FP8_TRY(cuda_status(cudaEventRecord(side->join, s2), who));
+        FP8_TRY(cuda_status(cudaStreamWaitEvent(s, side->join, 0), who));
+    }
+    if (bwd) {
+        FP8_TRY(mark(s));
         if (io->dx != nullptr)
             FP8_TRY(fp8_linear_dgrad(io->gq, d + FP8_META_G_SCALE, io->wqt, d + FP8_META_SCALE, M,
                                      N, K, FP8_RECIPE_DELAYED, io->dx, s));
-        FP8_TRY(mark());
+        FP8_TRY(mark(s));
         if (io->dw != nullptr)
             FP8_TRY(fp8_linear_wgrad(io->gqt, d + FP8_META_G_SCALE, io->xqt, d + FP8_META_X_SCALE,
                                      M, N, K, FP8_RECIPE_DELAYED, io->dw, s));
-        FP8_TRY(mark());
+        FP8_TRY(mark(s));
         FP8_TRY(fp8_meta_record(m, FP8_SLOT_G, io->amax + 2, s));
     }
-    while (events != nullptr && ev < FP8_STEP_NEVENTS) FP8_TRY(mark());
+    while (events != nullptr && ev < FP8_STEP_NEVENTS) FP8_TRY(mark(s));
     return FP8_OK;
 }
 

@@ -46,7 +46,8 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
                                       cudaStream_t s);
 // Two delayed-scaling quantisations in one launch (q and/or qt per tensor,
 // rows and cols multiples of 16).  amax_out, when given, must already be
-// zero: this launcher does not clear it.
+// zero: this launcher does not clear it.  If snap_dst is given, the launch
+// also copies *snap_src to it (before any state update that follows).
 struct DelayedQuantJob {
     const uint16_t *x;
     int64_t rows, cols;
@@ -55,7 +56,8 @@ struct DelayedQuantJob {
     float *amax_out;
 };
 cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const DelayedQuantJob &b,
-                                         cudaStream_t s);
+                                         cudaStream_t s, const float *snap_src = nullptr,
+                                         float *snap_dst = nullptr);
 // Forward state update in one launch: history[idx] = *amax_w, then the lag
 // update of the x scale from *amax_x.
 cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const float *amax_w,

@@ -197,6 +197,11 @@ struct QtJob {
 };
 struct QtJobs {
     QtJob job[2];
+    // optional scalar copy done by block 0 (snap_dst = *snap_src): lets a
+    // step keep the scale its forward GEMM must use while a concurrent state
+    // update replaces it
+    const float *snap_src;
+    float *snap_dst;
 };
 
 template <int kMode>
@@ -208,6 +213,8 @@ __global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jo
     __shared__ float tile_si;
     pdl_wait_prior();
     pdl_allow_next();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && jobs.snap_dst != nullptr)
+        *jobs.snap_dst = *jobs.snap_src;
 
     const bool second = (int)blockIdx.x >= jobs.job[0].tiles;
     const QtJob J = second ? jobs.job[1] : jobs.job[0];
@@ -486,12 +493,17 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
                            mode == kTensorDynamic ? nullptr : amax_out);
     jobs.job[1] = jobs.job[0];
     jobs.job[1].tiles = 0;
+    jobs.snap_src = nullptr;
+    jobs.snap_dst = nullptr;
     return launch_jobs(mode, jobs, s);
 }
 
 cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const DelayedQuantJob &b,
-                                         cudaStream_t s) {
+                                         cudaStream_t s, const float *snap_src,
+                                         float *snap_dst) {
     QtJobs jobs;
+    jobs.snap_src = snap_src;
+    jobs.snap_dst = snap_dst;
     jobs.job[0] = make_job(a.x, a.rows, a.cols, a.scale_inv, nullptr, nullptr, a.q, a.qt, nullptr,
                            nullptr, a.amax_out);
     jobs.job[1] = make_job(b.x, b.rows, b.cols, b.scale_inv, nullptr, nullptr, b.q, b.qt, nullptr,
