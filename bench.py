@@ -191,6 +191,25 @@ def kernel_times(steps_events):
     return {k: sum(v) / len(v) for k, v in acc.items()}
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of each rank's floats over all ranks, so the job
+    is timed by its slowest replica; the values unchanged when no process
+    group of more than one rank is up."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(ms_step: float, world: int) -> float:
+    """Every rank runs one full 4096^3 step per step (replicas, weak
+    scaling): the job's FLOPs over the slowest rank's step time."""
+    return STEP_FLOP * world / (ms_step * 1e-3) / 1e12
+
+
 def gpu_arm(args, rank, world):
     import torch
     import scaled_linear_layers_gb300 as fp8
@@ -304,10 +323,7 @@ def gpu_arm(args, rank, world):
 
     ms_step = ms_total / args.steps
     ms_e2e_step = ms_e2e / e2e_steps
-    if world > 1:
-        t = torch.tensor([ms_step, ms_e2e_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, ms_e2e_step = t.tolist()
+    ms_step, ms_e2e_step = max_over_ranks([ms_step, ms_e2e_step], dev)
     if rank != 0:
         return None
 
@@ -328,7 +344,7 @@ def gpu_arm(args, rank, world):
                           "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 3)}
         for k in ("meta_fwd", "meta_bwd"):
             kernels[k] = {"us": round(segs[k] * 1e3, 2)}
-    value = STEP_FLOP * world / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(ms_step, world)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -355,7 +371,7 @@ def gpu_arm(args, rank, world):
                      "kernel": "gemm_f8_pair_kernel (2-SM tcgen05; mean of the fprop/dgrad/wgrad launches)",
                      "peak_source": f"{peaks['src']} bf16 burst {peaks['bf16']} TFLOP/s x 2 (fp8:bf16 nominal)"},
         "kernels": kernels,
-        "e2e": {"value": round(STEP_FLOP * world / (ms_e2e_step * 1e-3) / 1e12, 2),
+        "e2e": {"value": round(whole_job_tflops(ms_e2e_step, world), 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e_step, 4)},
         "gpu_launches": launches,
