@@ -83,16 +83,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes or the hint (1 ms) runs out, instead of returning
+// after the hardware's default window; fewer polls while a barrier is far
+// from completing.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // limit_ns (or as soon as *abort is set by another thread of the block),
 // recording `code` in the device status word.  Returns false on give-up.
+// kSleep selects the hinted try_wait (each poll then lasts up to 1 ms, so the
+// limit is checked at least every 64 ms).
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   volatile int *abort, uint64_t limit_ns,
                                                   unsigned int code, unsigned int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > limit_ns) {
@@ -126,9 +146,13 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Arrive once on an mbarrier given by its shared::cluster address (which
-// may be in the peer CTA).
+// may be in the peer CTA).  Default (CTA-scope release) semantics: callers
+// use it to hand TMEM back after tcgen05.wait::ld, when the reads it orders
+// have already completed; a cluster-scope release would also wait for every
+// global load the thread has in flight (scale prefetches), which measured
+// at half the speed of the block-scaled pair kernel.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 

@@ -20,6 +20,15 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
+@pytest.fixture(params=["one_cta", "cta_pair"])
+def kernel(request, monkeypatch):
+    """Runs a test on the one-CTA kernel and on the CTA-pair kernel (256-row
+    pair tiles; with M a multiple of 128 but not of 256 the last pair's peer
+    rows lie past the matrix)."""
+    monkeypatch.setenv("FP8LINEAR_BLOCK_PAIR", "1" if request.param == "cta_pair" else "0")
+    return request.param
+
+
 def check(got, ref, bound):
     ok = oracle.gemm_tolerance_ok(got, ref, bound)
     assert ok.all(), f"{(~ok).sum()} of {ok.size} outside tolerance; first {np.argwhere(~ok)[:3]}"
@@ -42,7 +51,7 @@ def all_entries(R, C):
 
 
 @pytest.mark.parametrize("shape", SHAPES)
-def test_block_fprop(shape):
+def test_block_fprop(shape, kernel):
     M, N, K = shape
     x, w, _ = operands(M, N, K, 1)
     xq, xs, _ = oracle.quantize_rowtiles(x, 128)
@@ -55,7 +64,7 @@ def test_block_fprop(shape):
 
 
 @pytest.mark.parametrize("shape", SHAPES)
-def test_block_dgrad(shape):
+def test_block_dgrad(shape, kernel):
     M, N, K = shape
     _, w, g = operands(M, N, K, 2)
     gq, gs, _ = oracle.quantize_rowtiles(g, 128)
@@ -70,7 +79,7 @@ def test_block_dgrad(shape):
 
 
 @pytest.mark.parametrize("shape", SHAPES)
-def test_block_wgrad(shape):
+def test_block_wgrad(shape, kernel):
     M, N, K = shape
     x, _, g = operands(M, N, K, 3)
     gqt, gst, _ = oracle.quantize_coltiles_t(g, 128)   # [N, M], scales [N, M/128]
@@ -84,7 +93,7 @@ def test_block_wgrad(shape):
     check(dw.float().cpu().numpy().ravel(), ref, bound)
 
 
-def test_block_equal_scales_match_tensorwise_gemm():
+def test_block_equal_scales_match_tensorwise_gemm(kernel):
     """With every tile scale equal, the block GEMM reduces to the tensorwise
     one: both kernels must agree within the tolerance (and the oracle's two
     GEMMs agree exactly, pinned on the CPU)."""
@@ -104,7 +113,7 @@ def test_block_equal_scales_match_tensorwise_gemm():
     check(y_t.float().cpu().numpy(), ref, bound)
 
 
-def test_block_full_size_sampled():
+def test_block_full_size_sampled(kernel):
     """The block workload's fprop shape (M=32768, K=N=8192) on sampled rows."""
     M, N, K = 32768, 8192, 8192
     rng = np.random.default_rng(5)
