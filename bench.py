@@ -134,7 +134,9 @@ class ClockSampler:
 
 # --------------------------------------------------------------- GPU arm ---
 
-SEGMENTS = ["quant_fwd", "gemm_fprop", "meta_fwd", "quant_bwd", "gemm_dgrad", "gemm_wgrad",
+# the step's event segments; dgrad and wgrad run as one launch (between the
+# fifth and sixth events), the sixth segment is empty
+SEGMENTS = ["quant_fwd", "gemm_fprop", "meta_fwd", "quant_bwd", "gemm_dgrad_wgrad", "empty",
             "meta_bwd"]
 
 
@@ -178,8 +180,9 @@ class Step:
             if ev is not None:
                 self.events.append(ev)
         self.fp8.fp8_linear_step_delayed(self.meta, self.count, self.io, events=ev)
-        # kernels: 2 quantiser launches + 3 GEMMs + 2 state updates (+1 refresh)
-        self.launches += 7 + (1 if self.count[0] % 16 == 0 else 0)
+        # kernels: 2 quantiser launches + fprop + one dgrad/wgrad launch + 2
+        # state updates (+1 refresh)
+        self.launches += 6 + (1 if self.count[0] % 16 == 0 else 0)
 
 
 def kernel_times(steps_events):
@@ -332,11 +335,12 @@ def gpu_arm(args, rank, world):
     kernels = {}
     gemm_tflops = None
     if segs is not None:
-        gemm_ms = statistics.mean(segs[k] for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"))
-        gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
-        for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"):
+        # the roofline kernel: the launch carrying dgrad and wgrad (two of the
+        # step's three GEMMs)
+        gemm_tflops = 2 * GEMM_FLOP / (segs["gemm_dgrad_wgrad"] * 1e-3) / 1e12
+        for k, n in (("gemm_fprop", 1), ("gemm_dgrad_wgrad", 2)):
             kernels[k] = {"us": round(segs[k] * 1e3, 2),
-                          "tflops": round(GEMM_FLOP / (segs[k] * 1e-3) / 1e12, 1)}
+                          "tflops": round(n * GEMM_FLOP / (segs[k] * 1e-3) / 1e12, 1)}
         for k, b in QBYTES.items():
             gbs = b / (segs[k] * 1e-3) / 1e9
             kernels[k] = {"us": round(segs[k] * 1e3, 2), "gbs": round(gbs, 1),
@@ -367,8 +371,9 @@ def gpu_arm(args, rank, world):
                      "achieved": None if gemm_tflops is None else round(gemm_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": None if gemm_tflops is None else round(gemm_tflops / fp8_peak, 3),
-                     "traffic": profile_traffic("gemm_fp8_pair_4096.md"),
-                     "kernel": "gemm_f8_pair_kernel (2-SM tcgen05; mean of the fprop/dgrad/wgrad launches)",
+                     "traffic": profile_traffic("gemm_fp8_pair_dgrad_wgrad_4096.md"),
+                     "kernel": "gemm_f8_pair_kernel<256> carrying dgrad and wgrad (2-SM tcgen05, "
+                               "one launch, 2 x 2*4096^3 FLOP)",
                      "peak_source": f"{peaks['src']} bf16 burst {peaks['bf16']} TFLOP/s x 2 (fp8:bf16 nominal)"},
         "kernels": kernels,
         "e2e": {"value": round(whole_job_tflops(ms_e2e_step, world), 2),
@@ -563,8 +568,8 @@ class _DynLinear:
         sx, sw, sg = sc[0:1], sc[4:5], sc[8:9]
         fp8.fp8_linear_fprop(self.q["x"][0], sx, self.q["w"][0], sw, M, N, K, fp8.DYNAMIC, None,
                              self.y)
-        fp8.fp8_linear_dgrad(self.q["g"][0], sg, self.q["w"][1], sw, M, N, K, fp8.DYNAMIC, self.dx)
-        fp8.fp8_linear_wgrad(self.q["g"][1], sg, self.q["x"][1], sx, M, N, K, fp8.DYNAMIC, self.dw)
+        fp8.fp8_linear_dgrad_wgrad(self.q["g"][0], self.q["g"][1], sg, self.q["w"][1], sw,
+                                   self.q["x"][1], sx, M, N, K, fp8.DYNAMIC, self.dx, self.dw)
 
 
 def _gemm_line(metric_name, value_tflops, ms, flop, workload, extra, peaks):

@@ -197,6 +197,21 @@ fp8_status fp8_linear_wgrad(const uint8_t *gqt, const float *g_scale,
                             int64_t M, int64_t N, int64_t K, fp8_recipe r,
                             uint16_t *dw, cudaStream_t s);
 
+/* dgrad and wgrad of one backward pass in one launch (tensorwise recipes):
+ * dx = fp8_linear_dgrad(gq, g_scale, wqt, w_scale) and
+ * dw = fp8_linear_wgrad(gqt, g_scale, xqt, x_scale), same arguments, layouts
+ * and results as those two calls (AstrAI page, fp8_linear_backward: the two
+ * products of the backward of one linear).  The GEMMs are independent; on
+ * large shapes whose contraction lengths (N for dgrad, M for wgrad) are
+ * within 2x of each other their output tiles share one persistent launch of
+ * the 2-SM kernel, so neither ends in a partly filled wave; otherwise they
+ * run one after the other.  BLOCK returns FP8_ERR_UNSUPPORTED (its two GEMMs read
+ * different scale layouts of G: use the single calls). */
+fp8_status fp8_linear_dgrad_wgrad(const uint8_t *gq, const uint8_t *gqt, const float *g_scale,
+                                  const uint8_t *wqt, const float *w_scale, const uint8_t *xqt,
+                                  const float *x_scale, int64_t M, int64_t N, int64_t K,
+                                  fp8_recipe r, uint16_t *dx, uint16_t *dw, cudaStream_t s);
+
 /* ------------------------------------------------------------------------ */
 /* Delayed-scaling state (one per weight)                                    */
 /* ------------------------------------------------------------------------ */
@@ -280,7 +295,9 @@ typedef struct {
  *   one launch;
  *   if g: G -> gq, gqt with g_scale_inv (amax[2]) and X -> xqt with the
  *   updated x_scale_inv, one launch; dx = dgrad(gq, g_scale, wqt, scale);
- *   dw = wgrad(gqt, g_scale, xqt, x_scale); lag update of the g scale.
+ *   dw = wgrad(gqt, g_scale, xqt, x_scale) (both through
+ *   fp8_linear_dgrad_wgrad when dx and dw are given); lag update of the g
+ *   scale.
  * Results are those of the single calls in that order.  The forward state
  * update and the backward quantisation do not depend on fprop, so they run on
  * a second stream owned by the library (one per host thread and device),
@@ -292,9 +309,10 @@ typedef struct {
  * `events` (nullable) receives FP8_STEP_NEVENTS cudaEventRecord calls on the
  * stream of each segment (before: the forward quantisation, fprop, the
  * forward state update, the backward quantisation, dgrad, wgrad, the backward
- * state update; and at the end); events between kernels stop their
- * overlap, so the step runs slower while they are recorded.  Argument checks
- * happen before anything is enqueued. */
+ * state update; and at the end; with both dx and dw the combined launch lies
+ * between events 4 and 5 and event 6 follows event 5 directly); events
+ * between kernels stop their overlap, so the step runs slower while they are
+ * recorded.  Argument checks happen before anything is enqueued. */
 fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_linear_step_io *io,
                                    int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
                                    cudaStream_t s);

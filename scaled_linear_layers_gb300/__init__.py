@@ -21,7 +21,8 @@ _LIB = _lib.load()
 
 __all__ = [
     "fp8_amax", "fp8_quantize", "fp8_quantize_transpose", "fp8_linear_fprop",
-    "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_meta_init", "fp8_meta_record",
+    "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_linear_dgrad_wgrad", "fp8_meta_init",
+    "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
     "fp8_linear_step_delayed", "LinearStep", "fp8_quantize_fused_dynamic",
@@ -127,6 +128,14 @@ def fp8_linear_dgrad(gq, g_scale, wqt, w_scale, M, N, K, recipe, dx, stream=None
 def fp8_linear_wgrad(gqt, g_scale, xqt, x_scale, M, N, K, recipe, dw, stream=None):
     _check(_LIB.fp8_linear_wgrad(_ptr(_u8(gqt)), _ptr(g_scale), _ptr(_u8(xqt)), _ptr(x_scale), M,
                                  N, K, recipe, _ptr(dw), _stream(stream)))
+
+
+def fp8_linear_dgrad_wgrad(gq, gqt, g_scale, wqt, w_scale, xqt, x_scale, M, N, K, recipe, dx, dw,
+                           stream=None):
+    _check(_LIB.fp8_linear_dgrad_wgrad(_ptr(_u8(gq)), _ptr(_u8(gqt)), _ptr(g_scale),
+                                       _ptr(_u8(wqt)), _ptr(w_scale), _ptr(_u8(xqt)),
+                                       _ptr(x_scale), M, N, K, recipe, _ptr(dx), _ptr(dw),
+                                       _stream(stream)))
 
 
 class Fp8Meta:

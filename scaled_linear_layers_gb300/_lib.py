@@ -56,6 +56,7 @@ SIGNATURES = {
     "fp8_linear_fprop": (S, [P, P, P, P, I64, I64, I64, S, P, P, P]),
     "fp8_linear_dgrad": (S, [P, P, P, P, I64, I64, I64, S, P, P]),
     "fp8_linear_wgrad": (S, [P, P, P, P, I64, I64, I64, S, P, P]),
+    "fp8_linear_dgrad_wgrad": (S, [P, P, P, P, P, P, P, I64, I64, I64, S, P, P, P]),
     "fp8_meta_init": (S, [ctypes.POINTER(fp8_meta), P, I32, P]),
     "fp8_meta_record": (S, [ctypes.POINTER(fp8_meta), S, P, P]),
     "fp8_meta_refresh": (S, [ctypes.POINTER(fp8_meta), P]),

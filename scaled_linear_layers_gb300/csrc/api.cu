@@ -346,6 +346,23 @@ fp8_status fp8_linear_wgrad(const uint8_t *gqt, const float *g_scale, const uint
                        who, why);
 }
 
+fp8_status fp8_linear_dgrad_wgrad(const uint8_t *gq, const uint8_t *gqt, const float *g_scale,
+                                  const uint8_t *wqt, const float *w_scale, const uint8_t *xqt,
+                                  const float *x_scale, int64_t M, int64_t N, int64_t K,
+                                  fp8_recipe r, uint16_t *dx, uint16_t *dw, cudaStream_t s) {
+    const char *who = "fp8_linear_dgrad_wgrad";
+    if (r == FP8_RECIPE_BLOCK)
+        return fail(FP8_ERR_UNSUPPORTED,
+                    "%s: the block recipe takes fp8_linear_dgrad and fp8_linear_wgrad", who);
+    FP8_TRY(gemm_common(who, gq, g_scale, wqt, w_scale, M, N, K, r, dx, "M", "N", "K"));
+    FP8_TRY(gemm_common(who, gqt, g_scale, xqt, x_scale, M, N, K, r, dw, "M", "N", "K"));
+    const char *why = nullptr;
+    // dX [M,K] = Gq · (Wqᵀ)ᵀ (contraction N); dW [N,K] = Gqᵀ · (Xqᵀ)ᵀ (contraction M)
+    const PairGemm dgrad{gq, wqt, M, K, N, g_scale, w_scale, nullptr, dx};
+    const PairGemm wgrad{gqt, xqt, N, K, M, g_scale, x_scale, nullptr, dw};
+    return cuda_status(launch_gemm_tensor2(dgrad, wgrad, s, &why), who, why);
+}
+
 fp8_status fp8_meta_init(fp8_meta *m, float *dev_block, int32_t interval, cudaStream_t s) {
     const char *who = "fp8_meta_init";
     FP8_NEED(m, who);
@@ -517,13 +534,22 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     }
     if (bwd) {
         FP8_TRY(mark(s));
-        if (io->dx != nullptr)
-            FP8_TRY(fp8_linear_dgrad(io->gq, d + FP8_META_G_SCALE, io->wqt, d + FP8_META_SCALE, M,
-                                     N, K, FP8_RECIPE_DELAYED, io->dx, s));
-        FP8_TRY(mark(s));
-        if (io->dw != nullptr)
-            FP8_TRY(fp8_linear_wgrad(io->gqt, d + FP8_META_G_SCALE, io->xqt, d + FP8_META_X_SCALE,
-                                     M, N, K, FP8_RECIPE_DELAYED, io->dw, s));
+        if (io->dx != nullptr && io->dw != nullptr) {
+            // both backward GEMMs in one launch (they share its waves)
+            FP8_TRY(fp8_linear_dgrad_wgrad(io->gq, io->gqt, d + FP8_META_G_SCALE, io->wqt,
+                                           d + FP8_META_SCALE, io->xqt, d + FP8_META_X_SCALE, M, N,
+                                           K, FP8_RECIPE_DELAYED, io->dx, io->dw, s));
+            FP8_TRY(mark(s));
+        } else {
+            if (io->dx != nullptr)
+                FP8_TRY(fp8_linear_dgrad(io->gq, d + FP8_META_G_SCALE, io->wqt, d + FP8_META_SCALE,
+                                         M, N, K, FP8_RECIPE_DELAYED, io->dx, s));
+            FP8_TRY(mark(s));
+            if (io->dw != nullptr)
+                FP8_TRY(fp8_linear_wgrad(io->gqt, d + FP8_META_G_SCALE, io->xqt,
+                                         d + FP8_META_X_SCALE, M, N, K, FP8_RECIPE_DELAYED, io->dw,
+                                         s));
+        }
         FP8_TRY(mark(s));
         FP8_TRY(fp8_meta_record(m, FP8_SLOT_G, io->amax + 2, s));
     }

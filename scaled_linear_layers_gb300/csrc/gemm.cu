@@ -344,7 +344,10 @@ cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, in
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     const bool use_pair =
         pair_mode == 1 || (pair_mode != 0 && M >= 256 && pair_tiles >= num_sms() / 2);
-    if (use_pair) return launch_gemm_pair(A, B, M, N, K, sa, sb, bias, D, f >= 128 ? f : 0, s, why);
+    if (use_pair) {
+        const PairGemm g{A, B, M, N, K, sa, sb, bias, D};
+        return launch_gemm_pair(&g, 1, f >= 128 ? f : 0, s, why);
+    }
     const int bn = f ? f : choose_bn(M, N, num_sms());
     switch (bn) {
     case 224: return launch_bn<224>(A, B, M, N, K, sa, sb, bias, D, s, why);
@@ -353,6 +356,29 @@ cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, in
     case 128: return launch_bn<128>(A, B, M, N, K, sa, sb, bias, D, s, why);
     default: return launch_bn<256>(A, B, M, N, K, sa, sb, bias, D, s, why);
     }
+}
+
+cudaError_t launch_gemm_tensor2(const PairGemm &a, const PairGemm &b, cudaStream_t s,
+                                const char **why) {
+    const char *pe = getenv("FP8LINEAR_GEMM_PAIR");
+    const int pair_mode = pe ? atoi(pe) : -1;
+    const int64_t pair_tiles = ((a.M + 255) / 256) * ((a.N + 255) / 256) +
+                               ((b.M + 255) / 256) * ((b.N + 255) / 256);
+    // the pairs take tiles round-robin, so sharing a launch pays only when
+    // the two problems' tiles take about as long (contraction lengths within
+    // 2x); a much longer contraction is better alone
+    const int64_t kmax = a.K > b.K ? a.K : b.K, kmin = a.K > b.K ? b.K : a.K;
+    const bool use_pair = pair_mode == 1 || (pair_mode != 0 && a.M >= 256 && b.M >= 256 &&
+                                              pair_tiles >= num_sms() / 2 && kmax <= 2 * kmin);
+    if (use_pair) {
+        // longer tiles first: the last wave holds the shorter ones
+        const PairGemm g[2] = {a.K >= b.K ? a : b, a.K >= b.K ? b : a};
+        const int f = forced_bn();
+        return launch_gemm_pair(g, 2, f >= 128 ? f : 0, s, why);
+    }
+    cudaError_t e = launch_gemm_tensor(a.A, a.B, a.M, a.N, a.K, a.sa, a.sb, a.bias, a.D, s, why);
+    if (e != cudaSuccess) return e;
+    return launch_gemm_tensor(b.A, b.B, b.M, b.N, b.K, b.sa, b.sb, b.bias, b.D, s, why);
 }
 
 }  // namespace fp8

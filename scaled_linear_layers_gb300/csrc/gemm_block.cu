@@ -61,8 +61,17 @@ static_assert(COLS % 32 == 0 && COLS >= 32, "each epilogue warp reads whole 32-c
 constexpr uint32_t TMEM_COLS = GSLOTS * KG * BN;  // 512
 static_assert(TMEM_COLS == 512, "the four block slots fill TMEM");
 constexpr int GROUP_M = 8;
-// per-warp B-row scales: [2 groups in flight][KG blocks][COLS]
-constexpr int SBUF_FLOATS = EPI_WARPS * 2 * KG * COLS;
+// Scales are fetched PD groups ahead of their use.  One group (about 0.7 us
+// at the block workload's speed) measured best: deeper prefetch costs
+// registers the promotion needs (32768 x 8192 x 8192, PD 1/2/3: fprop 1828 /
+// 1772 / 1730, wgrad 1298 / 881 / 886 TFLOP/s).
+#ifndef FP8_BLOCK_PREFETCH
+#define FP8_BLOCK_PREFETCH 1
+#endif
+constexpr int PD = FP8_BLOCK_PREFETCH;
+static_assert(PD >= 1 && PD <= 4, "prefetch distance");
+// per-warp B-row scales: [PD + 1 groups in flight][KG blocks][COLS]
+constexpr int SBUF_FLOATS = EPI_WARPS * (PD + 1) * KG * COLS;
 template <bool kPair>
 constexpr size_t smem_bytes() {
     return 1024 + (size_t)Shape<kPair>::STAGES * Shape<kPair>::STAGE_BYTES +
@@ -281,7 +290,7 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
         // ------------------------------------------------- epilogue (8 warps)
         const int quarter = warp & 3;
         const int group = (warp - 2) >> 2;  // columns group*COLS .. +COLS-1 of the tile
-        float *wbuf = sbuf + (warp - 2) * 2 * KG * COLS;  // this warp's [2][KG][COLS] B-row scales
+        float *wbuf = sbuf + (warp - 2) * (PD + 1) * KG * COLS;  // [PD+1][KG][COLS] B-row scales
         constexpr int PER_LANE = COLS / 32;                // B-row scales each lane stages
         const BlockScales &sc = p.sc;
         bool ok = true;
@@ -301,47 +310,56 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
             uint64_t acc[COLS / 2];  // fp32 accumulators in pairs
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) acc[j] = 0ull;
-            // this group's and the next group's scalar scales
-            float sa_next[KG], sb_next[KG];
+            // scalar scales of the next PD groups (contraction blocks past the
+            // end read the last block's scales and go unused)
+            float sa_pf[PD][KG], sb_pf[PD][KG];
+            auto fetch = [&](int qn, float (&sa)[KG], float (&sb)[KG]) {
 #pragma unroll
-            for (int j = 0; j < KG; ++j) {
-                const int kb = min(j, nk - 1);
-                sa_next[j] = sa_row[(int64_t)kb * sc.sa_k];
-                sb_next[j] = kPerRowB ? 0.f : sb_ptr[(int64_t)kb * sc.sb_k];
-            }
+                for (int j = 0; j < KG; ++j) {
+                    const int kb = min(qn * KG + j, nk - 1);
+                    sa[j] = sa_row[(int64_t)kb * sc.sa_k];
+                    sb[j] = kPerRowB ? 0.f : sb_ptr[(int64_t)kb * sc.sb_k];
+                }
+            };
+#pragma unroll
+            for (int d = 0; d < PD; ++d) fetch(d, sa_pf[d], sb_pf[d]);
+            // per-row B: one cp.async group per contraction group (empty past
+            // the end, so that wait_group counts stay uniform)
             auto stage_scales = [&](int qn) {
-                const int nbn = min(KG, nk - qn * KG);
+                const int nbn = qn < ngroups ? min(KG, nk - qn * KG) : 0;
                 for (int j = 0; j < nbn; ++j) {
                     const float *src = sb_ptr + (int64_t)(qn * KG + j) * sc.sb_k;
-                    float *dst = wbuf + ((qn & 1) * KG + j) * COLS + PER_LANE * lane;
+                    float *dst = wbuf + ((qn % (PD + 1)) * KG + j) * COLS + PER_LANE * lane;
                     asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)),
                                  "l"(src), "n"(PER_LANE * 4)
                                  : "memory");
                 }
                 asm volatile("cp.async.commit_group;" ::: "memory");
             };
-            if (kPerRowB) stage_scales(0);
+            if (kPerRowB)
+                for (int d = 0; d < PD; ++d) stage_scales(d);
             for (int q = 0; q < ngroups; ++q, ++g) {
                 const int nb = min(KG, nk - q * KG);
                 const uint32_t gs = g % GSLOTS, gphase = (g / GSLOTS) & 1u;
                 float sa_cur[KG], sb_cur[KG];
 #pragma unroll
                 for (int j = 0; j < KG; ++j) {
-                    sa_cur[j] = sa_next[j];
-                    sb_cur[j] = sb_next[j];
+                    sa_cur[j] = sa_pf[0][j];
+                    sb_cur[j] = sb_pf[0][j];
                 }
-                if (kPerRowB) {
-                    asm volatile("cp.async.wait_group 0;" ::: "memory");
-                    __syncwarp();  // every lane's part of this group's scales has landed
-                    if (q + 1 < ngroups) stage_scales(q + 1);
-                }
-                if (q + 1 < ngroups) {  // prefetch the next group's scalar scales
+#pragma unroll
+                for (int d = 0; d + 1 < PD; ++d)
 #pragma unroll
                     for (int j = 0; j < KG; ++j) {
-                        const int kb = min((q + 1) * KG + j, nk - 1);
-                        sa_next[j] = sa_row[(int64_t)kb * sc.sa_k];
-                        if (!kPerRowB) sb_next[j] = sb_ptr[(int64_t)kb * sc.sb_k];
+                        sa_pf[d][j] = sa_pf[d + 1][j];
+                        sb_pf[d][j] = sb_pf[d + 1][j];
                     }
+                fetch(q + PD, sa_pf[PD - 1], sb_pf[PD - 1]);
+                if (kPerRowB) {
+                    // this group's copies were the oldest of PD in flight
+                    asm volatile("cp.async.wait_group %0;" ::"n"(PD - 1) : "memory");
+                    __syncwarp();  // every lane's part of this group's scales has landed
+                    stage_scales(q + PD);
                 }
                 if (ok)
                     ok = mbar_wait_bounded<true>(&sfull[gs], gphase, abort_flag, p.wait_limit_ns,
@@ -369,7 +387,7 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                                 mbar_arrive(&sempty[gs]);
                         }
                     }
-                    const float *buf = wbuf + ((q & 1) * KG + j) * COLS;
+                    const float *buf = wbuf + ((q % (PD + 1)) * KG + j) * COLS;
                     const uint64_t fsa = pack2(sa_cur[j], sa_cur[j]);
                     const float f1 = sa_cur[j] * sb_cur[j];
                     const uint64_t fts = pack2(f1, f1);

@@ -11,6 +11,10 @@
 // operand bytes per 128-deep contraction block instead of 128 x (128 + BN),
 // which is what limits the one-CTA kernel.
 //
+// One launch may carry two independent problems (a backward pass's dgrad and
+// wgrad): their tiles form one index space that the persistent pairs walk,
+// so the two GEMMs share waves instead of each ending in a partial one.
+//
 // Synchronisation: both CTAs' TMA loads complete on the leader's `full`
 // barrier (which expects the bytes of both); the leader's MMA commits arrive
 // on `empty` and `tfull` in both CTAs at once (multicast); both CTAs'
@@ -52,20 +56,42 @@ struct PairCfg {
     static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
 };
 
-struct PairArgs {
+struct PairProblem {
     int M, N, K;
     const float *sa, *sb;
     const uint16_t *bias;
     uint16_t *d;
     int64_t ldd;
+    int m_tiles, n_tiles, tiles;
+};
+
+struct PairArgs {
+    PairProblem pr[2];  // pr[1].tiles == 0 for a single problem
     uint64_t wait_limit_ns;
     unsigned int *status;
 };
 
+// Tile index -> problem, pair-row and column tile.  The fields are picked
+// with selects so the argument block is read in place.
+struct TileRef {
+    int pi, tm, tn;
+};
+__device__ __forceinline__ TileRef locate(const PairArgs &p, int tile) {
+    TileRef r;
+    r.pi = tile >= p.pr[0].tiles ? 1 : 0;
+    const int t = r.pi ? tile - p.pr[0].tiles : tile;
+    const int mt = r.pi ? p.pr[1].m_tiles : p.pr[0].m_tiles;
+    const int nt = r.pi ? p.pr[1].n_tiles : p.pr[0].n_tiles;
+    grouped_tile(t, mt, nt, GROUP_M, r.tm, r.tn);
+    return r;
+}
+
 template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    gemm_f8_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
-                        const __grid_constant__ CUtensorMap tma_b, const PairArgs p) {
+    gemm_f8_pair_kernel(const __grid_constant__ CUtensorMap tma_a0,
+                        const __grid_constant__ CUtensorMap tma_b0,
+                        const __grid_constant__ CUtensorMap tma_a1,
+                        const __grid_constant__ CUtensorMap tma_b1, const PairArgs p) {
     using C = PairCfg<BN>;
     constexpr int STAGES = C::STAGES, A_STAGE = C::A_STAGE, B_STAGE = C::B_STAGE;
     constexpr int BNH = C::BNH, BK = C::BK, KSUB = C::KSUB;
@@ -87,9 +113,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int m_tiles = (p.M + 255) / 256, n_tiles = (p.N + BN - 1) / BN;
-    const int num_tiles = m_tiles * n_tiles;
-    const int nk = (p.K + BK - 1) / BK;
+    const int num_tiles = p.pr[0].tiles + p.pr[1].tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -103,8 +127,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
-        tma_prefetch_desc(&tma_a);
-        tma_prefetch_desc(&tma_b);
+        tma_prefetch_desc(&tma_a0);
+        tma_prefetch_desc(&tma_b0);
+        if (p.pr[1].tiles > 0) {
+            tma_prefetch_desc(&tma_a1);
+            tma_prefetch_desc(&tma_b1);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_holder, TMEM_COLS);
@@ -124,10 +152,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                int tm, tn;
-                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
-                const int arow = tm * 256 + (int)rank * 128;
-                const int brow = tn * BN + (int)rank * BNH;
+                const TileRef r = locate(p, tile);
+                const CUtensorMap *ta = r.pi ? &tma_a1 : &tma_a0;
+                const CUtensorMap *tb = r.pi ? &tma_b1 : &tma_b0;
+                const int nk = ((r.pi ? p.pr[1].K : p.pr[0].K) + BK - 1) / BK;
+                const int arow = r.tm * 256 + (int)rank * 128;
+                const int brow = r.tn * BN + (int)rank * BNH;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns,
                                            kStatusTimeoutTma, p.status)) {
@@ -138,9 +168,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
 #pragma unroll
                     for (int ks = 0; ks < KSUB; ++ks) {
-                        tma_load_2d_pair(sA + stage * A_STAGE + ks * C::A_SUB, &tma_a, leader_full,
+                        tma_load_2d_pair(sA + stage * A_STAGE + ks * C::A_SUB, ta, leader_full,
                                          kb * BK + 128 * ks, arow);
-                        tma_load_2d_pair(sB + stage * B_STAGE + ks * C::B_SUB, &tma_b, leader_full,
+                        tma_load_2d_pair(sB + stage * B_STAGE + ks * C::B_SUB, tb, leader_full,
                                          kb * BK + 128 * ks, brow);
                     }
                     if (++stage == STAGES) {
@@ -169,6 +199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             int it = 0;
             for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++it) {
+                const int nk = ((tile >= p.pr[0].tiles ? p.pr[1].K : p.pr[0].K) + BK - 1) / BK;
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p.wait_limit_ns,
@@ -209,7 +240,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ---------------------------------------------- epilogue (both CTAs)
         const int quarter = warp & 3;
-        const float s = __fmul_rn(*p.sa, *p.sb);
         int it = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
             const int acc = it & 1;
@@ -218,10 +248,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                               kStatusTimeoutEpilogue, p.status);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
-            int tm, tn;
-            grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+            const TileRef tr = locate(p, tile);
+            const int tm = tr.tm, tn = tr.tn;
+            const int pM = tr.pi ? p.pr[1].M : p.pr[0].M;
+            const int pN = tr.pi ? p.pr[1].N : p.pr[0].N;
+            const uint16_t *bias = tr.pi ? p.pr[1].bias : p.pr[0].bias;
+            const float s = tr.pi ? __fmul_rn(*p.pr[1].sa, *p.pr[1].sb)
+                                  : __fmul_rn(*p.pr[0].sa, *p.pr[0].sb);
             const int row = tm * 256 + (int)rank * 128 + quarter * 32 + lane;
-            uint16_t *drow = p.d + (int64_t)row * p.ldd;
+            uint16_t *drow = (tr.pi ? p.pr[1].d : p.pr[0].d) +
+                             (int64_t)row * (tr.pi ? p.pr[1].ldd : p.pr[0].ldd);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
@@ -230,14 +266,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                    r);
                 tmem_ld_wait();
                 const int col = tn * BN + c * 32;
-                if (row < p.M && col < p.N) {
+                if (row < pM && col < pN) {
                     uint32_t packed[16];
-                    if (p.bias != nullptr) {
+                    if (bias != nullptr) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float b0 = __uint_as_float((uint32_t)p.bias[col + 2 * j] << 16);
+                            const float b0 = __uint_as_float((uint32_t)bias[col + 2 * j] << 16);
                             const float b1 =
-                                __uint_as_float((uint32_t)p.bias[col + 2 * j + 1] << 16);
+                                __uint_as_float((uint32_t)bias[col + 2 * j + 1] << 16);
                             packed[j] =
                                 pack_bf16x2(__fadd_rn(__fmul_rn(__uint_as_float(r[2 * j]), s), b0),
                                             __fadd_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), s), b1));
@@ -251,7 +287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     uint4 *dst = reinterpret_cast<uint4 *>(drow + col);
                     dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                     dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    if (col + 16 < p.N) {
+                    if (col + 16 < pN) {
                         dst[2] = make_uint4(packed[8], packed[9], packed[10], packed[11]);
                         dst[3] = make_uint4(packed[12], packed[13], packed[14], packed[15]);
                     }
@@ -274,9 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int BN>
-cudaError_t launch_pair_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
-                           const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
-                           cudaStream_t s, const char **why) {
+cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char **why) {
     using C = PairCfg<BN>;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -288,38 +322,50 @@ cudaError_t launch_pair_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    CUtensorMap ta, tb;
-    if (!make_tmap_k128(&ta, A, M, K, 128) || !make_tmap_k128(&tb, B, N, K, C::BNH)) {
-        *why = "cuTensorMapEncodeTiled failed";
-        return cudaErrorInvalidValue;
-    }
+    CUtensorMap ta[2], tb[2];
     PairArgs args;
-    args.M = (int)M;
-    args.N = (int)N;
-    args.K = (int)K;
-    args.sa = sa;
-    args.sb = sb;
-    args.bias = bias;
-    args.d = D;
-    args.ldd = N;
+    int64_t tiles = 0;
+    for (int i = 0; i < 2; ++i) {
+        const PairGemm &q = g[i < n ? i : 0];  // an absent second problem: copies, no tiles
+        if (!make_tmap_k128(&ta[i], q.A, q.M, q.K, 128) ||
+            !make_tmap_k128(&tb[i], q.B, q.N, q.K, C::BNH)) {
+            *why = "cuTensorMapEncodeTiled failed";
+            return cudaErrorInvalidValue;
+        }
+        PairProblem &pr = args.pr[i];
+        pr.M = (int)q.M;
+        pr.N = (int)q.N;
+        pr.K = (int)q.K;
+        pr.sa = q.sa;
+        pr.sb = q.sb;
+        pr.bias = q.bias;
+        pr.d = q.D;
+        pr.ldd = q.N;
+        pr.m_tiles = (int)((q.M + 255) / 256);
+        pr.n_tiles = (int)((q.N + BN - 1) / BN);
+        pr.tiles = i < n ? pr.m_tiles * pr.n_tiles : 0;
+        tiles += pr.tiles;
+    }
     args.wait_limit_ns = g_wait_limit_ns;
     args.status = device_status_word();
-    const int64_t tiles = ((M + 255) / 256) * ((N + BN - 1) / BN);
     const int64_t pairs = num_sms() / 2;
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    return launch_pdl(gemm_f8_pair_kernel<BN>, grid, NUM_THREADS, C::SMEM_BYTES, s, ta, tb, args);
+    return launch_pdl(gemm_f8_pair_kernel<BN>, grid, NUM_THREADS, C::SMEM_BYTES, s, ta[0], tb[0],
+                      ta[1], tb[1], args);
 }
 
 }  // namespace
 
 // Same cost model as the one-CTA chooser, per SM of a pair: waves of 256 x BN
-// tiles over the pairs times the bytes each SM streams per block, 128 + BN/2.
-int choose_pair_bn(int64_t M, int64_t N, int pairs) {
+// tiles (of all the launch's problems) over the pairs times the bytes each SM
+// streams per block, 128 + BN/2.
+int choose_pair_bn(const PairGemm *g, int n, int pairs) {
     static const int cand[] = {256, 224, 192, 160, 128};
     int best = 256;
     double best_cost = 1e30;
     for (int bn : cand) {
-        const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+        int64_t tiles = 0;
+        for (int i = 0; i < n; ++i) tiles += ((g[i].M + 255) / 256) * ((g[i].N + bn - 1) / bn);
         const int64_t waves = (tiles + pairs - 1) / pairs;
         const double cost = (double)waves * (128 + bn / 2);
         if (cost < best_cost - 1e-9) {
@@ -330,15 +376,17 @@ int choose_pair_bn(int64_t M, int64_t N, int pairs) {
     return best;
 }
 
-cudaError_t launch_gemm_pair(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
-                             const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
-                             int bn, cudaStream_t s, const char **why) {
-    switch (bn ? bn : choose_pair_bn(M, N, num_sms() / 2)) {
-    case 224: return launch_pair_bn<224>(A, B, M, N, K, sa, sb, bias, D, s, why);
-    case 192: return launch_pair_bn<192>(A, B, M, N, K, sa, sb, bias, D, s, why);
-    case 160: return launch_pair_bn<160>(A, B, M, N, K, sa, sb, bias, D, s, why);
-    case 128: return launch_pair_bn<128>(A, B, M, N, K, sa, sb, bias, D, s, why);
-    default: return launch_pair_bn<256>(A, B, M, N, K, sa, sb, bias, D, s, why);
+cudaError_t launch_gemm_pair(const PairGemm *g, int n, int bn, cudaStream_t s, const char **why) {
+    if (n < 1 || n > 2) {
+        *why = "a pair launch takes one or two problems";
+        return cudaErrorInvalidValue;
+    }
+    switch (bn ? bn : choose_pair_bn(g, n, num_sms() / 2)) {
+    case 224: return launch_pair_bn<224>(g, n, s, why);
+    case 192: return launch_pair_bn<192>(g, n, s, why);
+    case 160: return launch_pair_bn<160>(g, n, s, why);
+    case 128: return launch_pair_bn<128>(g, n, s, why);
+    default: return launch_pair_bn<256>(g, n, s, why);
     }
 }
 

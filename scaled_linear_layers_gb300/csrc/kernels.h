@@ -82,11 +82,22 @@ cudaError_t launch_gemm_tensor(const uint8_t *A, const uint8_t *B, int64_t M, in
                                const float *sa, const float *sb, const uint16_t *bias,
                                uint16_t *D, cudaStream_t s, const char **why);
 
-// The 2-SM (CTA pair) kernel behind launch_gemm_tensor for large problems;
-// bn = 0 lets it choose the N tile.
-cudaError_t launch_gemm_pair(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
-                             const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
-                             int bn, cudaStream_t s, const char **why);
+// One tensorwise GEMM as launch_gemm_tensor takes it.
+struct PairGemm {
+    const uint8_t *A, *B;
+    int64_t M, N, K;
+    const float *sa, *sb;
+    const uint16_t *bias;
+    uint16_t *D;
+};
+// The 2-SM (CTA pair) kernel behind launch_gemm_tensor for large problems:
+// n = 1 or 2 independent problems in one launch; bn = 0 lets it choose the N
+// tile (one for all problems).
+cudaError_t launch_gemm_pair(const PairGemm *g, int n, int bn, cudaStream_t s, const char **why);
+// Two tensorwise GEMMs: one pair launch when their tiles fill at least a wave
+// of pairs and their contraction lengths are within 2x, else one launch each.
+cudaError_t launch_gemm_tensor2(const PairGemm &a, const PairGemm &b, cudaStream_t s,
+                                const char **why);
 
 // Block-scaled variant: the contraction is split into 128-blocks; A's scale
 // of (row i, block kb) is sa[i * sa_row + kb * sa_k]; B's scale of (row j,

@@ -244,8 +244,9 @@ def dynamic_linear_gpu(x, w, g):
     y, dx, dw = bf16_out(M, N), bf16_out(M, K), bf16_out(N, K)
     X, W, G = res["x"], res["w"], res["g"]
     fp8.fp8_linear_fprop(X[0], X[2], W[0], W[2], M, N, K, fp8.DYNAMIC, None, y)
-    fp8.fp8_linear_dgrad(G[0], G[2], W[1], W[2], M, N, K, fp8.DYNAMIC, dx)
-    fp8.fp8_linear_wgrad(G[1], G[2], X[1], X[2], M, N, K, fp8.DYNAMIC, dw)
+    # the backward pair through the one-launch entry point, as the MLP workload runs it
+    fp8.fp8_linear_dgrad_wgrad(G[0], G[1], G[2], W[1], W[2], X[1], X[2], M, N, K, fp8.DYNAMIC,
+                               dx, dw)
     fp8.fp8_check_device_status()
     return res, y, dx, dw
 

@@ -173,3 +173,47 @@ def test_gemm_zero_k_tail_and_ragged_tiles():
     _, ref, bound = oracle.gemm(A, B, np.float32(1.0), np.float32(1.0))
     assert oracle.gemm_tolerance_ok(got[:M], ref, bound).all()
     assert np.all(got[M:] == 123.0)  # rows past M untouched
+
+
+@pytest.mark.parametrize("mode", ["auto", "pair"])
+@pytest.mark.parametrize("shape", [(256, 256, 256), (384, 640, 1152), (1024, 512, 768),
+                                   (2048, 4096, 1024)])
+def test_dgrad_wgrad_in_one_launch(shape, mode, monkeypatch):
+    """fp8_linear_dgrad_wgrad: dX = gs*ws Gq Wq and dW = gs*xs Gqᵀ Xq against
+    the oracle, and bit-equal to the two single calls.  "pair" forces the
+    shared 2-SM launch (with 256-row tiles: M=384 leaves half a tile of
+    dgrad rows past the matrix); "auto" lets the library choose."""
+    if mode == "pair":
+        monkeypatch.setenv("FP8LINEAR_GEMM_PAIR", "1")
+    M, N, K = shape
+    rng = np.random.default_rng(M + 3 * N + 5 * K)
+    G = random_codes(rng, (M, N))
+    W = random_codes(rng, (N, K))
+    X = random_codes(rng, (M, K))
+    gs, ws, xs = np.float32(0.0031), np.float32(0.07), np.float32(0.0009)
+    Gt, Wt, Xt = (np.ascontiguousarray(a.T) for a in (G, W, X))
+    dx, dw = bf16_out(M, K), bf16_out(N, K)
+    fp8.fp8_linear_dgrad_wgrad(to_dev_u8(G), to_dev_u8(Gt), scal(gs), to_dev_u8(Wt), scal(ws),
+                               to_dev_u8(Xt), scal(xs), M, N, K, fp8.DELAYED, dx, dw)
+    fp8.fp8_check_device_status()
+    got_dx, got_dw = dx.float().cpu().numpy(), dw.float().cpu().numpy()
+    rows = rng.choice(M, min(M, 96), replace=False)
+    ii, jj = np.repeat(rows, K), np.tile(np.arange(K), len(rows))
+    _, ref, bound = oracle.gemm_entries(G, Wt, gs, ws, ii, jj)
+    assert oracle.gemm_tolerance_ok(got_dx[ii, jj], ref, bound).all()
+    rows = rng.choice(N, min(N, 96), replace=False)
+    ii, jj = np.repeat(rows, K), np.tile(np.arange(K), len(rows))
+    _, ref, bound = oracle.gemm_entries(Gt, Xt, gs, xs, ii, jj)
+    assert oracle.gemm_tolerance_ok(got_dw[ii, jj], ref, bound).all()
+    # the single entry points (same kernel family) give the same bits
+    got1 = run_tensor_gemm(G, Wt, gs, ws, which="dgrad")
+    got2 = run_tensor_gemm(Gt, Xt, gs, xs, which="wgrad")
+    assert np.array_equal(got1, got_dx) and np.array_equal(got2, got_dw)
+
+
+def test_dgrad_wgrad_rejects_block_recipe():
+    z = torch.zeros(128 * 128, dtype=torch.uint8, device="cuda")
+    s = torch.ones(1, device="cuda")
+    out = bf16_out(128, 128)
+    with pytest.raises(fp8.Fp8Error, match="FP8_ERR_UNSUPPORTED"):
+        fp8.fp8_linear_dgrad_wgrad(z, z, s, z, s, z, s, 128, 128, 128, fp8.BLOCK, out, out)
