@@ -135,9 +135,9 @@ class ClockSampler:
 # --------------------------------------------------------------- GPU arm ---
 
 # the step's event segments; dgrad and wgrad run as one launch (between the
-# fifth and sixth events), the sixth segment is empty
-SEGMENTS = ["quant_fwd", "gemm_fprop", "meta_fwd", "quant_bwd", "gemm_dgrad_wgrad", "empty",
-            "meta_bwd"]
+# sixth and seventh events), the last segment is empty
+SEGMENTS = ["quant_fwd", "gemm_fprop", "meta_fwd", "quant_bwd", "meta_bwd", "gemm_dgrad_wgrad",
+            "empty"]
 
 
 class Step:

@@ -220,13 +220,14 @@ fp8_status fp8_linear_dgrad_wgrad(const uint8_t *gq, const uint8_t *gqt, const f
  *   [2] x_scale [3] x_scale_inv    activation, lagged one call
  *   [4] g_scale [5] g_scale_inv    gradient, lagged one call
  *   [6]     x scale used by the forward GEMM of the step in progress
- *           (written by fp8_linear_step_delayed; otherwise unused)
- *   [7]     reserved
+ *   [7]     g scale used by the backward GEMMs of the step in progress
+ *           ([6] and [7] are written by fp8_linear_step_delayed; otherwise
+ *           unused)
  *   [8 .. 8+interval) amax_history ring
  * Source: AstrAI fp8_state.py FP8TensorMeta (all fields start at 1). */
 enum { FP8_META_SCALE = 0, FP8_META_SCALE_INV = 1, FP8_META_X_SCALE = 2,
        FP8_META_X_SCALE_INV = 3, FP8_META_G_SCALE = 4, FP8_META_G_SCALE_INV = 5,
-       FP8_META_X_SCALE_FWD = 6, FP8_META_HISTORY = 8 };
+       FP8_META_X_SCALE_FWD = 6, FP8_META_G_SCALE_BWD = 7, FP8_META_HISTORY = 8 };
 #define FP8_META_FLOATS(interval) (8 + (interval))
 
 typedef struct {
@@ -294,12 +295,14 @@ typedef struct {
  *   history[idx] = amax[1] and the lag update of the x scale from amax[0],
  *   one launch;
  *   if g: G -> gq, gqt with g_scale_inv (amax[2]) and X -> xqt with the
- *   updated x_scale_inv, one launch; dx = dgrad(gq, g_scale, wqt, scale);
- *   dw = wgrad(gqt, g_scale, xqt, x_scale) (both through
- *   fp8_linear_dgrad_wgrad when dx and dw are given); lag update of the g
- *   scale.
- * Results are those of the single calls in that order.  The forward state
- * update and the backward quantisation do not depend on fprop, so they run on
+ *   updated x_scale_inv, one launch, which also copies g_scale to slot
+ *   FP8_META_G_SCALE_BWD; the lag update of the g scale from amax[2];
+ *   dx = dgrad(gq, g scale of that slot, wqt, scale) and
+ *   dw = wgrad(gqt, g scale of that slot, xqt, x_scale) (both through
+ *   fp8_linear_dgrad_wgrad when dx and dw are given).
+ * Results are those of the single calls of the page's order (the GEMMs read
+ * the scales the page's GEMMs read).  The forward state update, the backward
+ * quantisation and the g-scale update do not depend on fprop, so they run on
  * a second stream owned by the library (one per host thread and device),
  * forked from and joined back into `s` with events: the memory-bound
  * quantisation overlaps the compute-bound GEMM.  To the caller everything is
@@ -308,11 +311,11 @@ typedef struct {
  * same scale_inv, which gives the same bytes.  M, N, K multiples of 16.
  * `events` (nullable) receives FP8_STEP_NEVENTS cudaEventRecord calls on the
  * stream of each segment (before: the forward quantisation, fprop, the
- * forward state update, the backward quantisation, dgrad, wgrad, the backward
- * state update; and at the end; with both dx and dw the combined launch lies
- * between events 4 and 5 and event 6 follows event 5 directly); events
- * between kernels stop their overlap, so the step runs slower while they are
- * recorded.  Argument checks happen before anything is enqueued. */
+ * forward state update, the backward quantisation, the backward state
+ * update, dgrad, wgrad; and at the end; with both dx and dw the combined
+ * launch lies between events 5 and 6 and event 7 follows event 6 directly);
+ * events between kernels stop their overlap, so the step runs slower while
+ * they are recorded.  Argument checks happen before anything is enqueued. */
 fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_linear_step_io *io,
                                    int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
                                    cudaStream_t s);

@@ -522,36 +522,41 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     FP8_TRY(cuda_status(launch_meta_fwd(d, m->idx, io->amax + 0, io->amax + 1, s2), who));
     m->idx = (m->idx + 1) % m->interval;
     if (bwd) {
-        // backward: G (q and qt) and X again, transposed, with the updated scale
+        // backward: G (q and qt) and X again, transposed, with the updated
+        // scale; the launch keeps the g scale the backward GEMMs must use, so
+        // the lag update of the g scale runs right after it, off the GEMMs'
+        // critical path
         FP8_TRY(mark(s2));
         DelayedQuantJob jg{io->g, M, N, d + FP8_META_G_SCALE_INV, io->gq, io->gqt, io->amax + 2};
         DelayedQuantJob jxt{io->x, M, K, d + FP8_META_X_SCALE_INV, nullptr, io->xqt, nullptr};
-        FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s2), who));
+        FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s2, d + FP8_META_G_SCALE,
+                                                         d + FP8_META_G_SCALE_BWD),
+                            who));
+        FP8_TRY(mark(s2));
+        FP8_TRY(fp8_meta_record(m, FP8_SLOT_G, io->amax + 2, s2));
     }
     if (overlap) {  // join
         FP8_TRY(cuda_status(cudaEventRecord(side->join, s2), who));
         FP8_TRY(cuda_status(cudaStreamWaitEvent(s, side->join, 0), who));
     }
     if (bwd) {
+        const float *gs = d + FP8_META_G_SCALE_BWD;
         FP8_TRY(mark(s));
         if (io->dx != nullptr && io->dw != nullptr) {
             // both backward GEMMs in one launch (they share its waves)
-            FP8_TRY(fp8_linear_dgrad_wgrad(io->gq, io->gqt, d + FP8_META_G_SCALE, io->wqt,
-                                           d + FP8_META_SCALE, io->xqt, d + FP8_META_X_SCALE, M, N,
-                                           K, FP8_RECIPE_DELAYED, io->dx, io->dw, s));
+            FP8_TRY(fp8_linear_dgrad_wgrad(io->gq, io->gqt, gs, io->wqt, d + FP8_META_SCALE,
+                                           io->xqt, d + FP8_META_X_SCALE, M, N, K,
+                                           FP8_RECIPE_DELAYED, io->dx, io->dw, s));
             FP8_TRY(mark(s));
         } else {
             if (io->dx != nullptr)
-                FP8_TRY(fp8_linear_dgrad(io->gq, d + FP8_META_G_SCALE, io->wqt, d + FP8_META_SCALE,
-                                         M, N, K, FP8_RECIPE_DELAYED, io->dx, s));
+                FP8_TRY(fp8_linear_dgrad(io->gq, gs, io->wqt, d + FP8_META_SCALE, M, N, K,
+                                         FP8_RECIPE_DELAYED, io->dx, s));
             FP8_TRY(mark(s));
             if (io->dw != nullptr)
-                FP8_TRY(fp8_linear_wgrad(io->gqt, d + FP8_META_G_SCALE, io->xqt,
-                                         d + FP8_META_X_SCALE, M, N, K, FP8_RECIPE_DELAYED, io->dw,
-                                         s));
+                FP8_TRY(fp8_linear_wgrad(io->gqt, gs, io->xqt, d + FP8_META_X_SCALE, M, N, K,
+                                         FP8_RECIPE_DELAYED, io->dw, s));
         }
-        FP8_TRY(mark(s));
-        FP8_TRY(fp8_meta_record(m, FP8_SLOT_G, io->amax + 2, s));
     }
     while (events != nullptr && ev < FP8_STEP_NEVENTS) FP8_TRY(mark(s));
     return FP8_OK;

@@ -204,8 +204,11 @@ struct QtJobs {
     float *snap_dst;
 };
 
+// Four CTAs per SM for every mode: the row+column mode would otherwise take
+// 120 registers and run two (32768 x 8192: 4625 against 3839 GB/s); the
+// others fit 64 registers anyway.
 template <int kMode>
-__global__ void __launch_bounds__(256) quantize_transpose_kernel(const QtJobs jobs) {
+__global__ void __launch_bounds__(256, 4) quantize_transpose_kernel(const QtJobs jobs) {
     __shared__ uint32_t tile[128 * 32];
     __shared__ uint32_t red[8];
     __shared__ uint32_t colmax[8][128];
