@@ -72,6 +72,7 @@ def _load():
             "orc_gemm": (None, [P, P, I, I, I, F, F, P, P, P, P]),
             "orc_gemm_block_entries": (None, [P, P, I, I, P, P, I, P, P, I, P, P, P]),
             "orc_pad_rows": (I, [P, I, I, I, P]),
+            "orc_bias_grad": (None, [P, I, I, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -276,6 +277,29 @@ def pad_rows(x: np.ndarray, multiple: int = 16) -> np.ndarray:
     got = _load().orc_pad_rows(_p(x), rows, cols, multiple, _p(out))
     assert got == padded
     return out
+
+
+def bias_grad(g: np.ndarray):
+    """Column sums of the bf16 matrix g [rows, cols] (the bias gradient of a
+    linear), exact in fp64: returns (exact sums, their bf16 roundings, column
+    sums of |g|)."""
+    g = _bf16(g)
+    rows, cols = g.shape
+    d, db, mag = (np.empty(cols, np.float64) for _ in range(3))
+    _load().orc_bias_grad(_p(g), rows, cols, _p(d), _p(db), _p(mag))
+    return d, db, mag
+
+
+def bias_grad_tolerance_ok(got: np.ndarray, ref_bf16: np.ndarray, mag: np.ndarray, rows: int):
+    """A GPU bias gradient summed in fp32 in a fixed order and rounded once to
+    bf16 passes if |got - bf16(ref)| <= 2^-8 |ref| + (17 + ceil(rows/128)) *
+    2^-23 * sum|g|: the bf16 rounding is at most half an ulp (2^-9 relative)
+    on each of got and bf16(ref), and a sum of k fp32 terms taken in at most
+    17 + rows/128 sequential additions errs by at most that many units of
+    2^-24 times the sum of magnitudes (doubled for slack)."""
+    got = np.asarray(got, np.float64)
+    bound = 2.0 ** -8 * np.abs(ref_bf16) + (17 + -(-rows // 128)) * 2.0 ** -23 * mag
+    return np.abs(got - ref_bf16) <= bound
 
 
 def gemm_tolerance_ok(d_gpu: np.ndarray, d_ref_bf16: np.ndarray, bound: np.ndarray):

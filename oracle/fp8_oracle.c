@@ -343,3 +343,30 @@ int64_t orc_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t mult
     memset(out + rows * cols, 0, (size_t)((padded - rows) * cols) * sizeof(uint16_t));
     return padded;
 }
+
+/* ---------------------------------------------------------- bias gradient */
+
+/* Bias gradient of the linear y = x w^T + b: dbias[n] = sum over the rows m of
+ * the upstream gradient g[m][n].  The AstrAI page's fp8_linear_backward takes
+ * aten::linear_backward's output mask, whose third entry asks for this
+ * gradient; the page gives no arithmetic for it, so the definition is written
+ * out: each column summed in fp64 (bf16 values have 8 significant bits, so
+ * the sum of up to 2^45 of them is exact), then rounded once to bf16.
+ * d gets the exact sums, d_bf16 their bf16 roundings and mag the column sums
+ * of |g| (the scale of a summation-error bound). */
+void orc_bias_grad(const uint16_t *g, int64_t rows, int64_t cols, double *d, double *d_bf16,
+                   double *mag)
+{
+    for (int64_t n = 0; n < cols; ++n) {
+        d[n] = 0.0;
+        mag[n] = 0.0;
+    }
+    for (int64_t m = 0; m < rows; ++m)
+        for (int64_t n = 0; n < cols; ++n) {
+            double v = (double)orc_bf16_to_f32(g[m * cols + n]);
+            d[n] += v;
+            mag[n] += fabs(v);
+        }
+    for (int64_t n = 0; n < cols; ++n) d_bf16[n] = orc_round_to_bf16(d[n]);
+}
+

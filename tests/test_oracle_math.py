@@ -314,3 +314,46 @@ def test_fp8_storage_bytes_page_example():
     q, _ = oracle.quantize(np.zeros((16, 16), np.uint16), np.float32(1.0))
     assert q.itemsize == ex["itemsize"]
     assert int(np.prod(ex["shape"])) * q.itemsize == ex["bytes"]
+
+
+# -------------------------------------------------------------- bias grad ---
+# dbias = column sums of the upstream gradient (the third output of the
+# linear backward whose output mask the AstrAI page's fp8_linear_backward
+# passes through).
+
+def test_bias_grad_closed_form_on_integer_columns():
+    rows, cols = 96, 40
+    col_vals = np.arange(1, cols + 1, dtype=np.float32) * np.where(np.arange(cols) % 2, -1, 1)
+    g = synth.f32_to_bf16_bits(np.tile(col_vals, (rows, 1)))
+    d, db, mag = oracle.bias_grad(g)
+    assert np.array_equal(d, rows * col_vals.astype(np.float64))
+    assert np.array_equal(db, d)  # 96*k has at most 8 significant bits for k <= 40
+    assert np.array_equal(mag, np.abs(d))
+    # +v / -v alternating down a column cancels exactly
+    alt = synth.f32_to_bf16_bits(np.outer(np.where(np.arange(rows) % 2, -1.0, 1.0),
+                                          np.linspace(0.1, 7.0, cols)).astype(np.float32))
+    d, db, mag = oracle.bias_grad(alt)
+    assert not d.any() and not db.any() and (mag > 0).all()
+
+
+def test_bias_grad_matches_library_sum_and_is_order_free():
+    g = synth.normal_bf16((500, 72), 1e-3, seed=3, tensor="g")
+    d, db, _ = oracle.bias_grad(g)
+    ref = torch.from_numpy(_f32(g)).double().sum(0).numpy()
+    assert np.array_equal(d, ref)  # exact: bf16 values sum exactly in fp64
+    perm = np.random.default_rng(0).permutation(500)
+    d2, db2, _ = oracle.bias_grad(np.ascontiguousarray(g[perm]))
+    assert np.array_equal(d2, d) and np.array_equal(db2, db)
+    assert all(db[i] == oracle.round_to_bf16(d[i]) for i in range(72))
+
+
+def test_bias_grad_ignores_pad_rows_and_tolerance_catches_an_error():
+    g = synth.normal_bf16((3858, 24), 1e-3, seed=4, tensor="g")
+    gp = oracle.pad_rows(g, 16)
+    d, db, mag = oracle.bias_grad(g)
+    dp, dbp, magp = oracle.bias_grad(gp)
+    assert np.array_equal(d, dp) and np.array_equal(db, dbp) and np.array_equal(mag, magp)
+    assert oracle.bias_grad_tolerance_ok(db, db, mag, 3858).all()
+    # a one-term error (one row's value counted twice) is far outside the bound
+    bad = db + np.abs(_f32(g)[0]).astype(np.float64) * 8
+    assert not oracle.bias_grad_tolerance_ok(bad, db, mag, 3858).all()
