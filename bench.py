@@ -713,6 +713,8 @@ def workload_sweep(args):
         bs = torch.empty((R, C // 128), dtype=torch.float32, device=dev)
         bsi = torch.empty((R, C // 128), dtype=torch.float32, device=dev)
         ws = torch.zeros(fp8.fp8_quantize_fused_workspace_bytes() // 4, dtype=torch.int32, device=dev)
+        dbias = torch.empty(C, dtype=torch.bfloat16, device=dev)
+        dws = torch.empty(fp8.fp8_dbias_workspace_bytes(R, C) // 4, dtype=torch.float32, device=dev)
         s, si, a = sc[0:1], sc[1:2], sc[2:3]
         si.fill_(100.0)
         cases = {
@@ -721,6 +723,8 @@ def workload_sweep(args):
             "quantize_dynamic_2pass": (5, lambda i: fp8.fp8_quantize(xs[i % nbuf], fp8.DYNAMIC, s, sc[3:4], q, a)),
             "quantize_dynamic_fused": (3, lambda i: fp8.fp8_quantize_fused_dynamic(xs[i % nbuf], s, sc[3:4], q, None, a, ws)),
             "cast_transpose_delayed": (4, lambda i: fp8.fp8_quantize_transpose(xs[i % nbuf], fp8.DELAYED, None, si, q, qt, amax_out=a)),
+            # the same plus the bias gradient (column sums) in the same read
+            "cast_transpose_dbias": (4, lambda i: fp8.fp8_quantize_transpose_dbias(xs[i % nbuf], fp8.DELAYED, None, si, q, qt, dbias, dws, amax_out=a)),
             "block_1x128": (3, lambda i: fp8.fp8_quantize(xs[i % nbuf], fp8.BLOCK, bs, bsi, q, None)),
         }
         row = {"n": n}

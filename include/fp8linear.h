@@ -117,6 +117,22 @@ fp8_status fp8_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols,
                                   float *scale_t, float *scale_inv_t, float *amax_out,
                                   cudaStream_t s);
 
+/* Bias gradient fused into the quantisation of the upstream gradient g
+ * [rows, cols] (the linear backward's third output, which the AstrAI page's
+ * fp8_linear_backward asks for through its output mask): the results of
+ * fp8_quantize_transpose(g, ..., r, scale, scale_inv, q, qt, NULL, NULL,
+ * amax_out), plus dbias [cols] bf16 = the column sums of g, summed in fp32
+ * (per 128-row tile in a fixed order, then over the tiles in order) and
+ * rounded once to bf16.  The cast pass reads g once for both.  `workspace`:
+ * fp8_dbias_workspace_bytes(rows, cols) bytes of device memory (per-tile
+ * partial sums), overwritten.  r: DELAYED or DYNAMIC (others
+ * FP8_ERR_UNSUPPORTED).  rows = 0 gives dbias = 0. */
+size_t fp8_dbias_workspace_bytes(int64_t rows, int64_t cols);
+fp8_status fp8_quantize_transpose_dbias(const uint16_t *g, int64_t rows, int64_t cols,
+                                        fp8_recipe r, float *scale, float *scale_inv, uint8_t *q,
+                                        uint8_t *qt, float *amax_out, uint16_t *dbias,
+                                        float *workspace, cudaStream_t s);
+
 /* Bytes of workspace fp8_quantize_fused_dynamic needs (16 KiB). */
 size_t fp8_quantize_fused_workspace_bytes(void);
 
@@ -279,6 +295,8 @@ typedef struct {
     uint16_t *y;          /* [M,N] bf16 output                                */
     uint16_t *dx;         /* [M,K] bf16 input gradient (nullable)             */
     uint16_t *dw;         /* [N,K] bf16 weight gradient, overwritten (nullable) */
+    uint16_t *dbias;      /* [N] bf16 bias gradient (nullable; needs g)        */
+    float *dbias_workspace; /* fp8_dbias_workspace_bytes(M, N) (with dbias)    */
 } fp8_linear_step_io;
 
 /* Number of events fp8_linear_step_delayed records when given an array. */
@@ -296,7 +314,9 @@ typedef struct {
  *   one launch;
  *   if g: G -> gq, gqt with g_scale_inv (amax[2]) and X -> xqt with the
  *   updated x_scale_inv, one launch, which also copies g_scale to slot
- *   FP8_META_G_SCALE_BWD; the lag update of the g scale from amax[2];
+ *   FP8_META_G_SCALE_BWD (and, with dbias, sums G's columns as
+ *   fp8_quantize_transpose_dbias does); the lag update of the g scale from
+ *   amax[2];
  *   dx = dgrad(gq, g scale of that slot, wqt, scale) and
  *   dw = wgrad(gqt, g scale of that slot, xqt, x_scale) (both through
  *   fp8_linear_dgrad_wgrad when dx and dw are given).

@@ -22,6 +22,7 @@ _LIB = _lib.load()
 __all__ = [
     "fp8_amax", "fp8_quantize", "fp8_quantize_transpose", "fp8_linear_fprop",
     "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_linear_dgrad_wgrad", "fp8_meta_init",
+    "fp8_dbias_workspace_bytes", "fp8_quantize_transpose_dbias",
     "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
@@ -130,6 +131,19 @@ def fp8_linear_wgrad(gqt, g_scale, xqt, x_scale, M, N, K, recipe, dw, stream=Non
                                  N, K, recipe, _ptr(dw), _stream(stream)))
 
 
+def fp8_dbias_workspace_bytes(rows, cols):
+    return _LIB.fp8_dbias_workspace_bytes(rows, cols)
+
+
+def fp8_quantize_transpose_dbias(g, recipe, scale, scale_inv, q, qt, dbias, workspace,
+                                 amax_out=None, stream=None):
+    rows, cols = g.shape
+    _check(_LIB.fp8_quantize_transpose_dbias(_ptr(_bf16(g)), rows, cols, recipe, _ptr(scale),
+                                             _ptr(scale_inv), _ptr(_u8(q)), _ptr(_u8(qt)),
+                                             _ptr(amax_out),
+                                             _ptr(dbias), _ptr(workspace), _stream(stream)))
+
+
 def fp8_linear_dgrad_wgrad(gq, gqt, g_scale, wqt, w_scale, xqt, x_scale, M, N, K, recipe, dx, dw,
                            stream=None):
     _check(_LIB.fp8_linear_dgrad_wgrad(_ptr(_u8(gq)), _ptr(_u8(gqt)), _ptr(g_scale),
@@ -213,7 +227,7 @@ class LinearStep:
     built once from torch tensors (the caller keeps them alive), so a step
     is a single C call.  ``set_inputs`` swaps the x / g / w pointers."""
 
-    def __init__(self, M, N, K, device="cuda", backward=True, bias=None):
+    def __init__(self, M, N, K, device="cuda", backward=True, bias=None, dbias=False):
         u8 = dict(dtype=torch.uint8, device=device)
         bf = dict(dtype=torch.bfloat16, device=device)
         self.M, self.N, self.K = M, N, K
@@ -228,8 +242,14 @@ class LinearStep:
             self.dx, self.dw = torch.empty((M, K), **bf), torch.empty((N, K), **bf)
         else:
             self.xqt = self.gq = self.gqt = self.dx = self.dw = None
+        self.dbias = self.dbias_workspace = None
+        if backward and dbias:
+            self.dbias = torch.empty(N, **bf)
+            self.dbias_workspace = torch.empty(
+                _LIB.fp8_dbias_workspace_bytes(M, N) // 4, dtype=torch.float32, device=device)
         self.io = _lib.fp8_linear_step_io()
-        for name in ("xq", "xqt", "wq", "wqt", "gq", "gqt", "amax", "y", "dx", "dw", "bias"):
+        for name in ("xq", "xqt", "wq", "wqt", "gq", "gqt", "amax", "y", "dx", "dw", "bias",
+                     "dbias", "dbias_workspace"):
             t = getattr(self, name)
             setattr(self.io, name, None if t is None else t.data_ptr())
 

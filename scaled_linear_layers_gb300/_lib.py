@@ -38,7 +38,7 @@ class fp8_meta(ctypes.Structure):
 class fp8_linear_step_io(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("x", "w", "g", "bias", "xq", "xqt", "wq", "wqt", "gq", "gqt", "amax", "y", "dx",
-                 "dw")]
+                 "dw", "dbias", "dbias_workspace")]
 
 
 FP8_STEP_NEVENTS = 8
@@ -50,6 +50,8 @@ SIGNATURES = {
     "fp8_amax": (S, [P, I64, P, P]),
     "fp8_quantize": (S, [P, I64, I64, S, P, P, P, P, P]),
     "fp8_quantize_transpose": (S, [P, I64, I64, S, P, P, P, P, P, P, P, P]),
+    "fp8_dbias_workspace_bytes": (ctypes.c_size_t, [I64, I64]),
+    "fp8_quantize_transpose_dbias": (S, [P, I64, I64, S, P, P, P, P, P, P, P, P]),
     "fp8_quantize_fused_workspace_bytes": (ctypes.c_size_t, []),
     "fp8_quantize_fused_dynamic": (S, [P, I64, I64, P, P, P, P, P, P, P]),
     "fp8_quantize_fused_dynamic_noalloc": (S, [P, I64, I64, P, P, P, P, P, P]),

@@ -213,6 +213,57 @@ fp8_status fp8_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols,
                        who);
 }
 
+size_t fp8_dbias_workspace_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return (size_t)((rows + 127) / 128) * (size_t)cols * sizeof(float);
+}
+
+fp8_status fp8_quantize_transpose_dbias(const uint16_t *g, int64_t rows, int64_t cols,
+                                        fp8_recipe r, float *scale, float *scale_inv, uint8_t *q,
+                                        uint8_t *qt, float *amax_out, uint16_t *dbias,
+                                        float *workspace, cudaStream_t s) {
+    const char *who = "fp8_quantize_transpose_dbias";
+    if (r != FP8_RECIPE_DELAYED && r != FP8_RECIPE_DYNAMIC)
+        return fail(FP8_ERR_UNSUPPORTED, "%s: tensorwise recipes only (DELAYED, DYNAMIC)", who);
+    if (rows * cols > 0) {
+        FP8_NEED(dbias, who);
+        FP8_NEED(workspace, who);
+    }
+    FP8_ALIGN(dbias, who);
+    FP8_ALIGN(workspace, who);
+    // the quantisation's own checks, then the fused launch and the reduction
+    if (rows < 0 || cols < 0 || rows > 0x7FFFFFFF || cols > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: bad shape [%lld, %lld]", who, (long long)rows,
+                    (long long)cols);
+    FP8_TRY(check_dim16(who, "rows", rows, 16));
+    FP8_TRY(check_dim16(who, "cols", cols, 16));
+    if (rows * cols > 0) {
+        FP8_NEED(g, who);
+        FP8_NEED(qt, who);
+    }
+    FP8_ALIGN(g, who);
+    FP8_ALIGN(q, who);
+    FP8_ALIGN(qt, who);
+    FP8_NEED(scale_inv, who);
+    if (r == FP8_RECIPE_DYNAMIC) {
+        FP8_NEED(scale, who);
+        FP8_NEED(amax_out, who);
+    }
+    FP8_TRY(check_device(who));
+    if (rows * cols == 0) {
+        if (cols > 0) FP8_TRY(cuda_status(cudaMemsetAsync(dbias, 0, cols * 2, s), who));
+        return cuda_status(launch_quantize_transpose(g, rows, cols, r == FP8_RECIPE_DYNAMIC ? 1 : 0,
+                                                     scale, scale_inv, q, qt, nullptr, nullptr,
+                                                     amax_out, s),
+                           who);
+    }
+    FP8_TRY(cuda_status(launch_quantize_transpose(g, rows, cols, r == FP8_RECIPE_DYNAMIC ? 1 : 0,
+                                                  scale, scale_inv, q, qt, nullptr, nullptr,
+                                                  amax_out, s, workspace),
+                        who));
+    return cuda_status(launch_colsum_reduce(workspace, rows, cols, dbias, s), who);
+}
+
 size_t fp8_quantize_fused_workspace_bytes(void) { return kFusedWorkspaceBytes; }
 
 fp8_status fp8_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols, float *scale,
@@ -481,8 +532,12 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
         FP8_NEED(io->gqt, who);
         FP8_NEED(io->xqt, who);
     }
+    if (io->dbias != nullptr) {
+        if (!bwd) return fail(FP8_ERR_NULL, "%s: dbias needs g", who);
+        FP8_NEED(io->dbias_workspace, who);
+    }
     const void *ptrs[] = {io->x, io->w, io->g, io->bias, io->xq, io->xqt, io->wq, io->wqt,
-                          io->gq, io->gqt, io->y, io->dx, io->dw};
+                          io->gq, io->gqt, io->y, io->dx, io->dw, io->dbias, io->dbias_workspace};
     for (const void *p : ptrs)
         if (p != nullptr && !aligned16(p))
             return fail(FP8_ERR_ALIGNMENT, "%s: a buffer is not 16-byte aligned", who);
@@ -529,9 +584,13 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
         FP8_TRY(mark(s2));
         DelayedQuantJob jg{io->g, M, N, d + FP8_META_G_SCALE_INV, io->gq, io->gqt, io->amax + 2};
         DelayedQuantJob jxt{io->x, M, K, d + FP8_META_X_SCALE_INV, nullptr, io->xqt, nullptr};
+        jg.colsum = io->dbias != nullptr ? io->dbias_workspace : nullptr;  // G's column sums
         FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s2, d + FP8_META_G_SCALE,
                                                          d + FP8_META_G_SCALE_BWD),
                             who));
+        if (io->dbias != nullptr)
+            FP8_TRY(cuda_status(launch_colsum_reduce(io->dbias_workspace, M, N, io->dbias, s2),
+                                who));
         FP8_TRY(mark(s2));
         FP8_TRY(fp8_meta_record(m, FP8_SLOT_G, io->amax + 2, s2));
     }

@@ -40,10 +40,15 @@ cudaError_t launch_quantize_rowtiles(const uint16_t *x, int64_t rows, int64_t co
                                      float *scale_inv, uint8_t *q, float *amax_out,
                                      cudaStream_t s);
 // mode: 0 tensor/delayed, 1 tensor/dynamic, 2 128x128 tiles, 3 row+column tiles
+// colsum (tensor modes, nullable): per-tile column sums of x, [ceil(rows/128),
+// cols] fp32, for launch_colsum_reduce.
 cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, int mode,
                                       float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
                                       float *scale_t, float *scale_inv_t, float *amax_out,
-                                      cudaStream_t s);
+                                      cudaStream_t s, float *colsum = nullptr);
+// dbias [cols] bf16 = the per-tile column sums added in tile order.
+cudaError_t launch_colsum_reduce(const float *partials, int64_t rows, int64_t cols,
+                                 uint16_t *dbias, cudaStream_t s);
 // Two delayed-scaling quantisations in one launch (q and/or qt per tensor,
 // rows and cols multiples of 16).  amax_out, when given, must already be
 // zero: this launcher does not clear it.  If snap_dst is given, the launch
@@ -54,6 +59,7 @@ struct DelayedQuantJob {
     const float *scale_inv;
     uint8_t *q, *qt;
     float *amax_out;
+    float *colsum = nullptr;  // per-tile column sums (bias gradient), nullable
 };
 cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const DelayedQuantJob &b,
                                          cudaStream_t s, const float *snap_src = nullptr,

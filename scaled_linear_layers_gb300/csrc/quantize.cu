@@ -194,6 +194,9 @@ struct QtJob {
     const float *scale_src;
     uint8_t *q, *qt;
     float *amax_out, *scale, *scale_inv, *scale_t, *scale_inv_t;
+    // tensor modes: per-tile column sums of x, [tiles_y, C] fp32 (nullable);
+    // colsum_reduce_kernel turns them into the bias gradient
+    float *colsum;
 };
 struct QtJobs {
     QtJob job[2];
@@ -250,6 +253,40 @@ __global__ void __launch_bounds__(256, 4) quantize_transpose_kernel(const QtJobs
         if (bx == 0 && by == 0 && t == 0) {
             *scale = s;
             *scale_inv = si_all;
+        }
+    }
+
+    // column sums of the tile (bias gradient): per thread over its 8 rows in
+    // row order, then lanes l and l^16, then the 8 warps in warp order
+    if ((kMode == kTensorDelayed || kMode == kTensorDynamic) && J.colsum != nullptr) {
+        float cs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cs[e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                cs[2 * e] = __fadd_rn(cs[2 * e], bf16_lo(w4[e]));
+                cs[2 * e + 1] = __fadd_rn(cs[2 * e + 1], bf16_hi(w4[e]));
+            }
+        }
+        float *colsum_sh = reinterpret_cast<float *>(&colmax[0][0]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, cs[e], 16);
+            cs[e] = lane < 16 ? __fadd_rn(cs[e], o) : __fadd_rn(o, cs[e]);
+        }
+        if (lane < 16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) colsum_sh[warp * 128 + chunk * 8 + e] = cs[e];
+        }
+        __syncthreads();
+        if (t < 128 && c0 + t < C) {
+            float acc = colsum_sh[t];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) acc = __fadd_rn(acc, colsum_sh[w * 128 + t]);
+            J.colsum[(int64_t)by * C + c0 + t] = acc;
         }
     }
 
@@ -375,6 +412,22 @@ __global__ void __launch_bounds__(256, 4) quantize_transpose_kernel(const QtJobs
     tile_transpose_store(tile, qt, R, C, r0, c0);
 }
 
+// ------------------------------------------------------- bias gradient ---
+// dbias[n] = bf16( sum over the tiles' column sums of column n, in tile
+// order ); one thread per column.
+__global__ void __launch_bounds__(256) colsum_reduce_kernel(const float *__restrict__ part,
+                                                            int tiles_y, int cols,
+                                                            uint16_t *__restrict__ dbias) {
+    pdl_wait_prior();
+    pdl_allow_next();
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= cols) return;
+    float acc = 0.f;
+    for (int b = 0; b < tiles_y; ++b) acc = __fadd_rn(acc, part[(int64_t)b * cols + n]);
+    const __nv_bfloat16 h = __float2bfloat16_rn(acc);
+    dbias[n] = *reinterpret_cast<const uint16_t *>(&h);
+}
+
 // --------------------------------------------------------------- padding ---
 
 __global__ void __launch_bounds__(256) pad_rows_kernel_v16(const uint4 *__restrict__ x,
@@ -463,6 +516,7 @@ static QtJob make_job(const uint16_t *x, int64_t rows, int64_t cols, const float
     j.scale_inv = scale_inv;
     j.scale_t = scale_t;
     j.scale_inv_t = scale_inv_t;
+    j.colsum = nullptr;
     return j;
 }
 
@@ -480,7 +534,7 @@ static cudaError_t launch_jobs(int mode, const QtJobs &jobs, cudaStream_t s) {
 cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t cols, int mode,
                                       float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
                                       float *scale_t, float *scale_inv_t, float *amax_out,
-                                      cudaStream_t s) {
+                                      cudaStream_t s, float *colsum) {
     cudaError_t e;
     const float *src = nullptr;
     if (mode == kTensorDynamic) {
@@ -494,6 +548,7 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
     QtJobs jobs;
     jobs.job[0] = make_job(x, rows, cols, src, scale, scale_inv, q, qt, scale_t, scale_inv_t,
                            mode == kTensorDynamic ? nullptr : amax_out);
+    jobs.job[0].colsum = colsum;
     jobs.job[1] = jobs.job[0];
     jobs.job[1].tiles = 0;
     jobs.snap_src = nullptr;
@@ -509,9 +564,19 @@ cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const Delayed
     jobs.snap_dst = snap_dst;
     jobs.job[0] = make_job(a.x, a.rows, a.cols, a.scale_inv, nullptr, nullptr, a.q, a.qt, nullptr,
                            nullptr, a.amax_out);
+    jobs.job[0].colsum = a.colsum;
     jobs.job[1] = make_job(b.x, b.rows, b.cols, b.scale_inv, nullptr, nullptr, b.q, b.qt, nullptr,
                            nullptr, b.amax_out);
+    jobs.job[1].colsum = b.colsum;
     return launch_jobs(kTensorDelayed, jobs, s);
+}
+
+cudaError_t launch_colsum_reduce(const float *partials, int64_t rows, int64_t cols,
+                                 uint16_t *dbias, cudaStream_t s) {
+    if (cols == 0) return cudaSuccess;
+    const int tiles_y = (int)((rows + 127) / 128);
+    return launch_pdl(colsum_reduce_kernel, (int)((cols + 255) / 256), 256, 0, s, partials,
+                      tiles_y, (int)cols, dbias);
 }
 
 cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,

@@ -118,3 +118,18 @@ def test_pad_tokens_rejects_overlap_and_bad_multiple(lib):
     assert lib.fp8_pad_tokens(p, 10, 16, 16, p, ctypes.byref(out_rows), None) == 2
     assert "overlap" in lib.fp8_last_error().decode()
     assert out_rows.value == 16
+
+
+def test_dbias_entry_point_host_checks(lib):
+    good = ctypes.c_void_p(0x2000)
+    bad = ctypes.c_void_p(0x2002)
+    assert lib.fp8_dbias_workspace_bytes(4096, 4096) == 32 * 4096 * 4
+    assert lib.fp8_dbias_workspace_bytes(3872, 48) == 31 * 48 * 4
+    assert lib.fp8_dbias_workspace_bytes(0, 48) == 0
+    args = lambda r, ws, db: (good, 256, 128, r, good, good, good, good, None, db, ws, None)
+    assert lib.fp8_quantize_transpose_dbias(*args(2, good, good)) == 4  # block: unsupported
+    assert lib.fp8_quantize_transpose_dbias(*args(0, None, good)) == 1  # no workspace
+    assert lib.fp8_quantize_transpose_dbias(*args(0, good, None)) == 1  # no dbias
+    assert lib.fp8_quantize_transpose_dbias(*args(0, good, bad)) == 3   # misaligned dbias
+    assert lib.fp8_quantize_transpose_dbias(good, 250, 128, 0, good, good, good, good, None,
+                                            good, good, None) == 3     # rows % 16

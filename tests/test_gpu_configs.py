@@ -206,6 +206,46 @@ def test_composite_step_matches_oracle_20_steps():
         check_gemm(step.dw.float().cpu().numpy(), b["dw"])
 
 
+def test_composite_step_with_bias_and_bias_gradient():
+    """The step with a bias (added in fprop's epilogue) and the bias gradient
+    fused into G's quantisation (a padded token count: 3872 = 3858 rounded up
+    to 16, the SpecForge page's example, G's pad rows zero)."""
+    M, N, K = 3872, 256, 384
+    w = synth.normal_bf16((N, K), 0.02, 9, "w")
+    b = synth.normal_bf16((N,), 0.1, 9, "bias")
+    wd, bd = dev_bf16(w), dev_bf16(b)
+    step = fp8.LinearStep(M, N, K, bias=bd, dbias=True)
+    meta = fp8.Fp8Meta(16)
+    count = [0]
+    st = ost.State(16)
+    om = st.new_meta()
+    rng = np.random.default_rng(9)
+    for t in range(3):
+        x = synth.normal_bf16((M, K), 1.0, 9, "x", t)
+        g = synth.normal_bf16((M, N), 1e-3, 9, "g", t)
+        g[3858:] = 0
+        step.set_inputs(dev_bf16(x), wd, dev_bf16(g))
+        fp8.fp8_linear_step_delayed(meta, count, step)
+        fp8.fp8_check_device_status()
+        st.step()
+        ey, edx, edw = sample_entries(rng, M, N), sample_entries(rng, M, K), sample_entries(rng, N, K)
+        f = ost.linear_forward(om, x, w, ey, bias=b)
+        bw = ost.linear_backward(om, g, x, w, edx, edw)
+        check_gemm(step.y.float().cpu().numpy()[ey], f["y"])
+        check_gemm(step.dx.float().cpu().numpy()[edx], bw["dx"])
+        check_gemm(step.dw.float().cpu().numpy()[edw], bw["dw"])
+        _, ref_db, mag = oracle.bias_grad(g)
+        got = step.dbias.float().cpu().numpy().astype(np.float64)
+        assert oracle.bias_grad_tolerance_ok(got, ref_db, mag, M).all(), t
+        # the same bits as the stand-alone fused entry point on the same G
+        db2 = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+        ws2 = torch.empty_like(step.dbias_workspace)
+        fp8.fp8_quantize_transpose_dbias(dev_bf16(g), fp8.DELAYED, None,
+                                         torch.ones(1, device="cuda"), u8(M, N), u8(N, M), db2,
+                                         ws2)
+        assert torch.equal(db2, step.dbias)
+
+
 def test_composite_step_forward_only_and_events():
     M, N, K = 128, 256, 128
     x = synth.normal_bf16((M, K), 1.0, 8, "x")

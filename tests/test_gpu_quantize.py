@@ -123,6 +123,51 @@ def test_quantize_transpose_without_q():
     assert np.array_equal(host_u8(qt), ref_q.T)
 
 
+@pytest.mark.parametrize("shape", [(16, 16), (144, 272), (1024, 4096), (3872, 4096)])
+@pytest.mark.parametrize("recipe", ["delayed", "dynamic"])
+def test_quantize_transpose_dbias(shape, recipe):
+    """G's cast+transpose with the bias gradient (column sums of G) fused in:
+    bytes, amax and scales as the plain cast+transpose; dbias within the
+    fp32-summation bound of the oracle's exact sums; zero pad rows appended
+    to G change no bit of dbias."""
+    R, C = shape
+    g = synth.normal_with_outliers_bf16(shape, 1e-3, seed=R + C, tensor="g")
+    q, qt, s, si, a = u8(R, C), u8(C, R), f32(), f32(), f32()
+    db = torch.empty(C, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(fp8.fp8_dbias_workspace_bytes(R, C) // 4, dtype=torch.float32, device="cuda")
+    rec = fp8.DELAYED if recipe == "delayed" else fp8.DYNAMIC
+    if recipe == "delayed":
+        si.fill_(float(np.float32(448.0) / np.float32(0.01)))
+    fp8.fp8_quantize_transpose_dbias(dev_bf16(g), rec, s, si, q, qt, db, ws, amax_out=a)
+    q2, qt2, s2, si2, a2 = u8(R, C), u8(C, R), f32(), f32(), f32()
+    si2.copy_(si) if recipe == "delayed" else None
+    fp8.fp8_quantize_transpose(dev_bf16(g), rec, s2, si2, q2, qt2, amax_out=a2)
+    fp8.fp8_check_device_status()
+    assert torch.equal(q, q2) and torch.equal(qt, qt2) and torch.equal(a, a2)
+    _, ref_db, mag = oracle.bias_grad(g)
+    got = host_bf16(db).astype(np.uint32) << 16
+    got = got.view(np.float32).astype(np.float64)
+    ok = oracle.bias_grad_tolerance_ok(got, ref_db, mag, R)
+    assert ok.all(), f"{(~ok).sum()} columns outside; first {np.argwhere(~ok)[:3].ravel()}"
+    # padding: zero rows append zero tile sums (or add +0 within the last tile)
+    gp = oracle.pad_rows(g, 256)
+    Rp = gp.shape[0]
+    dbp = torch.empty(C, dtype=torch.bfloat16, device="cuda")
+    wsp = torch.empty(fp8.fp8_dbias_workspace_bytes(Rp, C) // 4, dtype=torch.float32,
+                      device="cuda")
+    fp8.fp8_quantize_transpose_dbias(dev_bf16(gp), rec, f32(), si.clone(), u8(Rp, C), u8(C, Rp),
+                                     dbp, wsp, amax_out=f32())
+    assert torch.equal(db, dbp)
+
+
+def test_quantize_transpose_dbias_empty_rows():
+    db = torch.full((32,), 1.0, dtype=torch.bfloat16, device="cuda")
+    si = torch.ones(1, device="cuda")
+    fp8.fp8_quantize_transpose_dbias(torch.empty((0, 32), dtype=torch.bfloat16, device="cuda"),
+                                     fp8.DELAYED, None, si, None, u8(32, 0), db, None)
+    assert not db.float().any()
+
+
 @pytest.mark.parametrize("shape", [(1, 128), (5, 384), (256, 1024), (333, 4096)])
 def test_quantize_rowtiles(shape):
     R, C = shape
