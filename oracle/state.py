@@ -113,13 +113,23 @@ def linear_forward(meta: Meta, x, w, entries=None, bias=None) -> dict:
 
 
 def linear_backward(meta: Meta, g, x, w, entries_dx=None, entries_dw=None,
-                    need=(True, True)) -> dict:
-    """Delayed-scaling backward.  g [M,N]; need = (dX, dW)."""
+                    need=(True, True), saved=None) -> dict:
+    """Delayed-scaling backward.  g [M,N]; need = (dX, dW).
+
+    saved = (xq, x_scale) kept by the forward: the torchao float8 behaviour
+    the SpecForge page ("Add training.fp8_linear", notes under the end-to-end
+    table) credits for its memory saving, float8 activations saved for
+    backward.  None re-quantises x with the current, just-updated x scale,
+    as the AstrAI page's fp8_linear_backward does."""
     used = dict(g_scale=meta.g_scale, g_scale_inv=meta.g_scale_inv,
                 w_scale=meta.scale, x_scale=meta.x_scale, x_scale_inv=meta.x_scale_inv)
     gq, amax_g = quantize(g, meta.g_scale_inv)
     wq, _ = quantize(w, meta.scale_inv)
-    xq, _ = quantize(x, meta.x_scale_inv)
+    if saved is None:
+        xq, _ = quantize(x, meta.x_scale_inv)
+    else:
+        xq, used["x_scale"] = saved
+        used["x_scale_inv"] = None
     out = dict(gq=gq, amax_g=amax_g, xq_bwd=xq, used=used)
     if need[0]:
         # dX [M,K] = Gq [M,N] · Wq [N,K]: contraction over N, B operand = Wqᵀ [K,N]
@@ -127,18 +137,22 @@ def linear_backward(meta: Meta, g, x, w, entries_dx=None, entries_dw=None,
     if need[1]:
         # dW [N,K] = Gqᵀ [N,M] · Xq [M,K]: contraction over M
         out["dw"] = _gemm_out(transpose_u8(gq), transpose_u8(xq), meta.g_scale,
-                              meta.x_scale, entries_dw)
+                              used["x_scale"], entries_dw)
     meta.g_scale, meta.g_scale_inv = lag_update(amax_g)
     return out
 
 
-def delayed_training_step(state: State, meta: Meta, x, w, g, entries=None) -> dict:
+def delayed_training_step(state: State, meta: Meta, x, w, g, entries=None,
+                          save_xq_fwd: bool = False) -> dict:
     """One training step: step() at autocast entry, forward, backward.
-    entries = dict(y=(ii,jj), dx=(ii,jj), dw=(ii,jj)) or None for full."""
+    entries = dict(y=(ii,jj), dx=(ii,jj), dw=(ii,jj)) or None for full.
+    save_xq_fwd: the backward uses the forward's Xq and x scale (see
+    linear_backward)."""
     state.step()
     e = entries or {}
     fwd = linear_forward(meta, x, w, e.get("y"))
-    bwd = linear_backward(meta, g, x, w, e.get("dx"), e.get("dw"))
+    saved = (fwd["xq"], fwd["used"]["x_scale"]) if save_xq_fwd else None
+    bwd = linear_backward(meta, g, x, w, e.get("dx"), e.get("dw"), saved=saved)
     return dict(fwd=fwd, bwd=bwd, step_count=state.step_count, meta=meta.snapshot())
 
 

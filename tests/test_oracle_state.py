@@ -153,3 +153,39 @@ def test_delayed_training_step_end_to_end_small():
         assert y.shape == (M, N)
         assert out["bwd"]["dx"][0].shape == (M, K) and out["bwd"]["dw"][0].shape == (N, K)
     assert st.step_count == 3
+
+
+def test_saved_forward_xq_agrees_when_the_x_scale_does_not_move():
+    """Backward with the forward's saved Xq (the float8-activations-saved-for-
+    backward behaviour of the SpecForge page) against the AstrAI page's
+    re-quantisation: the two differ only through the x scale, so when this
+    step's x has the same amax as the previous step's (the lag update then
+    writes back the same scale) every byte and every dW entry agrees; when
+    the amax moves, the re-quantised Xq follows the new scale and the saved
+    one does not."""
+    M, K, N = 48, 64, 32
+    w = synth.normal_bf16((N, K), 0.02, seed=1, tensor="w")
+    x0 = synth.normal_bf16((M, K), 1.0, seed=1, tensor="x", step=0)
+    g = synth.normal_bf16((M, N), 1e-3, seed=1, tensor="g", step=1)
+    # x1: a row permutation of x0 (same amax) -> the x scale does not move
+    x1 = np.ascontiguousarray(x0[::-1])
+    runs = {}
+    for save in (False, True):
+        st = State(16)
+        m = st.new_meta()
+        delayed_training_step(st, m, x0, w, g)
+        runs[save] = delayed_training_step(st, m, x1, w, g, save_xq_fwd=save)
+    a, b = runs[False]["bwd"], runs[True]["bwd"]
+    assert np.array_equal(a["xq_bwd"], b["xq_bwd"])
+    assert np.array_equal(a["dw"][0], b["dw"][0]) and np.array_equal(a["dx"][0], b["dx"][0])
+    assert b["used"]["x_scale"] == runs[True]["fwd"]["used"]["x_scale"]
+    # a step whose amax differs: the saved Xq keeps the forward scale
+    x2 = synth.normal_bf16((M, K), 3.0, seed=1, tensor="x", step=2)
+    outs = {}
+    for save in (False, True):
+        st = State(16)
+        m = st.new_meta()
+        delayed_training_step(st, m, x0, w, g)
+        outs[save] = delayed_training_step(st, m, x2, w, g, save_xq_fwd=save)
+    assert np.array_equal(outs[True]["bwd"]["xq_bwd"], outs[True]["fwd"]["xq"])
+    assert not np.array_equal(outs[False]["bwd"]["xq_bwd"], outs[True]["bwd"]["xq_bwd"])
