@@ -268,6 +268,24 @@ fp8_status fp8_meta_record(fp8_meta *m, fp8_slot which, const float *amax_dev, c
  * (FP8TensorMeta.refresh). */
 fp8_status fp8_meta_refresh(fp8_meta *m, cudaStream_t s);
 
+/* Checkpoint of one meta: the scaling state a restore must keep (the NeMo
+ * Speech page "feat(speechlm2): add padding-free packed speech training"
+ * lists a fix that keeps checkpoint metadata through a restore; the state is
+ * FP8TensorMeta's on the AstrAI page plus the step counter): a host byte blob = header (magic "F8MS", version 1, interval, idx,
+ * step_count; host byte order) + the FP8_META_FLOATS(interval) floats of the
+ * device block.  fp8_meta_state_bytes gives the blob size (0 for a bad
+ * interval).  Save copies the device block out and synchronises `s` before
+ * returning; load checks the header, copies the floats into dev_block
+ * (caller-owned, FP8_META_FLOATS(interval) floats, 16-byte aligned),
+ * synchronises `s`, then sets m (dev, interval, idx) and *step_count
+ * (nullable).  A run restored from a blob continues bit for bit as the run
+ * that saved it. */
+size_t fp8_meta_state_bytes(int32_t interval);
+fp8_status fp8_meta_save(const fp8_meta *m, int64_t step_count, void *host_buf, size_t bytes,
+                         cudaStream_t s);
+fp8_status fp8_meta_load(fp8_meta *m, float *dev_block, int64_t *step_count, const void *host_buf,
+                         size_t bytes, cudaStream_t s);
+
 /* FP8State.step: *step_count += 1 and, when it becomes a multiple of
  * interval, refresh every meta in metas[0..n).  Call once per training step
  * (at autocast entry), never again for the backward of the same step. */
@@ -297,7 +315,19 @@ typedef struct {
     uint16_t *dw;         /* [N,K] bf16 weight gradient, overwritten (nullable) */
     uint16_t *dbias;      /* [N] bf16 bias gradient (nullable; needs g)        */
     float *dbias_workspace; /* fp8_dbias_workspace_bytes(M, N) (with dbias)    */
+    int32_t flags;        /* FP8_STEP_* bits, 0 for the default step           */
 } fp8_linear_step_io;
+
+/* Step option: keep the forward's quantised activation for the backward
+ * instead of quantising x again there.  The forward launch writes xqt
+ * (Xq transposed, with the x scale fprop uses) beside xq, the backward reads
+ * no x, and wgrad takes that forward x scale (slot FP8_META_X_SCALE_FWD).
+ * This is the torchao float8 behaviour the SpecForge page credits for its
+ * memory saving (float8 activations saved for backward); the default follows
+ * the AstrAI page (x re-quantised in backward with the just-updated scale).
+ * The two agree bit for bit whenever that update leaves the x scale as it
+ * was (amax of this step's x equal to the previous one's). */
+#define FP8_STEP_SAVE_XQ_FWD 1
 
 /* Number of events fp8_linear_step_delayed records when given an array. */
 #define FP8_STEP_NEVENTS 8

@@ -193,6 +193,29 @@ class Fp8Meta:
     def history(self):
         return self.block[META_HISTORY:]
 
+    def save(self, step_count: int = 0, stream=None) -> bytes:
+        """The meta's checkpoint blob (fp8_meta_save; synchronises the stream)."""
+        n = _LIB.fp8_meta_state_bytes(self.c.interval)
+        buf = ctypes.create_string_buffer(n)
+        _check(_LIB.fp8_meta_save(ctypes.byref(self.c), int(step_count), buf, n,
+                                  _stream(stream)))
+        return buf.raw
+
+    @classmethod
+    def load(cls, blob: bytes, device="cuda", stream=None):
+        """A meta restored from a blob of save(); returns (meta, step_count)."""
+        hdr = ctypes.create_string_buffer(blob, len(blob))
+        interval = int.from_bytes(blob[8:12], "little", signed=True)
+        if not 1 <= interval <= 1024:
+            raise Fp8Error(2, "not a saved fp8 meta state")
+        self = cls.__new__(cls)
+        self.block = torch.empty(8 + interval, dtype=torch.float32, device=device)
+        self.c = _lib.fp8_meta()
+        cnt = ctypes.c_int64(0)
+        _check(_LIB.fp8_meta_load(ctypes.byref(self.c), _ptr(self.block), ctypes.byref(cnt), hdr,
+                                  len(blob), _stream(stream)))
+        return self, cnt.value
+
     @property
     def idx(self) -> int:
         return self.c.idx
@@ -227,7 +250,8 @@ class LinearStep:
     built once from torch tensors (the caller keeps them alive), so a step
     is a single C call.  ``set_inputs`` swaps the x / g / w pointers."""
 
-    def __init__(self, M, N, K, device="cuda", backward=True, bias=None, dbias=False):
+    def __init__(self, M, N, K, device="cuda", backward=True, bias=None, dbias=False,
+                 save_xq_fwd=False):
         u8 = dict(dtype=torch.uint8, device=device)
         bf = dict(dtype=torch.bfloat16, device=device)
         self.M, self.N, self.K = M, N, K
@@ -252,6 +276,7 @@ class LinearStep:
                      "dbias", "dbias_workspace"):
             t = getattr(self, name)
             setattr(self.io, name, None if t is None else t.data_ptr())
+        self.io.flags = _lib.FP8_STEP_SAVE_XQ_FWD if save_xq_fwd else 0
 
     def set_inputs(self, x, w, g=None):
         for t in (x, w) + ((g,) if g is not None else ()):

@@ -38,10 +38,11 @@ class fp8_meta(ctypes.Structure):
 class fp8_linear_step_io(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("x", "w", "g", "bias", "xq", "xqt", "wq", "wqt", "gq", "gqt", "amax", "y", "dx",
-                 "dw", "dbias", "dbias_workspace")]
+                 "dw", "dbias", "dbias_workspace")] + [("flags", ctypes.c_int32)]
 
 
 FP8_STEP_NEVENTS = 8
+FP8_STEP_SAVE_XQ_FWD = 1
 
 P, I64, I32, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
 S = ctypes.c_int  # fp8_status / enums
@@ -62,6 +63,9 @@ SIGNATURES = {
     "fp8_meta_init": (S, [ctypes.POINTER(fp8_meta), P, I32, P]),
     "fp8_meta_record": (S, [ctypes.POINTER(fp8_meta), S, P, P]),
     "fp8_meta_refresh": (S, [ctypes.POINTER(fp8_meta), P]),
+    "fp8_meta_state_bytes": (ctypes.c_size_t, [I32]),
+    "fp8_meta_save": (S, [ctypes.POINTER(fp8_meta), I64, P, ctypes.c_size_t, P]),
+    "fp8_meta_load": (S, [ctypes.POINTER(fp8_meta), P, ctypes.POINTER(I64), P, ctypes.c_size_t, P]),
     "fp8_state_step": (S, [ctypes.POINTER(I64), I32, ctypes.POINTER(fp8_meta), I32, P]),
     "fp8_linear_step_delayed": (S, [ctypes.POINTER(fp8_meta), ctypes.POINTER(I64),
                                     ctypes.POINTER(fp8_linear_step_io), I64, I64, I64, P, P]),

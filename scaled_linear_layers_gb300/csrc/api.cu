@@ -463,6 +463,79 @@ fp8_status fp8_meta_refresh(fp8_meta *m, cudaStream_t s) {
     return cuda_status(launch_meta_refresh(m->dev, m->interval, s), who);
 }
 
+namespace {
+
+// Header of a saved meta state; the device block's floats follow it.
+struct MetaBlobHeader {
+    uint32_t magic, version;
+    int32_t interval, idx;
+    int64_t step_count;
+};
+constexpr uint32_t kMetaBlobMagic = 0x534D3846u;  // "F8MS"
+constexpr uint32_t kMetaBlobVersion = 1;
+
+}  // namespace
+
+size_t fp8_meta_state_bytes(int32_t interval) {
+    if (interval < 1 || interval > 1024) return 0;
+    return sizeof(MetaBlobHeader) + (size_t)FP8_META_FLOATS(interval) * sizeof(float);
+}
+
+fp8_status fp8_meta_save(const fp8_meta *m, int64_t step_count, void *host_buf, size_t bytes,
+                         cudaStream_t s) {
+    const char *who = "fp8_meta_save";
+    FP8_NEED(m, who);
+    FP8_NEED(m->dev, who);
+    FP8_NEED(host_buf, who);
+    if (m->interval < 1 || m->interval > 1024 || m->idx < 0 || m->idx >= m->interval)
+        return fail(FP8_ERR_SHAPE, "%s: corrupt meta", who);
+    const size_t need = fp8_meta_state_bytes(m->interval);
+    if (bytes < need)
+        return fail(FP8_ERR_SHAPE, "%s: buffer of %zu bytes, %zu needed", who, bytes, need);
+    FP8_TRY(check_device(who));
+    MetaBlobHeader h{kMetaBlobMagic, kMetaBlobVersion, m->interval, m->idx, step_count};
+    std::memcpy(host_buf, &h, sizeof h);
+    float *dst = reinterpret_cast<float *>(static_cast<char *>(host_buf) + sizeof h);
+    FP8_TRY(cuda_status(cudaMemcpyAsync(dst, m->dev, FP8_META_FLOATS(m->interval) * sizeof(float),
+                                        cudaMemcpyDeviceToHost, s),
+                        who));
+    return cuda_status(cudaStreamSynchronize(s), who);
+}
+
+fp8_status fp8_meta_load(fp8_meta *m, float *dev_block, int64_t *step_count, const void *host_buf,
+                         size_t bytes, cudaStream_t s) {
+    const char *who = "fp8_meta_load";
+    FP8_NEED(m, who);
+    FP8_NEED(dev_block, who);
+    FP8_NEED(host_buf, who);
+    FP8_ALIGN(dev_block, who);
+    MetaBlobHeader h;
+    if (bytes < sizeof h) return fail(FP8_ERR_SHAPE, "%s: buffer shorter than the header", who);
+    std::memcpy(&h, host_buf, sizeof h);
+    if (h.magic != kMetaBlobMagic || h.version != kMetaBlobVersion)
+        return fail(FP8_ERR_SHAPE, "%s: not a saved fp8 meta state (version %u)", who,
+                    (unsigned)h.version);
+    if (h.interval < 1 || h.interval > 1024 || h.idx < 0 || h.idx >= h.interval)
+        return fail(FP8_ERR_SHAPE, "%s: corrupt state (interval %d, idx %d)", who, h.interval,
+                    h.idx);
+    if (bytes < fp8_meta_state_bytes(h.interval))
+        return fail(FP8_ERR_SHAPE, "%s: buffer of %zu bytes, %zu needed", who, bytes,
+                    fp8_meta_state_bytes(h.interval));
+    FP8_TRY(check_device(who));
+    const float *src =
+        reinterpret_cast<const float *>(static_cast<const char *>(host_buf) + sizeof h);
+    FP8_TRY(cuda_status(cudaMemcpyAsync(dev_block, src,
+                                        FP8_META_FLOATS(h.interval) * sizeof(float),
+                                        cudaMemcpyHostToDevice, s),
+                        who));
+    FP8_TRY(cuda_status(cudaStreamSynchronize(s), who));
+    m->dev = dev_block;
+    m->interval = h.interval;
+    m->idx = h.idx;
+    if (step_count != nullptr) *step_count = h.step_count;
+    return FP8_OK;
+}
+
 fp8_status fp8_state_step(int64_t *step_count, int32_t interval, fp8_meta *metas, int32_t n,
                           cudaStream_t s) {
     const char *who = "fp8_state_step";
@@ -560,7 +633,13 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     // forward: X (lagged x scale, q only) and W (q and qt) in one launch,
     // which also keeps the x scale fprop must use
     FP8_TRY(mark(s));
-    DelayedQuantJob jx{io->x, M, K, d + FP8_META_X_SCALE_INV, io->xq, nullptr, io->amax + 0};
+    if ((io->flags & ~FP8_STEP_SAVE_XQ_FWD) != 0)
+        return fail(FP8_ERR_SHAPE, "%s: unknown flags 0x%x", who, (unsigned)io->flags);
+    const bool save_x = (io->flags & FP8_STEP_SAVE_XQ_FWD) != 0;
+    if (save_x && io->xqt == nullptr)
+        return fail(FP8_ERR_NULL, "%s: FP8_STEP_SAVE_XQ_FWD needs xqt", who);
+    DelayedQuantJob jx{io->x, M, K, d + FP8_META_X_SCALE_INV, io->xq,
+                       save_x ? io->xqt : nullptr, io->amax + 0};
     DelayedQuantJob jw{io->w, N, K, d + FP8_META_SCALE_INV, io->wq, io->wqt, io->amax + 1};
     FP8_TRY(cuda_status(launch_quantize_delayed_pair(jx, jw, s, d + FP8_META_X_SCALE,
                                                      d + FP8_META_X_SCALE_FWD),
@@ -583,7 +662,10 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
         // critical path
         FP8_TRY(mark(s2));
         DelayedQuantJob jg{io->g, M, N, d + FP8_META_G_SCALE_INV, io->gq, io->gqt, io->amax + 2};
-        DelayedQuantJob jxt{io->x, M, K, d + FP8_META_X_SCALE_INV, nullptr, io->xqt, nullptr};
+        // X again, transposed, with the just-updated scale (none when the
+        // forward kept its Xqᵀ)
+        DelayedQuantJob jxt{io->x, save_x ? 0 : M, K, d + FP8_META_X_SCALE_INV, nullptr, io->xqt,
+                            nullptr};
         jg.colsum = io->dbias != nullptr ? io->dbias_workspace : nullptr;  // G's column sums
         FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s2, d + FP8_META_G_SCALE,
                                                          d + FP8_META_G_SCALE_BWD),
@@ -600,12 +682,13 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     }
     if (bwd) {
         const float *gs = d + FP8_META_G_SCALE_BWD;
+        const float *xs = d + (save_x ? FP8_META_X_SCALE_FWD : FP8_META_X_SCALE);
         FP8_TRY(mark(s));
         if (io->dx != nullptr && io->dw != nullptr) {
             // both backward GEMMs in one launch (they share its waves)
             FP8_TRY(fp8_linear_dgrad_wgrad(io->gq, io->gqt, gs, io->wqt, d + FP8_META_SCALE,
-                                           io->xqt, d + FP8_META_X_SCALE, M, N, K,
-                                           FP8_RECIPE_DELAYED, io->dx, io->dw, s));
+                                           io->xqt, xs, M, N, K, FP8_RECIPE_DELAYED, io->dx,
+                                           io->dw, s));
             FP8_TRY(mark(s));
         } else {
             if (io->dx != nullptr)
@@ -613,8 +696,8 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
                                          FP8_RECIPE_DELAYED, io->dx, s));
             FP8_TRY(mark(s));
             if (io->dw != nullptr)
-                FP8_TRY(fp8_linear_wgrad(io->gqt, gs, io->xqt, d + FP8_META_X_SCALE, M, N, K,
-                                         FP8_RECIPE_DELAYED, io->dw, s));
+                FP8_TRY(fp8_linear_wgrad(io->gqt, gs, io->xqt, xs, M, N, K, FP8_RECIPE_DELAYED,
+                                         io->dw, s));
         }
     }
     while (events != nullptr && ev < FP8_STEP_NEVENTS) FP8_TRY(mark(s));

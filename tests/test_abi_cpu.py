@@ -133,3 +133,28 @@ def test_dbias_entry_point_host_checks(lib):
     assert lib.fp8_quantize_transpose_dbias(*args(0, good, bad)) == 3   # misaligned dbias
     assert lib.fp8_quantize_transpose_dbias(good, 250, 128, 0, good, good, good, good, None,
                                             good, good, None) == 3     # rows % 16
+
+
+def test_meta_checkpoint_host_checks(lib):
+    from scaled_linear_layers_gb300 import _lib
+    assert lib.fp8_meta_state_bytes(16) == 24 + 4 * 24
+    assert lib.fp8_meta_state_bytes(0) == 0 and lib.fp8_meta_state_bytes(2000) == 0
+    m = _lib.fp8_meta()
+    good = ctypes.c_void_p(0x2000)
+    cnt = ctypes.c_int64(0)
+    blob = ctypes.create_string_buffer(120)
+    # an all-zero buffer is not a saved state
+    assert lib.fp8_meta_load(ctypes.byref(m), good, ctypes.byref(cnt), blob, 120, None) == 2
+    assert "not a saved fp8 meta state" in lib.fp8_last_error().decode()
+    # a header with a bad idx
+    hdr = (0x534D3846).to_bytes(4, "little") + (1).to_bytes(4, "little") + \
+        (16).to_bytes(4, "little") + (16).to_bytes(4, "little") + (0).to_bytes(8, "little")
+    blob = ctypes.create_string_buffer(hdr + bytes(96), 120)
+    assert lib.fp8_meta_load(ctypes.byref(m), good, ctypes.byref(cnt), blob, 120, None) == 2
+    # too short for its interval
+    hdr = hdr[:12] + (3).to_bytes(4, "little") + hdr[16:]
+    blob = ctypes.create_string_buffer(hdr + bytes(96), 120)
+    assert lib.fp8_meta_load(ctypes.byref(m), good, ctypes.byref(cnt), blob, 100, None) == 2
+    # save needs a big enough buffer
+    m.dev, m.interval, m.idx = good, 16, 0
+    assert lib.fp8_meta_save(ctypes.byref(m), 5, blob, 100, None) == 2

@@ -246,6 +246,69 @@ def test_composite_step_with_bias_and_bias_gradient():
         assert torch.equal(db2, step.dbias)
 
 
+def test_composite_step_with_saved_forward_xq():
+    """FP8_STEP_SAVE_XQ_FWD: the backward takes the forward's Xqᵀ and x scale
+    (no second read of X) and matches the oracle's saved-Xq variant."""
+    c = synth.CONFIG2
+    M, N, K = 256, 384, 512
+    w = synth.normal_bf16((N, K), c["w_sigma"], 11, "w")
+    wd = dev_bf16(w)
+    step = fp8.LinearStep(M, N, K, save_xq_fwd=True)
+    meta = fp8.Fp8Meta(16)
+    count = [0]
+    st = ost.State(16)
+    om = st.new_meta()
+    for t in range(18):
+        x = synth.normal_bf16((M, K), c["x_sigma"] * (1 + t % 3), 11, "x", t)
+        g = synth.normal_bf16((M, N), c["g_sigma"], 11, "g", t)
+        step.set_inputs(dev_bf16(x), wd, dev_bf16(g))
+        fp8.fp8_linear_step_delayed(meta, count, step)
+        fp8.fp8_check_device_status()
+        ref = ost.delayed_training_step(st, om, x, w, g, save_xq_fwd=True)
+        f, b = ref["fwd"], ref["bwd"]
+        assert np.array_equal(host_u8(step.xq), f["xq"])
+        assert np.array_equal(host_u8(step.xqt), f["xq"].T)
+        assert np.array_equal(host_u8(step.gq), b["gq"])
+        blk = meta.block.cpu().numpy()
+        for k, i in (("scale", 0), ("x_scale", 2), ("g_scale", 4)):
+            assert f32bits(blk[i]) == f32bits(ref["meta"][k]), (t, k)
+        check_gemm(step.y.float().cpu().numpy(), f["y"])
+        check_gemm(step.dx.float().cpu().numpy(), b["dx"])
+        check_gemm(step.dw.float().cpu().numpy(), b["dw"])
+
+
+def test_meta_checkpoint_restore_continues_bit_for_bit():
+    """fp8_meta_save after 10 steps, fp8_meta_load into a fresh meta: the
+    next 10 steps (across the step-16 refresh) give the same bits as the
+    run that saved it."""
+    c = synth.CONFIG2
+    M, N, K = 256, 256, 256
+    w = synth.normal_bf16((N, K), c["w_sigma"], 12, "w")
+    wd = dev_bf16(w)
+    xs = [dev_bf16(synth.normal_bf16((M, K), c["x_sigma"], 12, "x", t)) for t in range(20)]
+    gs = [dev_bf16(synth.normal_bf16((M, N), c["g_sigma"], 12, "g", t)) for t in range(20)]
+
+    def run(meta, count, step, ts):
+        outs = []
+        for t in ts:
+            step.set_inputs(xs[t], wd, gs[t])
+            fp8.fp8_linear_step_delayed(meta, count, step)
+            outs.append([step.y.clone(), step.dx.clone(), step.dw.clone(), meta.block.clone()])
+        fp8.fp8_check_device_status()
+        return outs
+
+    meta, count, step = fp8.Fp8Meta(16), [0], fp8.LinearStep(M, N, K)
+    run(meta, count, step, range(10))
+    blob = meta.save(count[0])
+    first = run(meta, count, step, range(10, 20))
+    meta2, cnt = fp8.Fp8Meta.load(blob)
+    assert cnt == 10 and meta2.c.idx == 10 and meta2.c.interval == 16
+    second = run(meta2, [cnt], fp8.LinearStep(M, N, K), range(10, 20))
+    for a, b in zip(first, second):
+        for ta, tb in zip(a, b):
+            assert torch.equal(ta, tb)
+
+
 def test_composite_step_forward_only_and_events():
     M, N, K = 128, 256, 128
     x = synth.normal_bf16((M, K), 1.0, 8, "x")
