@@ -73,6 +73,7 @@ def _load():
             "orc_gemm_block_entries": (None, [P, P, I, I, P, P, I, P, P, I, P, P, P]),
             "orc_pad_rows": (I, [P, I, I, I, P]),
             "orc_bias_grad": (None, [P, I, I, P, P, P]),
+            "orc_pad_bshd": (None, [P, I, I, I, I, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -276,6 +277,37 @@ def pad_rows(x: np.ndarray, multiple: int = 16) -> np.ndarray:
     out = np.empty((padded, cols), np.uint16)
     got = _load().orc_pad_rows(_p(x), rows, cols, multiple, _p(out))
     assert got == padded
+    return out
+
+
+def pad_multiple(cp_size: int, tp_size: int) -> int:
+    """Token multiple of a packed (THD) batch under context and tensor
+    parallelism.  The FP8 GEMMs need every rank's token count to be a
+    multiple of 16 (SpecForge page, Conclusion); with the tokens split over
+    cp * tp ranks (the NeMo page "Add FP8 support for SALMAutomodel" review:
+    the local linear sees M = B*T/tp, which is why its THD helper pads to
+    8 * cp * tp for TE's 8) that is 16 * cp * tp of the whole batch."""
+    return 16 * cp_size * tp_size
+
+
+def padded_seq_len(batch: int, seq: int, cp_size: int = 1, tp_size: int = 1) -> int:
+    """BSHD padding (same review): the smallest T' >= seq such that the
+    sequence dim splits evenly over the cp * tp ranks (T' % (cp*tp) == 0) and
+    every rank's token count batch * T' / (cp*tp) is a multiple of 16; found
+    by search."""
+    r = cp_size * tp_size
+    t = seq
+    while t % r or (batch * t) % (16 * r):
+        t += 1
+    return t
+
+
+def pad_bshd(x: np.ndarray, seq_out: int) -> np.ndarray:
+    """[B, T, H] bf16 -> [B, seq_out, H] with zero rows at each sequence's end."""
+    x = np.ascontiguousarray(x, np.uint16)
+    B, T, H = x.shape
+    out = np.empty((B, seq_out, H), np.uint16)
+    _load().orc_pad_bshd(_p(x), B, T, H, seq_out, _p(out))
     return out
 
 

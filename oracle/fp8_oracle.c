@@ -370,3 +370,18 @@ void orc_bias_grad(const uint16_t *g, int64_t rows, int64_t cols, double *d, dou
     for (int64_t n = 0; n < cols; ++n) d_bf16[n] = orc_round_to_bf16(d[n]);
 }
 
+/* ------------------------------------------------- padding of [B, T, H] --- */
+
+/* Per-sequence padding of a batch-major [B, T, H] bf16 tensor to [B, Tp, H]
+ * (NeMo page "Add FP8 support for SALMAutomodel": TE FP8 padding for BSHD
+ * inputs): every sequence keeps its T rows and gets Tp - T zero rows at its
+ * end, the same zero fill the THD path appends at the end of the packed
+ * batch. */
+void orc_pad_bshd(const uint16_t *x, int64_t B, int64_t T, int64_t H, int64_t Tp, uint16_t *out)
+{
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t t = 0; t < Tp; ++t)
+            for (int64_t h = 0; h < H; ++h)
+                out[(b * Tp + t) * H + h] = t < T ? x[(b * T + t) * H + h] : (uint16_t)0;
+}
+

@@ -357,3 +357,44 @@ def test_bias_grad_ignores_pad_rows_and_tolerance_catches_an_error():
     # a one-term error (one row's value counted twice) is far outside the bound
     bad = db + np.abs(_f32(g)[0]).astype(np.float64) * 8
     assert not oracle.bias_grad_tolerance_ok(bad, db, mag, 3858).all()
+
+
+# ------------------------------------------------------ parallel padding ---
+
+def test_pad_multiple_and_bshd_length_page_example():
+    ex = GOLDEN["bshd_tp_example"]
+    B, tp = ex["batch"], ex["tp_size"]
+    # the review's point: B*T % (8*tp) == 0 alone lets T be a multiple of 2
+    t8 = next(t for t in range(1, 64) if (B * t) % (8 * tp) == 0)
+    assert t8 == ex["multiple_from_8_tp"] and t8 % tp != 0
+    # our length splits over tp and gives every rank a multiple of 16 tokens
+    t = oracle.padded_seq_len(B, 1, 1, tp)
+    assert t % tp == 0 and (B * t // tp) % 16 == 0 and t == 4
+    assert GOLDEN["thd_pad_multiple_formula"]["value"] == "8 * cp_size * tp_size"
+    assert oracle.pad_multiple(1, 1) == GOLDEN["token_multiple"]["value"]
+    # a packed batch padded to pad_multiple leaves each of the cp*tp ranks a
+    # multiple of 16 tokens, and a smaller multiple would not for some size
+    for cp in (1, 2, 4):
+        for tp in (1, 2, 8):
+            m = oracle.pad_multiple(cp, tp)
+            assert (m // (cp * tp)) % 16 == 0 and m // 2 // (cp * tp) % 16 != 0
+
+
+def test_padded_seq_len_matches_closed_form():
+    from math import gcd
+    for B in (1, 2, 3, 16, 24):
+        for cp in (1, 2):
+            for tp in (1, 2, 4):
+                r = cp * tp
+                step_b = 16 * r // gcd(B, 16 * r)   # B*T' % (16r) == 0  <=>  T' % step_b == 0
+                L = r * step_b // gcd(r, step_b)
+                for T in (0, 1, 7, 16, 100, 3858):
+                    assert oracle.padded_seq_len(B, T, cp, tp) == -(-T // L) * L
+
+
+def test_pad_bshd_rows():
+    x = synth.normal_bf16((3, 5, 16), 1.0, seed=2, tensor="x")
+    out = oracle.pad_bshd(x, 8)
+    assert out.shape == (3, 8, 16)
+    assert np.array_equal(out[:, :5], x) and not out[:, 5:].any()
+    assert np.array_equal(oracle.pad_bshd(x, 5), x)
