@@ -757,12 +757,26 @@ def workload_sweep(args):
         rows_out.append(row)
         del xs
         torch.cuda.empty_cache()
+    # many weights in one pass: the MLP block's two weights (gate/up
+    # [28672, 4096], down [4096, 14336]) plus 64 [1024, 1024] weights
+    ws_multi = [_seeded_normal(torch, (28672, 4096), 0.02, 70, dev),
+                _seeded_normal(torch, (4096, 14336), 0.02, 71, dev)] + \
+        [_seeded_normal(torch, (1024, 1024), 0.02, 72 + i, dev) for i in range(64)]
+    nm = len(ws_multi)
+    am, sm, sim = (torch.empty(nm, dtype=torch.float32, device=dev) for _ in range(3))
+    ms = _timed(torch, lambda t: fp8.fp8_multi_amax_scales(ws_multi, am, sm, sim), 20, 3)
+    nbytes = 2 * sum(w.numel() for w in ws_multi)
+    multi = {"tensors": nm, "bytes": nbytes, "us": round(ms * 1e3, 2),
+             "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+             "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"], 3)}
+    del ws_multi
     fp8.fp8_check_device_status()
     best = max(r["cast_transpose_delayed"]["gbs"] for r in rows_out)
     return {"metric": "quantize GB/s (algorithmic bytes) vs HBM", "value": best, "unit": "GB/s",
             "higher_is_better": True, "data": "synthetic (seeded, on device)",
             "config": {"workload": "quantise-only sweep, 2^20..2^30 bf16 elements, [n/4096, 4096]"},
-            "hbm_peak_measured": peaks["hbm"], "sweep": rows_out}
+            "hbm_peak_measured": peaks["hbm"], "sweep": rows_out,
+            "multi_amax_scales": multi}
 
 
 def main():

@@ -386,6 +386,41 @@ int64_t fp8_padded_rows(int64_t rows, int64_t multiple);
 fp8_status fp8_pad_tokens(const uint16_t *x, int64_t rows, int64_t cols, int64_t multiple,
                           uint16_t *out, int64_t *padded_rows, cudaStream_t s);
 
+/* Token multiples under context / tensor parallelism (NeMo page "Add FP8
+ * support for SALMAutomodel", review of its BSHD and THD padding helpers:
+ * a rank's linear sees M = B*T/(cp*tp) tokens).  The FP8 GEMMs need every
+ * rank's token count to be a multiple of 16, so:
+ *   fp8_pad_multiple(cp, tp) = 16*cp*tp, the multiple to pass to
+ *     fp8_pad_tokens for a packed (THD) batch;
+ *   fp8_padded_seq_len(B, T, cp, tp) = the smallest T' >= T with T' a
+ *     multiple of cp*tp (the sequence dim splits evenly) and B*T' a multiple
+ *     of 16*cp*tp;
+ *   fp8_pad_tokens_bshd: out [B, T', H] = x [B, T, H] with T' - T zero rows
+ *     at the end of every sequence (H a multiple of 8, else
+ *     FP8_ERR_ALIGNMENT); *padded_seq (nullable) receives T'.
+ * -1 / FP8_ERR_SHAPE for batch < 1, seq < 0, cp or tp < 1. */
+int64_t fp8_pad_multiple(int32_t cp_size, int32_t tp_size);
+int64_t fp8_padded_seq_len(int64_t batch, int64_t seq, int32_t cp_size, int32_t tp_size);
+fp8_status fp8_pad_tokens_bshd(const uint16_t *x, int64_t batch, int64_t seq, int64_t hidden,
+                               int32_t cp_size, int32_t tp_size, uint16_t *out,
+                               int64_t *padded_seq, cudaStream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* Many weights at once                                                      */
+/* ------------------------------------------------------------------------ */
+/* Current-scaling amax and scales of n bf16 tensors in one pass (the
+ * SpecForge page runs torchao's precompute_float8_dynamic_scale_for_fsdp
+ * after every optimizer step: every float8 weight's scale computed together
+ * before its cast): for each i, amax[i] = max |w[i]| over numel[i] elements
+ * and scale[i], scale_inv[i] from it by the rule of fp8_meta_record's lag
+ * update (clamp 1e-12, a/448, 448/a).  w is a host array of n device
+ * pointers (16-byte aligned); amax, scale, scale_inv are device arrays of n
+ * floats.  One amax launch per 64 tensors plus one scale launch; the scales
+ * can then drive fp8_quantize / fp8_quantize_transpose with the DELAYED
+ * recipe (scale_inv as input). */
+fp8_status fp8_multi_amax_scales(const uint16_t *const *w, const int64_t *numel, int32_t n,
+                                 float *amax, float *scale, float *scale_inv, cudaStream_t s);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */

@@ -22,7 +22,8 @@ _LIB = _lib.load()
 __all__ = [
     "fp8_amax", "fp8_quantize", "fp8_quantize_transpose", "fp8_linear_fprop",
     "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_linear_dgrad_wgrad", "fp8_meta_init",
-    "fp8_dbias_workspace_bytes", "fp8_quantize_transpose_dbias",
+    "fp8_dbias_workspace_bytes", "fp8_quantize_transpose_dbias", "fp8_pad_multiple",
+    "fp8_padded_seq_len", "fp8_pad_tokens_bshd", "fp8_multi_amax_scales",
     "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
@@ -150,6 +151,35 @@ def fp8_linear_dgrad_wgrad(gq, gqt, g_scale, wqt, w_scale, xqt, x_scale, M, N, K
                                        _ptr(_u8(wqt)), _ptr(w_scale), _ptr(_u8(xqt)),
                                        _ptr(x_scale), M, N, K, recipe, _ptr(dx), _ptr(dw),
                                        _stream(stream)))
+
+
+def fp8_pad_multiple(cp_size=1, tp_size=1):
+    return _LIB.fp8_pad_multiple(cp_size, tp_size)
+
+
+def fp8_padded_seq_len(batch, seq, cp_size=1, tp_size=1):
+    return _LIB.fp8_padded_seq_len(batch, seq, cp_size, tp_size)
+
+
+def fp8_pad_tokens_bshd(x, cp_size, tp_size, out, stream=None):
+    """x [B, T, H] bf16 -> out [B, T', H]; returns T'."""
+    _bf16(x)
+    B, T, H = x.shape
+    tp = ctypes.c_int64(0)
+    _check(_LIB.fp8_pad_tokens_bshd(_ptr(x), B, T, H, cp_size, tp_size, _ptr(out),
+                                    ctypes.byref(tp), _stream(stream)))
+    return tp.value
+
+
+def fp8_multi_amax_scales(ws, amax, scale, scale_inv, stream=None):
+    """amax/scale/scale_inv: float32 device tensors of len(ws)."""
+    n = len(ws)
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in ws])
+    numel = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in ws])
+    for t in ws:
+        _bf16(t)
+    _check(_LIB.fp8_multi_amax_scales(ptrs, numel, n, _ptr(amax), _ptr(scale), _ptr(scale_inv),
+                                      _stream(stream)))
 
 
 class Fp8Meta:

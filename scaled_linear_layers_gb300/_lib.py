@@ -70,6 +70,11 @@ SIGNATURES = {
     "fp8_linear_step_delayed": (S, [ctypes.POINTER(fp8_meta), ctypes.POINTER(I64),
                                     ctypes.POINTER(fp8_linear_step_io), I64, I64, I64, P, P]),
     "fp8_padded_rows": (I64, [I64, I64]),
+    "fp8_pad_multiple": (I64, [I32, I32]),
+    "fp8_padded_seq_len": (I64, [I64, I64, I32, I32]),
+    "fp8_pad_tokens_bshd": (S, [P, I64, I64, I64, I32, I32, P, ctypes.POINTER(I64), P]),
+    "fp8_multi_amax_scales": (S, [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(I64), I32, P,
+                                  P, P, P]),
     "fp8_pad_tokens": (S, [P, I64, I64, I64, P, ctypes.POINTER(I64), P]),
     "fp8_check_device_status": (S, [P]),
     "fp8_selftest_wait_timeout": (S, [U32, P]),

@@ -704,6 +704,76 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     return FP8_OK;
 }
 
+int64_t fp8_pad_multiple(int32_t cp_size, int32_t tp_size) {
+    if (cp_size < 1 || tp_size < 1 || (int64_t)cp_size * tp_size > (1 << 20)) return -1;
+    return 16 * (int64_t)cp_size * tp_size;
+}
+
+int64_t fp8_padded_seq_len(int64_t batch, int64_t seq, int32_t cp_size, int32_t tp_size) {
+    if (batch < 1 || seq < 0 || cp_size < 1 || tp_size < 1) return -1;
+    const int64_t r = (int64_t)cp_size * tp_size;
+    if (r > (1 << 20)) return -1;
+    auto gcd = [](int64_t a, int64_t b) {
+        while (b) {
+            const int64_t t = a % b;
+            a = b;
+            b = t;
+        }
+        return a;
+    };
+    // T' % r == 0 and batch*T' % (16 r) == 0: T' a multiple of lcm(r, 16r / gcd(batch, 16r))
+    const int64_t step_b = 16 * r / gcd(batch % (16 * r), 16 * r);
+    const int64_t L = r / gcd(r, step_b) * step_b;
+    return (seq + L - 1) / L * L;
+}
+
+fp8_status fp8_pad_tokens_bshd(const uint16_t *x, int64_t batch, int64_t seq, int64_t hidden,
+                               int32_t cp_size, int32_t tp_size, uint16_t *out,
+                               int64_t *padded_seq, cudaStream_t s) {
+    const char *who = "fp8_pad_tokens_bshd";
+    const int64_t tp = fp8_padded_seq_len(batch, seq, cp_size, tp_size);
+    if (tp < 0 || hidden < 0)
+        return fail(FP8_ERR_SHAPE, "%s: batch=%lld seq=%lld hidden=%lld cp=%d tp=%d", who,
+                    (long long)batch, (long long)seq, (long long)hidden, cp_size, tp_size);
+    if (hidden % 8 != 0)
+        return fail(FP8_ERR_ALIGNMENT, "%s: hidden=%lld must be a multiple of 8", who,
+                    (long long)hidden);
+    if (padded_seq != nullptr) *padded_seq = tp;
+    if (batch * tp * hidden > 0) FP8_NEED(out, who);
+    if (batch * seq * hidden > 0) FP8_NEED(x, who);
+    FP8_ALIGN(x, who);
+    FP8_ALIGN(out, who);
+    if (x != nullptr && out != nullptr && batch * seq * hidden > 0) {
+        const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
+        if (xb < ob + batch * tp * hidden * 2 && ob < xb + batch * seq * hidden * 2)
+            return fail(FP8_ERR_SHAPE, "%s: x and out overlap", who);
+    }
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_pad_bshd(x, batch, seq, hidden, tp, out, s), who);
+}
+
+fp8_status fp8_multi_amax_scales(const uint16_t *const *w, const int64_t *numel, int32_t n,
+                                 float *amax, float *scale, float *scale_inv, cudaStream_t s) {
+    const char *who = "fp8_multi_amax_scales";
+    if (n < 0) return fail(FP8_ERR_SHAPE, "%s: n=%d", who, n);
+    if (n == 0) return FP8_OK;
+    FP8_NEED(w, who);
+    FP8_NEED(numel, who);
+    FP8_NEED(amax, who);
+    FP8_NEED(scale, who);
+    FP8_NEED(scale_inv, who);
+    for (int32_t i = 0; i < n; ++i) {
+        if (numel[i] < 0)
+            return fail(FP8_ERR_SHAPE, "%s: numel[%d]=%lld", who, i, (long long)numel[i]);
+        if (numel[i] > 0 && w[i] == nullptr)
+            return fail(FP8_ERR_NULL, "%s: w[%d] is NULL", who, i);
+        if (!aligned16(w[i]))
+            return fail(FP8_ERR_ALIGNMENT, "%s: w[%d] is not 16-byte aligned", who, i);
+    }
+    FP8_TRY(check_device(who));
+    return cuda_status(launch_multi_amax_scales(w, numel, n, amax, scale, scale_inv, s), who);
+}
+
 int64_t fp8_padded_rows(int64_t rows, int64_t multiple) {
     if (rows < 0 || multiple < 1) return -1;
     return (rows + multiple - 1) / multiple * multiple;

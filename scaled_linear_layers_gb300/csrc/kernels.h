@@ -78,6 +78,14 @@ cudaError_t launch_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t row
                                                   float *scale, float *scale_inv, uint8_t *q,
                                                   uint8_t *qt, float *amax_out, cudaStream_t s,
                                                   const char **why);
+// amax[i], scale[i], scale_inv[i] of the bf16 tensors w[i] (numel[i]
+// elements, 16-byte aligned): current scaling, one amax launch per 64
+// tensors and one scale launch.
+cudaError_t launch_multi_amax_scales(const uint16_t *const *w, const int64_t *numel, int n,
+                                     float *amax, float *scale, float *scale_inv, cudaStream_t s);
+// out [B, Tp, H] = x [B, T, H] padded per sequence with zero rows (H % 8 == 0).
+cudaError_t launch_pad_bshd(const uint16_t *x, int64_t B, int64_t T, int64_t H, int64_t Tp,
+                            uint16_t *out, cudaStream_t s);
 cudaError_t launch_pad_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t padded,
                             uint16_t *out, cudaStream_t s);
 

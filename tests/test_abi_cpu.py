@@ -158,3 +158,32 @@ def test_meta_checkpoint_host_checks(lib):
     # save needs a big enough buffer
     m.dev, m.interval, m.idx = good, 16, 0
     assert lib.fp8_meta_save(ctypes.byref(m), 5, blob, 100, None) == 2
+
+
+def test_parallel_padding_arithmetic_matches_the_oracle(lib):
+    import oracle
+    for cp in (1, 2, 3):
+        for tp in (1, 2, 4, 8):
+            assert lib.fp8_pad_multiple(cp, tp) == oracle.pad_multiple(cp, tp)
+            for B in (1, 2, 5, 16, 24):
+                for T in (0, 1, 9, 128, 3858):
+                    assert lib.fp8_padded_seq_len(B, T, cp, tp) == \
+                        oracle.padded_seq_len(B, T, cp, tp), (B, T, cp, tp)
+    assert lib.fp8_pad_multiple(0, 1) == -1 and lib.fp8_padded_seq_len(0, 4, 1, 1) == -1
+    good = ctypes.c_void_p(0x2000)
+    out = ctypes.c_int64(0)
+    assert lib.fp8_pad_tokens_bshd(good, 2, 5, 12, 1, 1, good, ctypes.byref(out), None) == 3
+    assert lib.fp8_pad_tokens_bshd(good, 0, 5, 16, 1, 1, good, ctypes.byref(out), None) == 2
+
+
+def test_multi_amax_host_checks(lib):
+    P = ctypes.c_void_p
+    ptrs = (P * 2)(0x2000, 0x2008)
+    numel = (ctypes.c_int64 * 2)(16, 16)
+    good = P(0x3000)
+    assert lib.fp8_multi_amax_scales(ptrs, numel, 0, None, None, None, None) == 0
+    assert lib.fp8_multi_amax_scales(ptrs, numel, 2, good, good, good, None) == 3  # misaligned w[1]
+    ptrs[1] = None
+    assert lib.fp8_multi_amax_scales(ptrs, numel, 2, good, good, good, None) == 1
+    numel[1] = -1
+    assert lib.fp8_multi_amax_scales(ptrs, numel, 2, good, good, good, None) == 2

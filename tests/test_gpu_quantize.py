@@ -237,3 +237,40 @@ def test_timeout_path_reports_and_leaves_the_context_usable():
     x = synth.normal_bf16((1024,), 1.0, seed=5, tensor="x")
     fp8.fp8_amax(dev_bf16(x), a)
     assert a.item() == oracle.amax(x)
+
+
+def test_multi_amax_scales_many_tensors():
+    """One pass over many weights (more than one launch's 64), sizes with
+    ragged tails, an empty tensor and special values: every amax and scale
+    bit for bit as the oracle's per-tensor amax and scale rule."""
+    shapes = [(4096, 4096), (3, 7), (0, 16), (1, 8), (65536 + 3,), (1024, 1000)] + \
+        [(17 * (i + 1), 9) for i in range(66)]
+    hs = []
+    for i, sh in enumerate(shapes):
+        h = synth.normal_with_outliers_bf16(sh, 0.02 * (1 + i % 5), seed=i, tensor="w")
+        hs.append(h)
+    hs[1] = hs[1].copy()
+    hs[1].ravel()[5] = 0xFF80  # -inf
+    ds = [dev_bf16(h) for h in hs]
+    n = len(ds)
+    amax, s, si = (torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(3))
+    fp8.fp8_multi_amax_scales(ds, amax, s, si)
+    fp8.fp8_check_device_status()
+    a_h, s_h, si_h = amax.cpu().numpy(), s.cpu().numpy(), si.cpu().numpy()
+    for i, h in enumerate(hs):
+        ra = oracle.amax(h.ravel())
+        rs, rsi = oracle.scale_from_amax(ra)
+        assert amax_bits(a_h[i]) == amax_bits(ra), (i, a_h[i], ra)
+        assert amax_bits(s_h[i]) == amax_bits(rs) and amax_bits(si_h[i]) == amax_bits(rsi), i
+
+
+@pytest.mark.parametrize("shape", [(3, 5, 16, 1, 4), (2, 3858, 64, 2, 2), (16, 1, 8, 1, 4),
+                                   (1, 128, 4096, 1, 1)])
+def test_pad_tokens_bshd(shape):
+    B, T, H, cp, tp = shape
+    x = synth.normal_bf16((B, T, H), 1.0, seed=B + T, tensor="x")
+    Tp = oracle.padded_seq_len(B, T, cp, tp)
+    out = torch.full((B, Tp, H), 7.0, dtype=torch.bfloat16, device="cuda")
+    got_tp = fp8.fp8_pad_tokens_bshd(dev_bf16(x), cp, tp, out)
+    assert got_tp == Tp
+    assert np.array_equal(host_bf16(out), oracle.pad_bshd(x, Tp))
