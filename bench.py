@@ -271,25 +271,26 @@ def gpu_arm(args, rank, world):
     # and its Y, dX, dW back out.  Three streams (H2D, compute, D2H) with
     # double-buffered device inputs and outputs let step t's copies overlap
     # steps t-1 / t+1's kernels; the meta state is shared, so the numerics
-    # are those of the device-resident loop.
-    n_host = 4
+    # are those of the device-resident loop.  (Three buffers measured slower:
+    # 0.68 against 0.58 ms a step; the host link is the limit either way.)
+    n_host, NB = 4, 2
     xp = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory() for h in x_host[:n_host]]
     gp = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory() for h in g_host[:n_host]]
-    x_buf = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    g_buf = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    ios = [step.io, fp8.LinearStep(M, N, K, device=dev)]
+    x_buf = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
+    g_buf = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
+    ios = [step.io] + [fp8.LinearStep(M, N, K, device=dev) for _ in range(NB - 1)]
     outs = [[torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
              torch.empty((M, K), dtype=torch.bfloat16).pin_memory(),
-             torch.empty((N, K), dtype=torch.bfloat16).pin_memory()] for _ in range(2)]
+             torch.empty((N, K), dtype=torch.bfloat16).pin_memory()] for _ in range(NB)]
     h2d = x_buf[0].numel() * 2 + g_buf[0].numel() * 2
     d2h = sum(o.numel() * 2 for o in outs[0])
     e2e_steps = max(3, min(args.steps, 200))
     s_comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_used = [torch.cuda.Event() for _ in range(2)]   # compute done with inputs of slot
-    ev_comp = [torch.cuda.Event() for _ in range(2)]   # outputs of slot written
-    ev_read = [torch.cuda.Event() for _ in range(2)]   # outputs of slot copied out
+    ev_in = [torch.cuda.Event() for _ in range(NB)]
+    ev_used = [torch.cuda.Event() for _ in range(NB)]   # compute done with inputs of slot
+    ev_comp = [torch.cuda.Event() for _ in range(NB)]   # outputs of slot written
+    ev_read = [torch.cuda.Event() for _ in range(NB)]   # outputs of slot copied out
     for e in ev_used + ev_read:
         e.record(s_comp)
     barrier()
@@ -299,7 +300,7 @@ def gpu_arm(args, rank, world):
     s_in.wait_event(e0)
     s_out.wait_event(e0)
     for t in range(e2e_steps):
-        b = t % 2
+        b = t % NB
         with torch.cuda.stream(s_in):
             s_in.wait_event(ev_used[b])
             x_buf[b].copy_(xp[t % n_host], non_blocking=True)

@@ -274,3 +274,27 @@ def test_pad_tokens_bshd(shape):
     got_tp = fp8.fp8_pad_tokens_bshd(dev_bf16(x), cp, tp, out)
     assert got_tp == Tp
     assert np.array_equal(host_bf16(out), oracle.pad_bshd(x, Tp))
+
+
+def test_quantize_transpose_largest_sweep_size_sampled():
+    """The sweep's largest size, 2^30 elements as [262144, 4096] (64 stacked
+    copies of one seeded block plus one planted maximum far down): the amax
+    bit for bit, and q / qᵀ on sampled rows against the oracle."""
+    base = synth.normal_bf16((4096, 4096), 1.0, seed=30, tensor="x")
+    x = np.tile(base, (64, 1))
+    x[200003, 4001] = synth.f32_to_bf16_bits(np.array([-37.5], np.float32))[0]
+    R, C = x.shape
+    xd = dev_bf16(x)
+    amax_ref = oracle.amax(x)
+    assert amax_ref == np.float32(37.5)
+    _, si_ref = oracle.scale_from_amax(amax_ref)
+    q, qt, si, a = u8(R, C), u8(C, R), f32(), f32()
+    si.fill_(float(si_ref))
+    fp8.fp8_quantize_transpose(xd, fp8.DELAYED, None, si, q, qt, amax_out=a)
+    fp8.fp8_check_device_status()
+    assert amax_bits(a.item()) == amax_bits(amax_ref)
+    rows = np.array([0, 4095, 4096, 131071, 200003, 262143])
+    ref, _ = oracle.quantize(np.ascontiguousarray(x[rows]), si_ref)
+    idx = torch.from_numpy(rows).cuda()
+    assert np.array_equal(host_u8(q.index_select(0, idx)), ref)
+    assert np.array_equal(host_u8(qt.index_select(1, idx)), ref.T)
