@@ -206,6 +206,46 @@ def test_composite_step_matches_oracle_20_steps():
         check_gemm(step.dw.float().cpu().numpy(), b["dw"])
 
 
+def test_composite_step_full_size_as_benchmarked():
+    """The benchmark's own launch configuration: fp8_linear_step_delayed at
+    M=N=K=4096 (fprop on the 2-SM kernel, dgrad and wgrad sharing one 2-SM
+    launch, the state update and backward quantisation on the second stream)
+    for 3 steps, against the oracle's state machine: every byte, amax and
+    scale, and the GEMMs on sampled entries and full row panels."""
+    c = synth.CONFIG2
+    M = N = K = 4096
+    w = synth.normal_bf16((N, K), c["w_sigma"], c["seed"], "w")
+    wd = dev_bf16(w)
+    step = fp8.LinearStep(M, N, K)
+    meta = fp8.Fp8Meta(16)
+    count = [0]
+    st = ost.State(16)
+    om = st.new_meta()
+    rng = np.random.default_rng(3)
+    for t in range(3):
+        x = synth.normal_bf16((M, K), c["x_sigma"], c["seed"], "x", t)
+        g = synth.normal_bf16((M, N), c["g_sigma"], c["seed"], "g", t)
+        step.set_inputs(dev_bf16(x), wd, dev_bf16(g))
+        fp8.fp8_linear_step_delayed(meta, count, step)
+        fp8.fp8_check_device_status()
+        ent = dict(y=sample_entries(rng, M, N), dx=sample_entries(rng, M, K),
+                   dw=sample_entries(rng, N, K))
+        ref = ost.delayed_training_step(st, om, x, w, g, ent)
+        f, b = ref["fwd"], ref["bwd"]
+        assert np.array_equal(host_u8(step.xq), f["xq"]) and np.array_equal(host_u8(step.wq), f["wq"])
+        assert np.array_equal(host_u8(step.gq), b["gq"])
+        assert np.array_equal(host_u8(step.xqt), b["xq_bwd"].T)
+        am = step.amax.cpu().numpy()
+        assert [f32bits(v) for v in am] == [f32bits(f["amax_x"]), f32bits(f["amax_w"]),
+                                            f32bits(b["amax_g"])]
+        blk = meta.block.cpu().numpy()
+        for k, i in (("scale", 0), ("x_scale", 2), ("g_scale", 4)):
+            assert f32bits(blk[i]) == f32bits(ref["meta"][k]), (t, k)
+        check_gemm(step.y.float().cpu().numpy(), f["y"], *ent["y"])
+        check_gemm(step.dx.float().cpu().numpy(), b["dx"], *ent["dx"])
+        check_gemm(step.dw.float().cpu().numpy(), b["dw"], *ent["dw"])
+
+
 def test_composite_step_with_bias_and_bias_gradient():
     """The step with a bias (added in fprop's epilogue) and the bias gradient
     fused into G's quantisation (a padded token count: 3872 = 3858 rounded up
