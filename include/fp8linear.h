@@ -430,6 +430,13 @@ fp8_status fp8_multi_amax_scales(const uint16_t *const *w, const int64_t *numel,
  * FP8_ERR_CUDA on a CUDA error, else FP8_OK. */
 fp8_status fp8_check_device_status(cudaStream_t s);
 
+/* Test hook (host-side fault injection, no GPU involvement): the calling
+ * thread's next n kernel launches made by the library fail with
+ * cudaErrorLaunchFailure without launching, so callers can test how they
+ * handle FP8_ERR_CUDA; n = 0 clears it.  Entry points that launch several
+ * kernels may have enqueued the earlier ones before the failing launch. */
+fp8_status fp8_inject_launch_failures(int32_t n);
+
 /* Diagnostic: launches one block that waits on a barrier nothing will ever
  * complete, with a wait limit of timeout_us microseconds (1..1000000); the
  * wait gives up, sets the device status word and the kernel returns.  Used to

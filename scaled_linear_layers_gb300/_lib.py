@@ -77,6 +77,7 @@ SIGNATURES = {
                                   P, P, P]),
     "fp8_pad_tokens": (S, [P, I64, I64, I64, P, ctypes.POINTER(I64), P]),
     "fp8_check_device_status": (S, [P]),
+    "fp8_inject_launch_failures": (S, [I32]),
     "fp8_selftest_wait_timeout": (S, [U32, P]),
     "fp8_last_error": (ctypes.c_char_p, []),
     "fp8_version": (ctypes.c_char_p, []),

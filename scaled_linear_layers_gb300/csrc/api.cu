@@ -32,6 +32,12 @@ fp8_status cuda_status(cudaError_t e, const char *where, const char *why = nullp
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+thread_local int tl_fail_launches = 0;
+
+namespace {
+
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];
 int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
@@ -798,6 +804,12 @@ fp8_status fp8_pad_tokens(const uint16_t *x, int64_t rows, int64_t cols, int64_t
     }
     FP8_TRY(check_device(who));
     return cuda_status(launch_pad_rows(x, rows, cols, padded, out, s), who);
+}
+
+fp8_status fp8_inject_launch_failures(int32_t n) {
+    if (n < 0) return fail(FP8_ERR_SHAPE, "fp8_inject_launch_failures: n=%d", n);
+    tl_fail_launches = n;
+    return FP8_OK;
 }
 
 fp8_status fp8_check_device_status(cudaStream_t s) {

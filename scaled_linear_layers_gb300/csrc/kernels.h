@@ -9,12 +9,21 @@ namespace fp8 {
 
 int num_sms();  // SM count of the current device (cached per device)
 
+// Host-side fault injection for the tests (fp8_inject_launch_failures): the
+// calling thread's next n launches through launch_pdl return
+// cudaErrorLaunchFailure without launching anything.
+extern thread_local int tl_fail_launches;
+
 // Launches `kernel` on `s` with programmatic stream serialisation allowed: it
 // may begin while the previous kernel on the stream drains, and must wait
 // (pdl_wait_prior) before reading or writing global memory.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t s, Args &&...args) {
+    if (tl_fail_launches > 0) {
+        --tl_fail_launches;
+        return cudaErrorLaunchFailure;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

@@ -239,6 +239,23 @@ def test_timeout_path_reports_and_leaves_the_context_usable():
     assert a.item() == oracle.amax(x)
 
 
+def test_injected_launch_failure_is_reported_and_recovers():
+    """Host-side fault injection: a failing launch surfaces as FP8_ERR_CUDA
+    with the entry point's name; the next call runs normally."""
+    from scaled_linear_layers_gb300 import _lib
+    lib = _lib.load()
+    x = synth.normal_bf16((4096,), 1.0, seed=6, tensor="x")
+    a = f32()
+    assert lib.fp8_inject_launch_failures(1) == 0
+    with pytest.raises(fp8.Fp8Error) as e:
+        fp8.fp8_amax(dev_bf16(x), a)
+    assert e.value.status == 5 and "fp8_amax" in str(e.value)
+    fp8.fp8_amax(dev_bf16(x), a)
+    fp8.fp8_check_device_status()
+    assert a.item() == oracle.amax(x)
+    assert lib.fp8_inject_launch_failures(-1) == 2
+
+
 def test_multi_amax_scales_many_tensors():
     """One pass over many weights (more than one launch's 64), sizes with
     ragged tails, an empty tensor and special values: every amax and scale
