@@ -615,6 +615,11 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
         if (!bwd) return fail(FP8_ERR_NULL, "%s: dbias needs g", who);
         FP8_NEED(io->dbias_workspace, who);
     }
+    if ((io->flags & ~FP8_STEP_SAVE_XQ_FWD) != 0)
+        return fail(FP8_ERR_SHAPE, "%s: unknown flags 0x%x", who, (unsigned)io->flags);
+    const bool save_x = (io->flags & FP8_STEP_SAVE_XQ_FWD) != 0;
+    if (save_x && io->xqt == nullptr)
+        return fail(FP8_ERR_NULL, "%s: FP8_STEP_SAVE_XQ_FWD needs xqt", who);
     const void *ptrs[] = {io->x, io->w, io->g, io->bias, io->xq, io->xqt, io->wq, io->wqt,
                           io->gq, io->gqt, io->y, io->dx, io->dw, io->dbias, io->dbias_workspace};
     for (const void *p : ptrs)
@@ -639,11 +644,6 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     // forward: X (lagged x scale, q only) and W (q and qt) in one launch,
     // which also keeps the x scale fprop must use
     FP8_TRY(mark(s));
-    if ((io->flags & ~FP8_STEP_SAVE_XQ_FWD) != 0)
-        return fail(FP8_ERR_SHAPE, "%s: unknown flags 0x%x", who, (unsigned)io->flags);
-    const bool save_x = (io->flags & FP8_STEP_SAVE_XQ_FWD) != 0;
-    if (save_x && io->xqt == nullptr)
-        return fail(FP8_ERR_NULL, "%s: FP8_STEP_SAVE_XQ_FWD needs xqt", who);
     DelayedQuantJob jx{io->x, M, K, d + FP8_META_X_SCALE_INV, io->xq,
                        save_x ? io->xqt : nullptr, io->amax + 0};
     DelayedQuantJob jw{io->w, N, K, d + FP8_META_SCALE_INV, io->wq, io->wqt, io->amax + 1};

@@ -187,3 +187,23 @@ def test_multi_amax_host_checks(lib):
     assert lib.fp8_multi_amax_scales(ptrs, numel, 2, good, good, good, None) == 1
     numel[1] = -1
     assert lib.fp8_multi_amax_scales(ptrs, numel, 2, good, good, good, None) == 2
+
+
+def test_step_rejects_bad_flags_before_touching_the_counter(lib):
+    from scaled_linear_layers_gb300 import _lib
+    m = _lib.fp8_meta()
+    good = 0x2000
+    m.dev, m.interval, m.idx = good, 16, 0
+    io = _lib.fp8_linear_step_io()
+    for name in ("x", "w", "xq", "wq", "wqt", "amax", "y"):
+        setattr(io, name, good)
+    io.flags = 4
+    cnt = ctypes.c_int64(7)
+    st = lib.fp8_linear_step_delayed(ctypes.byref(m), ctypes.byref(cnt), ctypes.byref(io),
+                                     16, 16, 16, None, None)
+    assert st == 2 and "unknown flags" in lib.fp8_last_error().decode()
+    assert cnt.value == 7  # nothing happened: the step counter is untouched
+    io.flags = 1  # saving Xq from the forward needs xqt
+    st = lib.fp8_linear_step_delayed(ctypes.byref(m), ctypes.byref(cnt), ctypes.byref(io),
+                                     16, 16, 16, None, None)
+    assert st == 1 and cnt.value == 7
