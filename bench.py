@@ -549,34 +549,18 @@ def _seeded_normal(torch, shape, sigma, seed, dev, outliers=None):
 
 
 class _DynLinear:
-    """fwd + dgrad + wgrad of one projection under current scaling: every
-    operand through the single-launch dynamic quantiser (q and qt)."""
+    """fwd + dgrad + wgrad of one projection under current scaling as one
+    native call (fp8_linear_step_dynamic): every operand through the
+    single-launch dynamic quantiser (q and qt), fprop, then dgrad and wgrad."""
 
     def __init__(self, fp8, torch, dev, M, N, K, x, w, g):
         self.fp8, self.M, self.N, self.K = fp8, M, N, K
-        self.x, self.w, self.g = x, w, g
-        u8 = dict(dtype=torch.uint8, device=dev)
-        bf = dict(dtype=torch.bfloat16, device=dev)
-        self.q = {n: (torch.empty((r, c), **u8), torch.empty((c, r), **u8))
-                  for n, (r, c) in (("x", (M, K)), ("w", (N, K)), ("g", (M, N)))}
-        self.sc = torch.empty(12, dtype=torch.float32, device=dev)
-        self.ws = [torch.zeros(fp8.fp8_quantize_fused_workspace_bytes() // 4, dtype=torch.int32,
-                               device=dev) for _ in range(3)]
-        self.y, self.dx, self.dw = (torch.empty((M, N), **bf), torch.empty((M, K), **bf),
-                                    torch.empty((N, K), **bf))
+        self.step = fp8.LinearStep(M, N, K, device=dev)
+        self.step.set_inputs(x, w, g)
+        self.state = fp8.DynamicStepState(device=dev)
 
     def run(self):
-        fp8, sc = self.fp8, self.sc
-        for i, (n, t) in enumerate((("x", self.x), ("w", self.w), ("g", self.g))):
-            fp8.fp8_quantize_fused_dynamic(t, sc[4 * i:4 * i + 1], sc[4 * i + 1:4 * i + 2],
-                                           self.q[n][0], self.q[n][1], sc[4 * i + 2:4 * i + 3],
-                                           self.ws[i])
-        M, N, K = self.M, self.N, self.K
-        sx, sw, sg = sc[0:1], sc[4:5], sc[8:9]
-        fp8.fp8_linear_fprop(self.q["x"][0], sx, self.q["w"][0], sw, M, N, K, fp8.DYNAMIC, None,
-                             self.y)
-        fp8.fp8_linear_dgrad_wgrad(self.q["g"][0], self.q["g"][1], sg, self.q["w"][1], sw,
-                                   self.q["x"][1], sx, M, N, K, fp8.DYNAMIC, self.dx, self.dw)
+        self.fp8.fp8_linear_step_dynamic(self.state, self.step)
 
 
 def _gemm_line(metric_name, value_tflops, ms, flop, workload, extra, peaks):

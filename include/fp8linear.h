@@ -370,6 +370,22 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
                                    int64_t M, int64_t N, int64_t K, cudaEvent_t *events,
                                    cudaStream_t s);
 
+/* One training step of one linear under current (dynamic tensorwise) scaling,
+ * the torchao Float8Linear recipe of the SpecForge page ("Add
+ * training.fp8_linear", Modifications): X -> xq (and xqt with g), W -> wq (and
+ * wqt with g), each through the single-launch dynamic quantiser (amax[0],
+ * amax[1]); y = fprop(xq, wq) (+ bias); with g: G -> gq, gqt (amax[2]), then
+ * dx and dw as fp8_linear_dgrad_wgrad computes them (either may be NULL).
+ * Every scale comes from its tensor's own amax of this call (the lag rule
+ * applied to the current amax).  `scales`: 6 device floats, receives
+ * scale, scale_inv of x, w and g in that order.  `workspace`:
+ * 3 * fp8_quantize_fused_workspace_bytes() of device memory, all zero before
+ * the first call and reused as each call leaves it; concurrent calls need
+ * their own.  io->dbias must be NULL and io->flags 0.  No state: the step is the
+ * same at every call.  Argument checks happen before anything is enqueued. */
+fp8_status fp8_linear_step_dynamic(const fp8_linear_step_io *io, float *scales, void *workspace,
+                                   int64_t M, int64_t N, int64_t K, cudaStream_t s);
+
 /* ------------------------------------------------------------------------ */
 /* Token padding                                                             */
 /* ------------------------------------------------------------------------ */

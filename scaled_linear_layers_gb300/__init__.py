@@ -24,6 +24,7 @@ __all__ = [
     "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_linear_dgrad_wgrad", "fp8_meta_init",
     "fp8_dbias_workspace_bytes", "fp8_quantize_transpose_dbias", "fp8_pad_multiple",
     "fp8_padded_seq_len", "fp8_pad_tokens_bshd", "fp8_multi_amax_scales",
+    "fp8_linear_step_dynamic", "DynamicStepState",
     "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
@@ -151,6 +152,23 @@ def fp8_linear_dgrad_wgrad(gq, gqt, g_scale, wqt, w_scale, xqt, x_scale, M, N, K
                                        _ptr(_u8(wqt)), _ptr(w_scale), _ptr(_u8(xqt)),
                                        _ptr(x_scale), M, N, K, recipe, _ptr(dx), _ptr(dw),
                                        _stream(stream)))
+
+
+class DynamicStepState:
+    """Device scratch of fp8_linear_step_dynamic: the 6 scales and the three
+    quantiser workspaces (zeroed once)."""
+
+    def __init__(self, device="cuda"):
+        self.scales = torch.empty(6, dtype=torch.float32, device=device)
+        n = 3 * _LIB.fp8_quantize_fused_workspace_bytes() // 4
+        self.workspace = torch.zeros(n, dtype=torch.int32, device=device)
+
+
+def fp8_linear_step_dynamic(state: DynamicStepState, step: "LinearStep", stream=None):
+    """One current-scaling training step (see the C header)."""
+    _check(_LIB.fp8_linear_step_dynamic(ctypes.byref(step.io), _ptr(state.scales),
+                                        _ptr(state.workspace), step.M, step.N, step.K,
+                                        _stream(stream)))
 
 
 def fp8_pad_multiple(cp_size=1, tp_size=1):

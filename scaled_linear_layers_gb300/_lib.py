@@ -69,6 +69,7 @@ SIGNATURES = {
     "fp8_state_step": (S, [ctypes.POINTER(I64), I32, ctypes.POINTER(fp8_meta), I32, P]),
     "fp8_linear_step_delayed": (S, [ctypes.POINTER(fp8_meta), ctypes.POINTER(I64),
                                     ctypes.POINTER(fp8_linear_step_io), I64, I64, I64, P, P]),
+    "fp8_linear_step_dynamic": (S, [ctypes.POINTER(fp8_linear_step_io), P, P, I64, I64, I64, P]),
     "fp8_padded_rows": (I64, [I64, I64]),
     "fp8_pad_multiple": (I64, [I32, I32]),
     "fp8_padded_seq_len": (I64, [I64, I64, I32, I32]),

@@ -710,6 +710,70 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     return FP8_OK;
 }
 
+fp8_status fp8_linear_step_dynamic(const fp8_linear_step_io *io, float *scales, void *workspace,
+                                   int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+    const char *who = "fp8_linear_step_dynamic";
+    FP8_NEED(io, who);
+    FP8_NEED(scales, who);
+    FP8_NEED(workspace, who);
+    if (M <= 0 || N <= 0 || K <= 0 || M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: bad shape [M=%lld, N=%lld, K=%lld]", who, (long long)M,
+                    (long long)N, (long long)K);
+    FP8_TRY(check_dim16(who, "M", M, 16));
+    FP8_TRY(check_dim16(who, "N", N, 16));
+    FP8_TRY(check_dim16(who, "K", K, 16));
+    const bool bwd = io->g != nullptr;
+    FP8_NEED(io->x, who);
+    FP8_NEED(io->w, who);
+    FP8_NEED(io->xq, who);
+    FP8_NEED(io->wq, who);
+    FP8_NEED(io->amax, who);
+    FP8_NEED(io->y, who);
+    if (bwd) {
+        FP8_NEED(io->wqt, who);
+        FP8_NEED(io->gq, who);
+        FP8_NEED(io->gqt, who);
+        FP8_NEED(io->xqt, who);
+    }
+    if (io->dbias != nullptr)
+        return fail(FP8_ERR_UNSUPPORTED, "%s: dbias is fused into the delayed-scaling step only",
+                    who);
+    if (io->flags != 0) return fail(FP8_ERR_SHAPE, "%s: unknown flags 0x%x", who, (unsigned)io->flags);
+    const void *ptrs[] = {io->x, io->w, io->g, io->bias, io->xq, io->xqt, io->wq, io->wqt,
+                          io->gq, io->gqt, io->y, io->dx, io->dw, workspace};
+    for (const void *p : ptrs)
+        if (p != nullptr && !aligned16(p))
+            return fail(FP8_ERR_ALIGNMENT, "%s: a buffer is not 16-byte aligned", who);
+    FP8_TRY(check_device(who));
+    unsigned int *ws = static_cast<unsigned int *>(workspace);
+    const size_t wsw = kFusedWorkspaceBytes / sizeof(unsigned int);
+    // X and W: current scaling, each in one launch (q, and qᵀ for the backward)
+    FP8_TRY(cuda_status(launch_quantize_fused_dynamic(io->x, M, K, scales + 0, scales + 1, io->xq,
+                                                      bwd ? io->xqt : nullptr, io->amax + 0, ws,
+                                                      s),
+                        who));
+    FP8_TRY(cuda_status(launch_quantize_fused_dynamic(io->w, N, K, scales + 2, scales + 3, io->wq,
+                                                      bwd ? io->wqt : nullptr, io->amax + 1,
+                                                      ws + wsw, s),
+                        who));
+    FP8_TRY(fp8_linear_fprop(io->xq, scales + 0, io->wq, scales + 2, M, N, K, FP8_RECIPE_DYNAMIC,
+                             io->bias, io->y, s));
+    if (!bwd) return FP8_OK;
+    FP8_TRY(cuda_status(launch_quantize_fused_dynamic(io->g, M, N, scales + 4, scales + 5, io->gq,
+                                                      io->gqt, io->amax + 2, ws + 2 * wsw, s),
+                        who));
+    if (io->dx != nullptr && io->dw != nullptr)
+        return fp8_linear_dgrad_wgrad(io->gq, io->gqt, scales + 4, io->wqt, scales + 2, io->xqt,
+                                      scales + 0, M, N, K, FP8_RECIPE_DYNAMIC, io->dx, io->dw, s);
+    if (io->dx != nullptr)
+        FP8_TRY(fp8_linear_dgrad(io->gq, scales + 4, io->wqt, scales + 2, M, N, K,
+                                 FP8_RECIPE_DYNAMIC, io->dx, s));
+    if (io->dw != nullptr)
+        FP8_TRY(fp8_linear_wgrad(io->gqt, scales + 4, io->xqt, scales + 0, M, N, K,
+                                 FP8_RECIPE_DYNAMIC, io->dw, s));
+    return FP8_OK;
+}
+
 int64_t fp8_pad_multiple(int32_t cp_size, int32_t tp_size) {
     if (cp_size < 1 || tp_size < 1 || (int64_t)cp_size * tp_size > (1 << 20)) return -1;
     return 16 * (int64_t)cp_size * tp_size;

@@ -349,6 +349,49 @@ def test_meta_checkpoint_restore_continues_bit_for_bit():
             assert torch.equal(ta, tb)
 
 
+@pytest.mark.parametrize("shape", [(256, 384, 512), (2048, 4096, 1024)])
+def test_dynamic_step_one_call(shape):
+    """fp8_linear_step_dynamic against the oracle's current-scaling step: every
+    byte, amax and scale bit for bit, the GEMMs within the tolerance (all
+    entries at the small shape, sampled at the larger one, where dgrad and
+    wgrad share a 2-SM launch); a second call on new inputs reuses the
+    scratch."""
+    M, N, K = shape
+    st = fp8.DynamicStepState()
+    step = fp8.LinearStep(M, N, K)
+    rng = np.random.default_rng(M)
+    w = synth.normal_bf16((N, K), 0.02, 21, "w")
+    for t in range(2):
+        x = synth.normal_bf16((M, K), 1.0, 21, "x", t)
+        g = synth.normal_bf16((M, N), 1e-3, 21, "g", t)
+        step.set_inputs(dev_bf16(x), dev_bf16(w), dev_bf16(g))
+        fp8.fp8_linear_step_dynamic(st, step)
+        fp8.fp8_check_device_status()
+        small = M * N * K <= 256 * 384 * 512
+        ent = None if small else dict(y=sample_entries(rng, M, N), dx=sample_entries(rng, M, K),
+                                      dw=sample_entries(rng, N, K))
+        ref = ost.dynamic_linear_step(x, w, g, ent)
+        sc = st.scales.cpu().numpy()
+        am = step.amax.cpu().numpy()
+        for i, name in enumerate(("x", "w", "g")):
+            r = ref[name]
+            assert f32bits(am[i]) == f32bits(r["amax"]), name
+            assert f32bits(sc[2 * i]) == f32bits(r["scale"]) and \
+                f32bits(sc[2 * i + 1]) == f32bits(r["scale_inv"]), name
+        assert np.array_equal(host_u8(step.xq), ref["x"]["q"])
+        assert np.array_equal(host_u8(step.wqt), ref["w"]["q"].T)
+        assert np.array_equal(host_u8(step.gqt), ref["g"]["q"].T)
+        assert np.array_equal(host_u8(step.xqt), ref["x"]["q"].T)
+        if small:
+            check_gemm(step.y.float().cpu().numpy(), ref["y"])
+            check_gemm(step.dx.float().cpu().numpy(), ref["dx"])
+            check_gemm(step.dw.float().cpu().numpy(), ref["dw"])
+        else:
+            check_gemm(step.y.float().cpu().numpy(), ref["y"], *ent["y"])
+            check_gemm(step.dx.float().cpu().numpy(), ref["dx"], *ent["dx"])
+            check_gemm(step.dw.float().cpu().numpy(), ref["dw"], *ent["dw"])
+
+
 def test_composite_step_forward_only_and_events():
     M, N, K = 128, 256, 128
     x = synth.normal_bf16((M, K), 1.0, 8, "x")
