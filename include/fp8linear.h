@@ -386,6 +386,28 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
 fp8_status fp8_linear_step_dynamic(const fp8_linear_step_io *io, float *scales, void *workspace,
                                    int64_t M, int64_t N, int64_t K, cudaStream_t s);
 
+/* One training step of one linear under the block recipe (TE recipe=block,
+ * the NeMo "Add FP8 support for SALMAutomodel" page; 1x128 activation and
+ * gradient tiles, 128x128 weight tiles): X -> xq with 1x128 row-tile scales
+ * and xqt with 128x1 column-tile scales (one launch), W -> wq and wqt with
+ * 128x128 tile scales, y = fprop(xq, wq); with g: G -> gq and gqt with row
+ * and column tiles (one launch), dx = dgrad(gq, wqt), dw = wgrad(gqt, xqt)
+ * (either may be NULL).  Same results as fp8_quantize_transpose and the
+ * three GEMM calls with the BLOCK / BLOCK_2D recipes.  M, N, K multiples of
+ * 128.  io->amax (nullable) receives the tensor amaxes of x, w, g; bias,
+ * dbias and flags are not supported (NULL / 0).  Every scale array is
+ * required (the forward-only step leaves the column-tile arrays of X
+ * written but unused). */
+typedef struct {
+    float *x_scale, *x_scale_inv;     /* [M, K/128]     row tiles of X (fprop)        */
+    float *x_scale_t, *x_scale_inv_t; /* [M/128, K]     column tiles of X (wgrad)     */
+    float *w_scale, *w_scale_inv;     /* [N/128, K/128] 128x128 tiles of W            */
+    float *g_scale, *g_scale_inv;     /* [M, N/128]     row tiles of G (dgrad)        */
+    float *g_scale_t, *g_scale_inv_t; /* [M/128, N]     column tiles of G (wgrad)     */
+} fp8_block_step_scales;
+fp8_status fp8_linear_step_block(const fp8_linear_step_io *io, const fp8_block_step_scales *sc,
+                                 int64_t M, int64_t N, int64_t K, cudaStream_t s);
+
 /* ------------------------------------------------------------------------ */
 /* Token padding                                                             */
 /* ------------------------------------------------------------------------ */

@@ -24,7 +24,7 @@ __all__ = [
     "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_linear_dgrad_wgrad", "fp8_meta_init",
     "fp8_dbias_workspace_bytes", "fp8_quantize_transpose_dbias", "fp8_pad_multiple",
     "fp8_padded_seq_len", "fp8_pad_tokens_bshd", "fp8_multi_amax_scales",
-    "fp8_linear_step_dynamic", "DynamicStepState",
+    "fp8_linear_step_dynamic", "DynamicStepState", "fp8_linear_step_block", "BlockStepScales",
     "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
@@ -169,6 +169,30 @@ def fp8_linear_step_dynamic(state: DynamicStepState, step: "LinearStep", stream=
     _check(_LIB.fp8_linear_step_dynamic(ctypes.byref(step.io), _ptr(state.scales),
                                         _ptr(state.workspace), step.M, step.N, step.K,
                                         _stream(stream)))
+
+
+class BlockStepScales:
+    """The tile-scale arrays of fp8_linear_step_block for an [M, N, K] linear
+    (torch float32 tensors this object owns, named as in the C struct)."""
+
+    def __init__(self, M, N, K, device="cuda"):
+        f = dict(dtype=torch.float32, device=device)
+        shapes = {"x_scale": (M, K // 128), "x_scale_t": (M // 128, K),
+                  "w_scale": (N // 128, K // 128), "g_scale": (M, N // 128),
+                  "g_scale_t": (M // 128, N)}
+        self.c = _lib.fp8_block_step_scales()
+        for name, shape in shapes.items():
+            inv = name.replace("_scale", "_scale_inv")
+            for n in (name, inv):
+                t = torch.empty(shape, **f)
+                setattr(self, n, t)
+                setattr(self.c, n, t.data_ptr())
+
+
+def fp8_linear_step_block(scales: BlockStepScales, step: "LinearStep", stream=None):
+    """One block-recipe training step (see the C header)."""
+    _check(_LIB.fp8_linear_step_block(ctypes.byref(step.io), ctypes.byref(scales.c), step.M,
+                                      step.N, step.K, _stream(stream)))
 
 
 def fp8_pad_multiple(cp_size=1, tp_size=1):

@@ -41,6 +41,12 @@ class fp8_linear_step_io(ctypes.Structure):
                  "dw", "dbias", "dbias_workspace")] + [("flags", ctypes.c_int32)]
 
 
+class fp8_block_step_scales(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("x_scale", "x_scale_inv", "x_scale_t", "x_scale_inv_t", "w_scale", "w_scale_inv",
+                 "g_scale", "g_scale_inv", "g_scale_t", "g_scale_inv_t")]
+
+
 FP8_STEP_NEVENTS = 8
 FP8_STEP_SAVE_XQ_FWD = 1
 
@@ -70,6 +76,8 @@ SIGNATURES = {
     "fp8_linear_step_delayed": (S, [ctypes.POINTER(fp8_meta), ctypes.POINTER(I64),
                                     ctypes.POINTER(fp8_linear_step_io), I64, I64, I64, P, P]),
     "fp8_linear_step_dynamic": (S, [ctypes.POINTER(fp8_linear_step_io), P, P, I64, I64, I64, P]),
+    "fp8_linear_step_block": (S, [ctypes.POINTER(fp8_linear_step_io),
+                                  ctypes.POINTER(fp8_block_step_scales), I64, I64, I64, P]),
     "fp8_padded_rows": (I64, [I64, I64]),
     "fp8_pad_multiple": (I64, [I32, I32]),
     "fp8_padded_seq_len": (I64, [I64, I64, I32, I32]),

@@ -774,6 +774,67 @@ fp8_status fp8_linear_step_dynamic(const fp8_linear_step_io *io, float *scales, 
     return FP8_OK;
 }
 
+fp8_status fp8_linear_step_block(const fp8_linear_step_io *io, const fp8_block_step_scales *sc,
+                                 int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+    const char *who = "fp8_linear_step_block";
+    FP8_NEED(io, who);
+    FP8_NEED(sc, who);
+    if (M <= 0 || N <= 0 || K <= 0 || M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return fail(FP8_ERR_SHAPE, "%s: bad shape [M=%lld, N=%lld, K=%lld]", who, (long long)M,
+                    (long long)N, (long long)K);
+    FP8_TRY(check_dim16(who, "M", M, 128));
+    FP8_TRY(check_dim16(who, "N", N, 128));
+    FP8_TRY(check_dim16(who, "K", K, 128));
+    const bool bwd = io->g != nullptr;
+    FP8_NEED(io->x, who);
+    FP8_NEED(io->w, who);
+    FP8_NEED(io->xq, who);
+    FP8_NEED(io->wq, who);
+    FP8_NEED(io->y, who);
+    if (bwd) {
+        FP8_NEED(io->xqt, who);
+        FP8_NEED(io->wqt, who);
+        FP8_NEED(io->gq, who);
+        FP8_NEED(io->gqt, who);
+    }
+    if (io->bias != nullptr || io->dbias != nullptr || io->flags != 0)
+        return fail(FP8_ERR_UNSUPPORTED, "%s: bias, dbias and flags are not supported", who);
+    const float *scs[] = {sc->x_scale, sc->x_scale_inv, sc->x_scale_t, sc->x_scale_inv_t,
+                          sc->w_scale, sc->w_scale_inv, sc->g_scale, sc->g_scale_inv,
+                          sc->g_scale_t, sc->g_scale_inv_t};
+    for (const float *p : scs)
+        if (p == nullptr) return fail(FP8_ERR_NULL, "%s: a scale array is NULL", who);
+    const void *ptrs[] = {io->x, io->w, io->g, io->xq, io->xqt, io->wq, io->wqt,
+                          io->gq, io->gqt, io->y, io->dx, io->dw};
+    for (const void *p : ptrs)
+        if (p != nullptr && !aligned16(p))
+            return fail(FP8_ERR_ALIGNMENT, "%s: a buffer is not 16-byte aligned", who);
+    FP8_TRY(check_device(who));
+    float *amax = io->amax;
+    FP8_TRY(cuda_status(launch_quantize_transpose(io->x, M, K, 3, sc->x_scale, sc->x_scale_inv,
+                                                  io->xq, bwd ? io->xqt : nullptr, sc->x_scale_t,
+                                                  sc->x_scale_inv_t, amax, s),
+                        who));
+    FP8_TRY(cuda_status(launch_quantize_transpose(io->w, N, K, 2, sc->w_scale, sc->w_scale_inv,
+                                                  io->wq, bwd ? io->wqt : nullptr, nullptr,
+                                                  nullptr, amax ? amax + 1 : nullptr, s),
+                        who));
+    FP8_TRY(fp8_linear_fprop(io->xq, sc->x_scale, io->wq, sc->w_scale, M, N, K,
+                             FP8_RECIPE_BLOCK, nullptr, io->y, s));
+    if (!bwd) return FP8_OK;
+    FP8_TRY(cuda_status(launch_quantize_transpose(io->g, M, N, 3, sc->g_scale, sc->g_scale_inv,
+                                                  io->gq, io->gqt, sc->g_scale_t,
+                                                  sc->g_scale_inv_t, amax ? amax + 2 : nullptr, s),
+                        who));
+    if (io->dx != nullptr)
+        FP8_TRY(fp8_linear_dgrad(io->gq, sc->g_scale, io->wqt, sc->w_scale, M, N, K,
+                                 FP8_RECIPE_BLOCK, io->dx, s));
+    if (io->dw != nullptr)
+        FP8_TRY(fp8_linear_wgrad(io->gqt, sc->g_scale_t, io->xqt, sc->x_scale_t, M, N, K,
+                                 FP8_RECIPE_BLOCK, io->dw, s));
+    return FP8_OK;
+}
+
 int64_t fp8_pad_multiple(int32_t cp_size, int32_t tp_size) {
     if (cp_size < 1 || tp_size < 1 || (int64_t)cp_size * tp_size > (1 << 20)) return -1;
     return 16 * (int64_t)cp_size * tp_size;

@@ -392,6 +392,61 @@ def test_dynamic_step_one_call(shape):
             check_gemm(step.dw.float().cpu().numpy(), ref["dw"], *ent["dw"])
 
 
+def test_block_step_one_call_matches_the_single_calls_and_the_oracle():
+    """fp8_linear_step_block at 512x384x640 (ragged pair and group tails):
+    the same bits as the quantise-transpose and GEMM calls it stands for, and
+    every output within the tolerance of the oracle's block GEMMs."""
+    M, N, K = 512, 384, 640
+    xh = synth.normal_with_outliers_bf16((M, K), 1.0, 31, "x")
+    wh = synth.normal_with_outliers_bf16((N, K), 1.0, 31, "w")
+    gh = synth.normal_with_outliers_bf16((M, N), 1.0, 31, "g")
+    x, w, g = dev_bf16(xh), dev_bf16(wh), dev_bf16(gh)
+    step = fp8.LinearStep(M, N, K)
+    step.set_inputs(x, w, g)
+    sc = fp8.BlockStepScales(M, N, K)
+    fp8.fp8_linear_step_block(sc, step)
+    fp8.fp8_check_device_status()
+    # the single calls
+    xq, xqt = u8(M, K), u8(K, M)
+    xs, xsi, xst, xsit = f32(M, K // 128), f32(M, K // 128), f32(M // 128, K), f32(M // 128, K)
+    fp8.fp8_quantize_transpose(x, fp8.BLOCK, xs, xsi, xq, xqt, xst, xsit)
+    wq, wqt = u8(N, K), u8(K, N)
+    ws, wsi = f32(N // 128, K // 128), f32(N // 128, K // 128)
+    fp8.fp8_quantize_transpose(w, fp8.BLOCK_2D, ws, wsi, wq, wqt)
+    gq, gqt = u8(M, N), u8(N, M)
+    gs, gsi, gst, gsit = f32(M, N // 128), f32(M, N // 128), f32(M // 128, N), f32(M // 128, N)
+    fp8.fp8_quantize_transpose(g, fp8.BLOCK, gs, gsi, gq, gqt, gst, gsit)
+    y, dx, dw = bf16_out(M, N), bf16_out(M, K), bf16_out(N, K)
+    fp8.fp8_linear_fprop(xq, xs, wq, ws, M, N, K, fp8.BLOCK, None, y)
+    fp8.fp8_linear_dgrad(gq, gs, wqt, ws, M, N, K, fp8.BLOCK, dx)
+    fp8.fp8_linear_wgrad(gqt, gst, xqt, xst, M, N, K, fp8.BLOCK, dw)
+    for a, b in ((step.xq, xq), (step.xqt, xqt), (step.wq, wq), (step.wqt, wqt), (step.gq, gq),
+                 (step.gqt, gqt), (sc.x_scale, xs), (sc.x_scale_t, xst), (sc.w_scale, ws),
+                 (sc.g_scale, gs), (sc.g_scale_t, gst), (step.y, y), (step.dx, dx),
+                 (step.dw, dw)):
+        assert torch.equal(a, b)
+    # the oracle
+    xq_ref, xs_ref, _ = oracle.quantize_rowtiles(xh, 128)
+    wq_ref, ws_ref, _ = oracle.quantize_sqtiles(wh, 128)
+    gq_ref, gs_ref, _ = oracle.quantize_rowtiles(gh, 128)
+    gqt_ref, gst_ref, _ = oracle.quantize_coltiles_t(gh, 128)
+    xqt_ref, xst_ref, _ = oracle.quantize_coltiles_t(xh, 128)
+    assert np.array_equal(host_u8(step.xq), xq_ref) and np.array_equal(host_u8(step.wq), wq_ref)
+    assert np.array_equal(host_u8(step.gqt), gqt_ref) and np.array_equal(host_u8(step.xqt), xqt_ref)
+    ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    check_gemm(step.y.float().cpu().numpy().ravel(),
+               oracle.gemm_block_entries(xq_ref, wq_ref, xs_ref, ws_ref, 128, ii.ravel(), jj.ravel()))
+    ii, jj = np.meshgrid(np.arange(M), np.arange(K), indexing="ij")
+    check_gemm(step.dx.float().cpu().numpy().ravel(),
+               oracle.gemm_block_entries(gq_ref, wq_ref.T.copy(), gs_ref,
+                                         np.ascontiguousarray(ws_ref.T), 128, ii.ravel(),
+                                         jj.ravel()))
+    ii, jj = np.meshgrid(np.arange(N), np.arange(K), indexing="ij")
+    check_gemm(step.dw.float().cpu().numpy().ravel(),
+               oracle.gemm_block_entries(gqt_ref, xqt_ref, gst_ref, xst_ref, 1, ii.ravel(),
+                                         jj.ravel()))
+
+
 def test_composite_step_forward_only_and_events():
     M, N, K = 128, 256, 128
     x = synth.normal_bf16((M, K), 1.0, 8, "x")
