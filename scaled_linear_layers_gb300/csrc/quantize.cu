@@ -63,30 +63,33 @@ __global__ void __launch_bounds__(256)
     } else {
         si = *scale_src;
     }
+    // 16-byte vectors of 8 bf16 -> 8 e4m3 bytes; consecutive lanes take
+    // consecutive vectors (full 512-byte loads per warp instruction), four
+    // vectors in flight per thread
     uint32_t m = 0;
-    const int64_t nchunk = n >> 4;  // 16 elements = 32 B in, 16 B out
+    const int64_t nvec = n >> 3;
     const uint4 *xv = reinterpret_cast<const uint4 *>(x);
-    uint4 *qv = reinterpret_cast<uint4 *>(q);
+    uint2 *qv = reinterpret_cast<uint2 *>(q);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + stride < nchunk; i += 2 * stride) {
-        uint4 a0 = ldg_nc_v4(xv + 2 * i), a1 = ldg_nc_v4(xv + 2 * i + 1);
-        uint4 b0 = ldg_nc_v4(xv + 2 * (i + stride)), b1 = ldg_nc_v4(xv + 2 * (i + stride) + 1);
-        if (!kDynamic) m = max(m, max(max(absmax_bits8(a0), absmax_bits8(a1)),
-                                      max(absmax_bits8(b0), absmax_bits8(b1))));
-        qv[i] = make_uint4(quant4(a0.x, a0.y, si), quant4(a0.z, a0.w, si), quant4(a1.x, a1.y, si),
-                           quant4(a1.z, a1.w, si));
-        qv[i + stride] = make_uint4(quant4(b0.x, b0.y, si), quant4(b0.z, b0.w, si),
-                                    quant4(b1.x, b1.y, si), quant4(b1.z, b1.w, si));
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+        const uint4 a = ldg_nc_v4(xv + i), b = ldg_nc_v4(xv + i + stride);
+        const uint4 c = ldg_nc_v4(xv + i + 2 * stride), d = ldg_nc_v4(xv + i + 3 * stride);
+        if (!kDynamic)
+            m = max(m, max(max(absmax_bits8(a), absmax_bits8(b)),
+                           max(absmax_bits8(c), absmax_bits8(d))));
+        qv[i] = make_uint2(quant4(a.x, a.y, si), quant4(a.z, a.w, si));
+        qv[i + stride] = make_uint2(quant4(b.x, b.y, si), quant4(b.z, b.w, si));
+        qv[i + 2 * stride] = make_uint2(quant4(c.x, c.y, si), quant4(c.z, c.w, si));
+        qv[i + 3 * stride] = make_uint2(quant4(d.x, d.y, si), quant4(d.z, d.w, si));
     }
-    for (; i < nchunk; i += stride) {
-        uint4 a0 = ldg_nc_v4(xv + 2 * i), a1 = ldg_nc_v4(xv + 2 * i + 1);
-        if (!kDynamic) m = max(m, max(absmax_bits8(a0), absmax_bits8(a1)));
-        qv[i] = make_uint4(quant4(a0.x, a0.y, si), quant4(a0.z, a0.w, si), quant4(a1.x, a1.y, si),
-                           quant4(a1.z, a1.w, si));
+    for (; i < nvec; i += stride) {
+        const uint4 a = ldg_nc_v4(xv + i);
+        if (!kDynamic) m = max(m, absmax_bits8(a));
+        qv[i] = make_uint2(quant4(a.x, a.y, si), quant4(a.z, a.w, si));
     }
-    if (blockIdx.x == 0) {  // ragged tail: fewer than 16 elements
-        for (int64_t j = (nchunk << 4) + threadIdx.x; j < n; j += blockDim.x) {
+    if (blockIdx.x == 0) {  // ragged tail: fewer than 8 elements
+        for (int64_t j = (nvec << 3) + threadIdx.x; j < n; j += blockDim.x) {
             uint32_t h = x[j];
             if (!kDynamic) m = max(m, h & 0x7FFFu);
             q[j] = (uint8_t)(cvt_e4m3x2(__fmul_rn(__uint_as_float(h << 16), si), 0.0f) & 0xFFu);
@@ -470,7 +473,7 @@ cudaError_t launch_quantize_tensor(const uint16_t *x, int64_t n, bool dynamic, f
                                    float *scale_inv, uint8_t *q, float *amax_out,
                                    cudaStream_t s) {
     cudaError_t e;
-    const int grid = grid_for((n >> 4) / 2 + 1, 256);
+    const int grid = grid_for((n >> 3) / 4 + 1, 256);
     if (dynamic) {
         if ((e = launch_amax(x, n, amax_out, s)) != cudaSuccess) return e;
         e = launch_pdl(quantize_kernel<true>, grid, 256, 0, s, x, n, (const float *)amax_out, q,
