@@ -11,8 +11,8 @@
 // promotion reads the other.  Eight epilogue warps (two per TMEM lane
 // quarter, 64 columns each) read a group's partials back one block at a
 // time, hand the group slot back after the last read and fold each partial
-// into fp32 register accumulators with its two block scales using packed
-// fp32x2 FMAs.  A hand-off costs a few hundred cycles of barrier traffic
+// into fp32 register accumulators with its two block scales (packed fp32x2
+// FMAs for per-tile B, a multiply and an FMA per element for per-row B).  A hand-off costs a few hundred cycles of barrier traffic
 // whatever it carries, so pairing the blocks halves that cost per block.
 // B's scale is one value per 128-row tile (weights) or one per row (wgrad's
 // Xᵀ operand: each warp stages its 64 scales of the next group into shared
@@ -102,12 +102,6 @@ __device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 
@@ -307,9 +301,16 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
             const float *sb_ptr =
                 kPerRowB ? sc.sb + (int64_t)min(j0 + PER_LANE * lane, p.N - PER_LANE) * sc.sb_row
                          : sc.sb + (int64_t)(min(j0, p.N - 1) / sc.b_rows) * sc.sb_row;
-            uint64_t acc[COLS / 2];  // fp32 accumulators in pairs
+            // fp32 accumulators: in pairs for per-tile B (one packed FMA per
+            // pair), single for per-row B (a multiply and an FMA per element
+            // measured faster there than their packed forms: 1356 against
+            // 1297 TFLOP/s for wgrad at 32768 x 8192 x 8192)
+            uint64_t acc[COLS / 2];
+            float accs[COLS];
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) acc[j] = 0ull;
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) accs[j] = 0.f;
             // scalar scales of the next PD groups (contraction blocks past the
             // end read the last block's scales and go unused)
             float sa_pf[PD][KG], sb_pf[PD][KG];
@@ -388,18 +389,20 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                         }
                     }
                     const float *buf = wbuf + ((q % (PD + 1)) * KG + j) * COLS;
-                    const uint64_t fsa = pack2(sa_cur[j], sa_cur[j]);
                     const float f1 = sa_cur[j] * sb_cur[j];
                     const uint64_t fts = pack2(f1, f1);
+                    if constexpr (kPerRowB) {
 #pragma unroll
-                    for (int a = 0; a < COLS / 2; ++a) {
-                        const uint64_t pv = pack2(__uint_as_float(r[a / 16][(2 * a) % 32]),
-                                                  __uint_as_float(r[a / 16][(2 * a) % 32 + 1]));
-                        if (kPerRowB) {
-                            const float2 sb2 = *reinterpret_cast<const float2 *>(buf + 2 * a);
-                            const uint64_t f = mul2(pack2(sb2.x, sb2.y), fsa);
-                            acc[a] = fma2(pv, f, acc[a]);
-                        } else {
+                        for (int a = 0; a < COLS; ++a) {
+                            const float f = __fmul_rn(buf[a], sa_cur[j]);
+                            accs[a] = __fmaf_rn(__uint_as_float(r[a / 32][a % 32]), f, accs[a]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int a = 0; a < COLS / 2; ++a) {
+                            const uint64_t pv =
+                                pack2(__uint_as_float(r[a / 16][(2 * a) % 32]),
+                                      __uint_as_float(r[a / 16][(2 * a) % 32 + 1]));
                             acc[a] = fma2(pv, fts, acc[a]);
                         }
                     }
@@ -411,7 +414,14 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                 for (int c = 0; c < COLS / 8; ++c) {
                     float v[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) unpack2(acc[4 * c + e], v[2 * e], v[2 * e + 1]);
+                    for (int e = 0; e < 4; ++e) {
+                        if constexpr (kPerRowB) {
+                            v[2 * e] = accs[8 * c + 2 * e];
+                            v[2 * e + 1] = accs[8 * c + 2 * e + 1];
+                        } else {
+                            unpack2(acc[4 * c + e], v[2 * e], v[2 * e + 1]);
+                        }
+                    }
                     dst[c] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
                                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
                 }
