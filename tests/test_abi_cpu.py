@@ -207,3 +207,31 @@ def test_step_rejects_bad_flags_before_touching_the_counter(lib):
     st = lib.fp8_linear_step_delayed(ctypes.byref(m), ctypes.byref(cnt), ctypes.byref(io),
                                      16, 16, 16, None, None)
     assert st == 1 and cnt.value == 7
+
+
+def test_recipe_steps_host_checks(lib):
+    from scaled_linear_layers_gb300 import _lib
+    good = 0x2000
+    io = _lib.fp8_linear_step_io()
+    for name in ("x", "w", "xq", "wq", "wqt", "amax", "y"):
+        setattr(io, name, good)
+    P = ctypes.c_void_p
+    # dynamic: scales and workspace are required; dbias and flags are not supported
+    assert lib.fp8_linear_step_dynamic(ctypes.byref(io), None, P(good), 16, 16, 16, None) == 1
+    io.dbias = good
+    assert lib.fp8_linear_step_dynamic(ctypes.byref(io), P(good), P(good), 16, 16, 16, None) == 4
+    io.dbias = None
+    io.flags = 1
+    assert lib.fp8_linear_step_dynamic(ctypes.byref(io), P(good), P(good), 16, 16, 16, None) == 2
+    io.flags = 0
+    assert lib.fp8_linear_step_dynamic(ctypes.byref(io), P(good), P(good), 16, 24, 16, None) == 3
+    # block: dims multiples of 128, every scale array, no bias
+    sc = _lib.fp8_block_step_scales()
+    for name, _ in sc._fields_:
+        setattr(sc, name, good)
+    assert lib.fp8_linear_step_block(ctypes.byref(io), ctypes.byref(sc), 128, 128, 192, None) == 3
+    io.bias = good
+    assert lib.fp8_linear_step_block(ctypes.byref(io), ctypes.byref(sc), 128, 128, 128, None) == 4
+    io.bias = None
+    sc.g_scale_t = None
+    assert lib.fp8_linear_step_block(ctypes.byref(io), ctypes.byref(sc), 128, 128, 128, None) == 1
