@@ -1,6 +1,9 @@
 // C-ABI entry points: host-side validation, then launches on the caller's
-// stream.  Nothing here allocates device memory or synchronises (except
-// fp8_check_device_status).
+// stream.  Nothing here allocates device memory; nothing synchronises except
+// fp8_check_device_status and the meta checkpoint's save and load.  The
+// delayed-scaling step also uses a second stream the library owns (created
+// once per host thread and device), forked from and joined back into the
+// caller's stream with events.
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>

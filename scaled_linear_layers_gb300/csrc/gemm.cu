@@ -15,7 +15,10 @@
 //               by s_A*s_B, add bias, round to bf16 and store; the second
 //               accumulator lets the next tile's MMAs run meanwhile.
 // Every mbarrier wait is bounded; on expiry the kernel records a status bit,
-// drains its own MMAs and frees its TMEM before returning.
+// drains its own MMAs and frees its TMEM before returning.  This one-CTA
+// kernel serves problems too small for a wave of 256-row pair tiles (and
+// every shape when FP8LINEAR_GEMM_PAIR=0); the 2-SM kernel in gemm_pair.cu
+// takes the rest, and launch_gemm_tensor2 puts two problems in one launch.
 #include <cuda.h>
 
 #include <cstdlib>
