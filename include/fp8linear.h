@@ -185,7 +185,8 @@ fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, i
  * Tensorwise recipes (DELAYED, DYNAMIC): x_scale, w_scale, g_scale are [1].
  * BLOCK recipe: activation/gradient scales are per 1x128 tile of the operand
  * as passed (row-major [rows, contraction/128]) and w_scale is the 128x128
- * grid [N/128, K/128] of W.
+ * grid [N/128, K/128] of W.  Under BLOCK the scale pointers must also be
+ * 16-byte aligned (else FP8_ERR_ALIGNMENT).
  * Source: AstrAI fp8_state.py comment "D = A_SCALE * B_SCALE * A * B" and
  * fp8_linear_forward / fp8_linear_backward. */
 

@@ -350,6 +350,11 @@ static fp8_status gemm_common(const char *who, const uint8_t *A, const float *sa
     FP8_ALIGN(A, who);
     FP8_ALIGN(B, who);
     FP8_ALIGN(D, who);
+    if (r == FP8_RECIPE_BLOCK) {
+        // the block kernel stages per-row B scales with 16-byte async copies
+        if (!aligned16(sa) || !aligned16(sb))
+            return fail(FP8_ERR_ALIGNMENT, "%s: block scales are not 16-byte aligned", who);
+    }
     if (r != FP8_RECIPE_DELAYED && r != FP8_RECIPE_DYNAMIC && r != FP8_RECIPE_BLOCK)
         return fail(FP8_ERR_SHAPE, "%s: recipe %d is not a GEMM recipe", who, (int)r);
     return check_device(who);

@@ -3,29 +3,31 @@
 //
 //   D[i,j] = bf16( sum_kb sA(i,kb) * sB(j,kb) * sum_{k in block kb} A[i,k] B[j,k] )
 //
-// One persistent CTA per SM owns 128 x 128 output tiles.  The contraction is
-// walked in groups of two 128-deep blocks: one TMA stage, one round of MMAs
-// and one hand-off per group.  The MMA warp writes each block's partial
-// product (fresh accumulation) into its own 128-column TMEM slot; the four
-// slots form two group slots, so the MMAs of one group run while the
-// promotion reads the other.  Eight epilogue warps (two per TMEM lane
-// quarter, 64 columns each) read a group's partials back one block at a
-// time, hand the group slot back after the last read and fold each partial
-// into fp32 register accumulators with its two block scales (packed fp32x2
-// FMAs for per-tile B, a multiply and an FMA per element for per-row B).  A hand-off costs a few hundred cycles of barrier traffic
-// whatever it carries, so pairing the blocks halves that cost per block.
-// B's scale is one value per 128-row tile (weights) or one per row (wgrad's
-// Xᵀ operand: each warp stages its 64 scales of the next group into shared
-// memory with cp.async, from a layout contiguous over rows).  Every handshake
-// is local to the SM, and every wait is bounded, as in the other GEMM kernels.
+// One persistent CTA per SM owns 128 x 256 (or 128 x 128) output tiles.  The
+// contraction is walked in groups (one 128-deep block for 256-wide tiles, two
+// for 128-wide ones): one TMA stage, one round of MMAs and one hand-off per
+// group.  The MMA warp writes each block's partial product (fresh
+// accumulation) into its own TMEM slot; the slots form two group slots, so
+// the MMAs of one group run while the promotion reads the other.  Eight
+// epilogue warps (two per TMEM lane quarter, half the tile's columns each)
+// read a group's partials back, hand the group slot back after the last read
+// and fold each partial into fp32 register accumulators with its two block
+// scales (a packed fp32x2 FMA per pair for per-tile B; a multiply and an FMA
+// per element or pair for per-row B).  A hand-off costs a few hundred cycles
+// of barrier traffic whatever it carries, so each carries 128 x 256 partial
+// products.  B's scale is one value per 128-row tile (weights) or one per row
+// (wgrad's Xᵀ operand: each warp stages its columns' scales of the next group
+// into shared memory with cp.async, from a layout contiguous over rows; with
+// wide tiles each thread reads four rows x 32 columns of the partial, so that
+// it needs a quarter of those scales).  Every handshake is local to the SM
+// (or the CTA pair), and every wait is bounded, as in the other GEMM kernels.
 //
 // The same pipeline also runs on CTA pairs (tcgen05 cta_group::2,
-// as in the tensorwise pair kernel): a pair owns a 256 x 128 tile, each CTA
-// loads its 128 rows of A and 64 rows of B, the leader issues M=256 MMAs whose
-// rows land in both CTAs' TMEM, commits multicast to both, and both CTAs'
-// epilogue warps hand group slots back to the leader.  Each SM then streams
-// 128 x (128 + 64) operand bytes per block instead of 128 x (128 + 128), with
-// the same promotion work per SM.
+// as in the tensorwise pair kernel): a pair owns a 256 x BN tile, each CTA
+// loads its 128 rows of A and BN/2 rows of B, the leader issues M=256 MMAs
+// whose rows land in both CTAs' TMEM, commits multicast to both, and both
+// CTAs' epilogue warps hand group slots back to the leader.  Each SM then
+// streams half of B's bytes, with the same promotion work per SM.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -38,46 +40,81 @@ extern uint64_t g_wait_limit_ns;
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 128;
-constexpr int KG = 2;      // contraction blocks per group (stage, MMA round, hand-off)
+constexpr int BM = 128, BK = 128;
 constexpr int GSLOTS = 2;  // group slots of KG TMEM slots each
 constexpr int A_BLK = BM * BK;
-// B rows each CTA loads per block: the whole N tile, or half of it in a pair
-template <bool kPair> struct Shape {
-    static constexpr int B_ROWS = kPair ? BN / 2 : BN;
-    static constexpr int B_BLK = B_ROWS * BK;
-    static constexpr int A_STAGE = KG * A_BLK, B_STAGE = KG * B_BLK;
-    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int STAGES = kPair ? 4 : 3;  // TMA ring depth, in groups
-    static constexpr uint32_t IDESC = idesc_f8_f32(kPair ? 2 * BM : BM, BN);
-};
 #ifndef FP8_BLOCK_EPI_WARPS
 #define FP8_BLOCK_EPI_WARPS 8
 #endif
 constexpr int EPI_WARPS = FP8_BLOCK_EPI_WARPS;  // 8 or 16
-constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
-constexpr int COLS = BN * 4 / EPI_WARPS;  // accumulator columns per epilogue thread
-static_assert(COLS % 32 == 0 && COLS >= 32, "each epilogue warp reads whole 32-column loads");
-constexpr uint32_t TMEM_COLS = GSLOTS * KG * BN;  // 512
-static_assert(TMEM_COLS == 512, "the four block slots fill TMEM");
 constexpr int GROUP_M = 8;
 // Scales are fetched PD groups ahead of their use.  One group (about 0.7 us
 // at the block workload's speed) measured best: deeper prefetch costs
 // registers the promotion needs (32768 x 8192 x 8192, PD 1/2/3: fprop 1828 /
 // 1772 / 1730, wgrad 1298 / 881 / 886 TFLOP/s).
+// Wide tiles: the TMEM load of the next 32-column chunk is in flight while
+// the current chunk is folded in (wgrad 1476 against 1449 TFLOP/s without;
+// fprop unchanged at 2552-2554).
+#ifndef FP8_BLOCK_PIPE
+#define FP8_BLOCK_PIPE 1
+#endif
 #ifndef FP8_BLOCK_PREFETCH
 #define FP8_BLOCK_PREFETCH 1
 #endif
 constexpr int PD = FP8_BLOCK_PREFETCH;
 static_assert(PD >= 1 && PD <= 4, "prefetch distance");
-// per-warp B-row scales: [PD + 1 groups in flight][KG blocks][COLS]
-constexpr int SBUF_FLOATS = EPI_WARPS * (PD + 1) * KG * COLS;
-template <bool kPair>
-constexpr size_t smem_bytes() {
-    return 1024 + (size_t)Shape<kPair>::STAGES * Shape<kPair>::STAGE_BYTES +
-           SBUF_FLOATS * sizeof(float) + 256;
-}
-static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "smem");
+
+// Tile geometry.  kBN = 128: two contraction blocks per group in four
+// 128-column TMEM slots, 64 accumulator columns per epilogue thread; warps 0
+// (TMA) and 1 (MMA) then the epilogue warps, 10 in all, which caps a thread at
+// 168 registers (three warps share some SM sub-partitions).  kBN = 256: one
+// block per group in two 256-column slots and 128 accumulator columns per
+// thread, which do not fit in 168 registers: the CTA has three warpgroups
+// (TMA, MMA and two idle warps; then the eight epilogue warps) and moves
+// registers from the first to the others with setmaxnreg, 40 + 2 x 232 per
+// lane of a warp triple = 3 x 168, the launch's own allocation.  Either way a
+// hand-off carries 128 x 256 partial products.
+template <bool kPair, int kBN> struct Shape {
+    static constexpr int BN = kBN;
+    static constexpr int KG = kBN == 256 ? 1 : 2;  // contraction blocks per group
+    // B rows each CTA loads per block: the whole N tile, or half of it in a pair
+    static constexpr int B_ROWS = kPair ? BN / 2 : BN;
+    static constexpr int B_BLK = B_ROWS * BK;
+    static constexpr int A_STAGE = KG * A_BLK, B_STAGE = KG * B_BLK;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;  // TMA ring depth, in groups
+    static constexpr uint32_t IDESC = idesc_f8_f32(kPair ? 2 * BM : BM, BN);
+    static constexpr int COLS = BN * 4 / EPI_WARPS;  // accumulator columns per epilogue thread
+    // 32-column TMEM loads per wait: with 128 accumulator columns a second
+    // load in flight costs more in registers than it saves in latency
+    // (32768 x 8192 x 8192, one CTA: fprop 2582 / 2565 / 2029 TFLOP/s for 1 /
+    // 2 / 4 loads per wait)
+    static constexpr int CH = COLS >= 128 ? 1 : 2;
+    // per-row B, wide tiles: each epilogue thread reads four rows x 32
+    // columns of the accumulator (16-lane TMEM loads) instead of one row x 128
+    // columns, so that it needs 32 column scales per block instead of 128: the
+    // broadcast shared-memory loads of those scales, not the arithmetic, bound
+    // the one-row form (ncu: 639 M shared wavefronts per wgrad launch, L1 83 %
+    // busy).  128-wide tiles keep one row per thread with scalar arithmetic
+    // (1374 TFLOP/s against 1265 for packed pairs at 168 registers).
+    static constexpr bool ROWS4 = kBN == 256;
+    static constexpr uint32_t TMEM_COLS = GSLOTS * KG * BN;
+    static constexpr bool SPLIT_REGS = kBN == 256;
+    static constexpr int EPI0 = SPLIT_REGS ? 4 : 2;  // first epilogue warp
+    static constexpr int THREADS = 32 * (EPI0 + EPI_WARPS);
+    static constexpr int REGS_LOW = 40, REGS_HIGH = 232;
+    static_assert(!SPLIT_REGS || (EPI_WARPS == 8 && 128 * REGS_LOW + 256 * REGS_HIGH <= 384 * 168),
+                  "the register split fits the 384-thread launch's allocation");
+    // per-warp B-row scales: [PD + 1 groups in flight][KG blocks][COLS]
+    static constexpr int SBUF_FLOATS = EPI_WARPS * (PD + 1) * KG * COLS;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES +
+                                   SBUF_FLOATS * sizeof(float) + 256;
+    static_assert(COLS % 32 == 0 && COLS >= 32, "each epilogue warp reads whole 32-column loads");
+    static_assert((COLS / 32) % CH == 0, "loads per wait divide a thread's columns");
+    static_assert(TMEM_COLS == 512, "the block slots fill TMEM");
+    static_assert(STAGES >= 3, "TMA ring depth");
+    static_assert(SMEM <= 227 * 1024, "smem");
+};
 
 struct BlockArgs {
     int M, N, K;
@@ -98,6 +135,13 @@ __device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
 
+// d = a * b on two fp32 lanes (round to nearest)
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // d = a * b + c on two fp32 lanes (each lane one IEEE fma, round to nearest)
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t d;
@@ -105,12 +149,15 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-template <bool kPerRowB, bool kPair>
+template <bool kPerRowB, bool kPair, int kBN>
 __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const CUtensorMap &tma_b,
                                                 const BlockArgs &p) {
-    using S = Shape<kPair>;
+    using S = Shape<kPair, kBN>;
     constexpr int STAGES = S::STAGES, A_STAGE = S::A_STAGE, B_STAGE = S::B_STAGE;
-    constexpr int B_BLK = S::B_BLK;
+    constexpr int B_BLK = S::B_BLK, BN = S::BN, KG = S::KG, COLS = S::COLS, CH = S::CH;
+    constexpr int SBUF_FLOATS = S::SBUF_FLOATS;
+    constexpr uint32_t TMEM_COLS = S::TMEM_COLS;
+    constexpr int EPI0 = S::EPI0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -170,8 +217,16 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
     const uint32_t tmem_base = *tmem_holder;
     pdl_wait_prior();  // set-up done; the previous kernel's results are needed from here
     pdl_allow_next();
+    // register split (wide tiles): each warp of the first warpgroup gives
+    // registers back as it enters its role, each epilogue warp takes more;
+    // inside the branches so that the compiler sizes each role to its limit
+    auto regs_low = [] {
+        if constexpr (S::SPLIT_REGS)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::REGS_LOW));
+    };
 
     if (warp == 0) {
+        regs_low();
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             int stage = 0;
@@ -228,6 +283,7 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
             }
         }
     } else if (warp == 1) {
+        regs_low();
         if (lane == 0 && rank == 0) {
             // ------------------------------------------- MMA issuer (leader)
             int stage = 0;
@@ -280,15 +336,159 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
             volatile int no_abort = 0;
             mbar_wait_bounded(drain, 0, &no_abort, p.wait_limit_ns, kStatusTimeoutMma, p.status);
         }
+    } else if (warp < EPI0) {
+        regs_low();  // idle warps of the first warpgroup
     } else {
         // ------------------------------------------------- epilogue (8 warps)
-        const int quarter = warp & 3;
-        const int group = (warp - 2) >> 2;  // columns group*COLS .. +COLS-1 of the tile
-        float *wbuf = sbuf + (warp - 2) * (PD + 1) * KG * COLS;  // [PD+1][KG][COLS] B-row scales
+        if constexpr (S::SPLIT_REGS)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::REGS_HIGH));
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int group = (warp - EPI0) >> 2;  // columns group*COLS .. +COLS-1 of the tile
+        float *wbuf = sbuf + (warp - EPI0) * (PD + 1) * KG * COLS;  // [PD+1][KG][COLS] B-row scales
         constexpr int PER_LANE = COLS / 32;                // B-row scales each lane stages
         const BlockScales &sc = p.sc;
         bool ok = true;
         uint32_t g = 0;
+        if constexpr (kPerRowB && S::ROWS4) {
+            // Four-row fragments: thread t of a warp holds rows 8i + t/4
+            // (i = 0..3) of its lane quarter and, in each 8-column group j of
+            // its COLS columns, columns 8j + 2(t%4) and +1, as packed pairs.
+            static_assert(KG == 1 && CH == 1, "wide tiles: one block per group");
+            const int fr = lane >> 2, fc = lane & 3;
+            for (int tile = unit; tile < num_tiles; tile += units) {
+                int tm, tn;
+                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+                const int row0 = tm * TM + (int)rank * BM + quarter * 32 + fr;
+                const int j0 = tn * BN + group * COLS;
+                const float *sa_rows[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    sa_rows[i] = sc.sa + (int64_t)min(row0 + 8 * i, p.M - 1) * sc.sa_row;
+                const float *sb_ptr =
+                    sc.sb + (int64_t)min(j0 + PER_LANE * lane, p.N - PER_LANE) * sc.sb_row;
+                uint64_t acc[4][COLS / 8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < COLS / 8; ++j) acc[i][j] = 0ull;
+                float sa_pf[PD][4];
+                auto fetch = [&](int qn, float (&sa)[4]) {
+                    const int kb = min(qn, nk - 1);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sa[i] = sa_rows[i][(int64_t)kb * sc.sa_k];
+                };
+#pragma unroll
+                for (int d = 0; d < PD; ++d) fetch(d, sa_pf[d]);
+                auto stage_scales = [&](int qn) {
+                    if (qn < ngroups) {
+                        const float *src = sb_ptr + (int64_t)qn * sc.sb_k;
+                        float *dst = wbuf + (qn % (PD + 1)) * COLS + PER_LANE * lane;
+                        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)),
+                                     "l"(src), "n"(PER_LANE * 4)
+                                     : "memory");
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                };
+                for (int d = 0; d < PD; ++d) stage_scales(d);
+                for (int q = 0; q < ngroups; ++q, ++g) {
+                    const uint32_t gs = g % GSLOTS, gphase = (g / GSLOTS) & 1u;
+                    uint64_t sa2[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sa2[i] = pack2(sa_pf[0][i], sa_pf[0][i]);
+#pragma unroll
+                    for (int d = 0; d + 1 < PD; ++d)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) sa_pf[d][i] = sa_pf[d + 1][i];
+                    fetch(q + PD, sa_pf[PD - 1]);
+                    asm volatile("cp.async.wait_group %0;" ::"n"(PD - 1) : "memory");
+                    __syncwarp();
+                    stage_scales(q + PD);
+                    if (ok)
+                        ok = mbar_wait_bounded<true>(&sfull[gs], gphase, abort_flag,
+                                                     p.wait_limit_ns, kStatusTimeoutEpilogue,
+                                                     p.status);
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) continue;
+                    tc_fence_after();
+                    const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                           gs * BN + (uint32_t)(group * COLS);
+                    const float *buf = wbuf + (q % (PD + 1)) * COLS + 2 * fc;
+                    constexpr int NC = COLS / 32;
+                    auto hand_back = [&] {  // the block's partial is in registers
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (kPair)
+                                mbar_arrive_cluster(mapa_shared(smem_u32(&sempty[gs]), 0));
+                            else
+                                mbar_arrive(&sempty[gs]);
+                        }
+                    };
+                    // chunk c's lanes +0..15 / +16..31 of the quarter in
+                    // ra / rb [c % 2]; with FP8_BLOCK_PIPE the load of chunk
+                    // c + 1 is in flight while chunk c is folded in
+                    uint32_t ra[2][16], rb[2][16];
+                    if (FP8_BLOCK_PIPE) {
+                        tmem_ld_16x256b_x4(taddr, ra[0]);
+                        tmem_ld_16x256b_x4(taddr + (16u << 16), rb[0]);
+                        tmem_ld_wait();
+                        tmem_regs_ready(ra[0]);
+                        tmem_regs_ready(rb[0]);
+                        if (NC == 1) hand_back();
+                    }
+#pragma unroll
+                    for (int c0 = 0; c0 < NC; ++c0) {
+                        uint32_t(&r0)[16] = ra[c0 & 1];
+                        uint32_t(&r1)[16] = rb[c0 & 1];
+                        if (!FP8_BLOCK_PIPE) {
+                            tmem_ld_16x256b_x4(taddr + 32 * c0, r0);
+                            tmem_ld_16x256b_x4(taddr + (16u << 16) + 32 * c0, r1);
+                            tmem_ld_wait();
+                            tmem_regs_ready(r0);
+                            tmem_regs_ready(r1);
+                            if (c0 + 1 == NC) hand_back();
+                        } else if (c0 + 1 < NC) {
+                            tmem_ld_16x256b_x4(taddr + 32 * (c0 + 1), ra[(c0 + 1) & 1]);
+                            tmem_ld_16x256b_x4(taddr + (16u << 16) + 32 * (c0 + 1), rb[(c0 + 1) & 1]);
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = 4 * c0 + jj;
+                            const float2 sbv = *reinterpret_cast<const float2 *>(buf + 8 * j);
+                            const uint64_t sb2 = pack2(sbv.x, sbv.y);
+                            acc[0][j] = fma2(pack2(__uint_as_float(r0[4 * jj]), __uint_as_float(r0[4 * jj + 1])),
+                                             mul2(sb2, sa2[0]), acc[0][j]);
+                            acc[1][j] = fma2(pack2(__uint_as_float(r0[4 * jj + 2]), __uint_as_float(r0[4 * jj + 3])),
+                                             mul2(sb2, sa2[1]), acc[1][j]);
+                            acc[2][j] = fma2(pack2(__uint_as_float(r1[4 * jj]), __uint_as_float(r1[4 * jj + 1])),
+                                             mul2(sb2, sa2[2]), acc[2][j]);
+                            acc[3][j] = fma2(pack2(__uint_as_float(r1[4 * jj + 2]), __uint_as_float(r1[4 * jj + 3])),
+                                             mul2(sb2, sa2[3]), acc[3][j]);
+                        }
+                        if (FP8_BLOCK_PIPE && c0 + 1 < NC) {
+                            tmem_ld_wait();
+                            tmem_regs_ready(ra[(c0 + 1) & 1]);
+                            tmem_regs_ready(rb[(c0 + 1) & 1]);
+                            if (c0 + 2 == NC) hand_back();
+                        }
+                    }
+                }
+                if (ok && j0 < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = row0 + 8 * i;
+                        if (row >= p.M) continue;
+                        uint32_t *dst = reinterpret_cast<uint32_t *>(p.d + (int64_t)row * p.ldd + j0 + 2 * fc);
+#pragma unroll
+                        for (int j = 0; j < COLS / 8; ++j) {
+                            float lo, hi;
+                            unpack2(acc[i][j], lo, hi);
+                            dst[4 * j] = pack_bf16x2(lo, hi);
+                        }
+                    }
+                }
+            }
+        } else {
         for (int tile = unit; tile < num_tiles; tile += units) {
             int tm, tn;
             grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
@@ -373,12 +573,10 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                     if (j >= nb) break;
                     const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                            (gs * KG + j) * BN + (uint32_t)(group * COLS);
-                    uint32_t r[COLS / 32][32];
-#pragma unroll
-                    for (int c = 0; c < COLS / 32; ++c)
-                        tmem_ld_32x32b_x32(taddr + 32 * c, r[c]);
-                    tmem_ld_wait();
-                    if (j == nb - 1) {  // the group's last partial is in registers
+                    const float *buf = wbuf + ((q % (PD + 1)) * KG + j) * COLS;
+                    const float f1 = sa_cur[j] * sb_cur[j];
+                    const uint64_t fts = pack2(f1, f1);
+                    auto hand_back = [&] {  // the group's last partial is in registers
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
@@ -387,23 +585,55 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                             else
                                 mbar_arrive(&sempty[gs]);
                         }
+                    };
+                    // one 32-column load per wait (wide tiles): with
+                    // FP8_BLOCK_PIPE the next chunk's load is in flight while
+                    // the current one is folded in
+                    constexpr bool kPipe = FP8_BLOCK_PIPE && CH == 1;
+                    constexpr int NC = COLS / 32;
+                    uint32_t rp[2][32];
+                    if constexpr (kPipe) {
+                        tmem_ld_32x32b_x32(taddr, rp[0]);
+                        tmem_ld_wait();
+                        tmem_regs_ready(rp[0]);
+                        if (NC == 1 && j == nb - 1) hand_back();
                     }
-                    const float *buf = wbuf + ((q % (PD + 1)) * KG + j) * COLS;
-                    const float f1 = sa_cur[j] * sb_cur[j];
-                    const uint64_t fts = pack2(f1, f1);
-                    if constexpr (kPerRowB) {
 #pragma unroll
-                        for (int a = 0; a < COLS; ++a) {
-                            const float f = __fmul_rn(buf[a], sa_cur[j]);
-                            accs[a] = __fmaf_rn(__uint_as_float(r[a / 32][a % 32]), f, accs[a]);
+                    for (int c0 = 0; c0 < COLS / 32; c0 += CH) {
+                        uint32_t rl[CH][32];
+                        if constexpr (!kPipe) {
+#pragma unroll
+                            for (int c = 0; c < CH; ++c)
+                                tmem_ld_32x32b_x32(taddr + 32 * (c0 + c), rl[c]);
+                            tmem_ld_wait();
+                            if (j == nb - 1 && c0 + CH == COLS / 32) hand_back();
+                        } else if (c0 + 1 < NC) {
+                            tmem_ld_32x32b_x32(taddr + 32 * (c0 + 1), rp[(c0 + 1) & 1]);
                         }
-                    } else {
+                        uint32_t(&r)[CH][32] = *reinterpret_cast<uint32_t(*)[CH][32]>(
+                            kPipe ? &rp[c0 & 1][0] : &rl[0][0]);
+                        if constexpr (kPerRowB) {
 #pragma unroll
-                        for (int a = 0; a < COLS / 2; ++a) {
-                            const uint64_t pv =
-                                pack2(__uint_as_float(r[a / 16][(2 * a) % 32]),
-                                      __uint_as_float(r[a / 16][(2 * a) % 32 + 1]));
-                            acc[a] = fma2(pv, fts, acc[a]);
+                            for (int a = 0; a < 32 * CH; ++a) {
+                                const float f = __fmul_rn(buf[32 * c0 + a], sa_cur[j]);
+                                accs[32 * c0 + a] =
+                                    __fmaf_rn(__uint_as_float(r[a / 32][a % 32]), f, accs[32 * c0 + a]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int a = 0; a < 16 * CH; ++a) {
+                                const uint64_t pv =
+                                    pack2(__uint_as_float(r[a / 16][(2 * a) % 32]),
+                                          __uint_as_float(r[a / 16][(2 * a) % 32 + 1]));
+                                acc[16 * c0 + a] = fma2(pv, fts, acc[16 * c0 + a]);
+                            }
+                        }
+                        if constexpr (kPipe) {
+                            if (c0 + 1 < NC) {
+                                tmem_ld_wait();
+                                tmem_regs_ready(rp[(c0 + 1) & 1]);
+                                if (c0 + 2 == NC && j == nb - 1) hand_back();
+                            }
                         }
                     }
                 }
@@ -427,6 +657,7 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                 }
             }
         }
+        }  // one-row epilogue
     }
 
     __syncwarp();  // lanes that skipped a role wait here for their warp's lane 0
@@ -445,62 +676,66 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
     }
 }
 
-template <bool kPerRowB>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <bool kPerRowB, int kBN>
+__global__ void __launch_bounds__(Shape<false, kBN>::THREADS, 1)
     gemm_f8_block_kernel(const __grid_constant__ CUtensorMap tma_a,
                          const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
-    block_gemm_body<kPerRowB, false>(tma_a, tma_b, p);
+    block_gemm_body<kPerRowB, false, kBN>(tma_a, tma_b, p);
 }
 
-template <bool kPerRowB>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+template <bool kPerRowB, int kBN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<true, kBN>::THREADS, 1)
     gemm_f8_block_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                               const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
-    block_gemm_body<kPerRowB, true>(tma_a, tma_b, p);
+    block_gemm_body<kPerRowB, true, kBN>(tma_a, tma_b, p);
 }
 
-template <bool kPerRowB, bool kPair>
+template <bool kPerRowB, bool kPair, int kBN>
 cudaError_t launch_block(const CUtensorMap &ta, const CUtensorMap &tb, const BlockArgs &args,
                          int grid, cudaStream_t s) {
-    auto kernel = kPair ? gemm_f8_block_pair_kernel<kPerRowB> : gemm_f8_block_kernel<kPerRowB>;
+    auto kernel = kPair ? gemm_f8_block_pair_kernel<kPerRowB, kBN>
+                        : gemm_f8_block_kernel<kPerRowB, kBN>;
+    constexpr size_t smem = Shape<kPair, kBN>::SMEM;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem_bytes<kPair>());
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    return launch_pdl(kernel, grid, NUM_THREADS, smem_bytes<kPair>(), s, ta, tb, args);
+    return launch_pdl(kernel, grid, Shape<kPair, kBN>::THREADS, smem, s, ta, tb, args);
 }
 
-template <bool kPair>
+template <bool kPair, int kBN>
 cudaError_t launch_shape(const uint8_t *A, const uint8_t *B, const BlockArgs &args,
                          cudaStream_t s, const char **why) {
     CUtensorMap ta, tb;
     if (!make_tmap_k128(&ta, A, args.M, args.K, BM) ||
-        !make_tmap_k128(&tb, B, args.N, args.K, Shape<kPair>::B_ROWS)) {
+        !make_tmap_k128(&tb, B, args.N, args.K, Shape<kPair, kBN>::B_ROWS)) {
         *why = "cuTensorMapEncodeTiled failed";
         return cudaErrorInvalidValue;
     }
     const int64_t tm = kPair ? 2 * BM : BM;
-    const int64_t tiles = ((args.M + tm - 1) / tm) * ((args.N + BN - 1) / BN);
+    const int64_t tiles = ((args.M + tm - 1) / tm) * ((args.N + kBN - 1) / kBN);
     const int64_t units = kPair ? num_sms() / 2 : num_sms();
     const int grid = (int)(tiles < units ? tiles : units) * (kPair ? 2 : 1);
-    if (args.sc.b_rows == 1) return launch_block<true, kPair>(ta, tb, args, grid, s);
-    if (args.sc.b_rows == 128) return launch_block<false, kPair>(ta, tb, args, grid, s);
+    if (args.sc.b_rows == 1) return launch_block<true, kPair, kBN>(ta, tb, args, grid, s);
+    if (args.sc.b_rows == 128) return launch_block<false, kPair, kBN>(ta, tb, args, grid, s);
     *why = "B scales must be per row or per 128-row tile";
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-// One-CTA tiles by default.  The pair kernel streams half as many B bytes per
-// SM but measured no faster (32768 x 8192 x 8192: fprop 1857 vs 1845 TFLOP/s,
-// wgrad 1119 vs 1187): at this tile width both run into the promotion's cost
-// per block, not the operand traffic.  FP8LINEAR_BLOCK_PAIR=1 selects it (the
-// tests run both kernels).
+// Kernel choice, measured at 32768 x 8192 x 8192 (TFLOP/s):
+//                       one CTA 128   one CTA 256   pair 128   pair 256
+//   per-tile B (fprop)      1829          2552-2582     1697       1871-1887
+//   per-row B (wgrad)       1374          1476          1311       1489
+// One CTA with 256-wide tiles by default; problems with fewer 128 x 256 tiles
+// than SMs take 128-wide tiles.  FP8LINEAR_BLOCK_PAIR=0/1 and
+// FP8LINEAR_BLOCK_BN=128/256 override the choice (the tests run all four).
 cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
                               const BlockScales &sc, uint16_t *D, cudaStream_t s,
                               const char **why) {
@@ -514,9 +749,15 @@ cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int
     args.wait_limit_ns = g_wait_limit_ns;
     args.status = device_status_word();
     const char *pe = getenv("FP8LINEAR_BLOCK_PAIR");
-    const int pair_mode = pe ? atoi(pe) : -1;
-    return pair_mode == 1 ? launch_shape<true>(A, B, args, s, why)
-                          : launch_shape<false>(A, B, args, s, why);
+    const char *be = getenv("FP8LINEAR_BLOCK_BN");
+    const bool wide = be != nullptr ? atoi(be) == 256
+                                    : ((M + 127) / 128) * ((N + 255) / 256) >= num_sms();
+    const bool pair = pe != nullptr && atoi(pe) == 1;
+    if (wide)
+        return pair ? launch_shape<true, 256>(A, B, args, s, why)
+                    : launch_shape<false, 256>(A, B, args, s, why);
+    return pair ? launch_shape<true, 128>(A, B, args, s, why)
+                : launch_shape<false, 128>(A, B, args, s, why);
 }
 
 }  // namespace fp8

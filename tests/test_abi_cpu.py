@@ -75,6 +75,15 @@ def test_gemm_rejects_unaligned_token_count_with_the_pages_message(lib):
     assert st == 3 and f"but got M={ex['rows']}" in lib.fp8_last_error().decode()
 
 
+def test_gemm_block_recipe_needs_aligned_scale_pointers(lib):
+    # host-side check only: the fake addresses are never dereferenced
+    ok, off = 0x10000, 0x10004
+    st = lib.fp8_linear_wgrad(ok, ok, ok, off, 256, 256, 256, 2, ok, None)
+    assert st == 3 and "block scales are not 16-byte aligned" in lib.fp8_last_error().decode()
+    st = lib.fp8_linear_fprop(ok, off, ok, ok, 256, 256, 256, 2, None, ok, None)
+    assert st == 3 and "block scales are not 16-byte aligned" in lib.fp8_last_error().decode()
+
+
 def test_gemm_block_recipe_needs_multiples_of_128(lib):
     st = lib.fp8_linear_fprop(None, None, None, None, 256, 256, 144, 2, None, None, None)
     assert st == 3 and "divisible by 128" in lib.fp8_last_error().decode()

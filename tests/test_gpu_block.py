@@ -20,12 +20,15 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-@pytest.fixture(params=["one_cta", "cta_pair"])
+@pytest.fixture(params=["one_cta", "cta_pair", "one_cta_n256", "cta_pair_n256"])
 def kernel(request, monkeypatch):
     """Runs a test on the one-CTA kernel and on the CTA-pair kernel (256-row
     pair tiles; with M a multiple of 128 but not of 256 the last pair's peer
-    rows lie past the matrix)."""
-    monkeypatch.setenv("FP8LINEAR_BLOCK_PAIR", "1" if request.param == "cta_pair" else "0")
+    rows lie past the matrix), each with 128- and 256-column tiles (with N a
+    multiple of 128 but not of 256 the last tile's right half lies past the
+    matrix)."""
+    monkeypatch.setenv("FP8LINEAR_BLOCK_PAIR", "1" if "pair" in request.param else "0")
+    monkeypatch.setenv("FP8LINEAR_BLOCK_BN", "256" if request.param.endswith("n256") else "128")
     return request.param
 
 
