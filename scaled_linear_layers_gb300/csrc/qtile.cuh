@@ -26,6 +26,23 @@ __device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v) {
     return max(max(absmax_bits2(v.x), absmax_bits2(v.y)), max(absmax_bits2(v.z), absmax_bits2(v.w)));
 }
 
+// The same maximum with sign bits cleared, unsigned 16-bit lane maxima (one
+// max.u16x2 per pair of words), then the larger half: fewer instructions.
+// Faster in the tile kernels (1x128 row tiles, row+column cast+transpose:
+// 4.70 -> 4.83 TB/s); slower in the tensorwise loop of quantize_kernel
+// (6.04 -> 5.43 TB/s at 2^30 elements), which keeps absmax_bits8.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t absmax_bits8_u16x2(const uint4 &v) {
+    const uint32_t m = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                 max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
+}
+
 // Block-wide max of a per-thread bf16-magnitude bit pattern; result valid in
 // thread 0.  `red` holds one word per warp.
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
@@ -61,7 +78,7 @@ __device__ __forceinline__ void tile_load(const uint16_t *__restrict__ x, int R,
 __device__ __forceinline__ uint32_t tile_absmax_bits(const uint4 (&v)[8]) {
     uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m = max(m, absmax_bits8(v[i]));
+    for (int i = 0; i < 8; ++i) m = max(m, absmax_bits8_u16x2(v[i]));
     return m;
 }
 
