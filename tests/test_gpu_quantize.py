@@ -168,7 +168,9 @@ def test_quantize_transpose_dbias_empty_rows():
     assert not db.float().any()
 
 
-@pytest.mark.parametrize("shape", [(1, 128), (5, 384), (256, 1024), (333, 4096)])
+# 78003 tiles: more than one pass of the persistent grid (152 SMs x 8 CTAs x
+# 64 tiles) and a last group of 8 tiles that is only partly filled
+@pytest.mark.parametrize("shape", [(1, 128), (5, 384), (256, 1024), (333, 4096), (26001, 384)])
 def test_quantize_rowtiles(shape):
     R, C = shape
     x = synth.normal_with_outliers_bf16(shape, 1.0, seed=R, tensor="x")
