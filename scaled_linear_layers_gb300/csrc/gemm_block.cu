@@ -692,20 +692,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<true, kBN>::TH
 
 template <bool kPerRowB, bool kPair, int kBN>
 cudaError_t launch_block(const CUtensorMap &ta, const CUtensorMap &tb, const BlockArgs &args,
-                         int grid, cudaStream_t s) {
+                         int grid, cudaStream_t s, const char **why) {
+    using S = Shape<kPair, kBN>;
     auto kernel = kPair ? gemm_f8_block_pair_kernel<kPerRowB, kBN>
                         : gemm_f8_block_kernel<kPerRowB, kBN>;
-    constexpr size_t smem = Shape<kPair, kBN>::SMEM;
+    constexpr size_t smem = S::SMEM;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (S::SPLIT_REGS) {
+            // setmaxnreg.inc waits until the CTA's own register allocation
+            // (threads x registers per thread at launch) can supply the
+            // raised counts; a build that launched with fewer registers than
+            // the split assumes would wait forever, so it is refused here
+            cudaFuncAttributes fa;
+            cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            if ((int64_t)fa.numRegs * S::THREADS <
+                (int64_t)128 * S::REGS_LOW + (int64_t)(S::THREADS - 128) * S::REGS_HIGH) {
+                *why = "block GEMM: the register split does not fit the kernel's launch allocation";
+                return cudaErrorInvalidConfiguration;
+            }
+        }
         cudaError_t e =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    return launch_pdl(kernel, grid, Shape<kPair, kBN>::THREADS, smem, s, ta, tb, args);
+    return launch_pdl(kernel, grid, S::THREADS, smem, s, ta, tb, args);
 }
 
 template <bool kPair, int kBN>
@@ -721,8 +736,8 @@ cudaError_t launch_shape(const uint8_t *A, const uint8_t *B, const BlockArgs &ar
     const int64_t tiles = ((args.M + tm - 1) / tm) * ((args.N + kBN - 1) / kBN);
     const int64_t units = kPair ? num_sms() / 2 : num_sms();
     const int grid = (int)(tiles < units ? tiles : units) * (kPair ? 2 : 1);
-    if (args.sc.b_rows == 1) return launch_block<true, kPair, kBN>(ta, tb, args, grid, s);
-    if (args.sc.b_rows == 128) return launch_block<false, kPair, kBN>(ta, tb, args, grid, s);
+    if (args.sc.b_rows == 1) return launch_block<true, kPair, kBN>(ta, tb, args, grid, s, why);
+    if (args.sc.b_rows == 128) return launch_block<false, kPair, kBN>(ta, tb, args, grid, s, why);
     *why = "B scales must be per row or per 128-row tile";
     return cudaErrorInvalidValue;
 }
