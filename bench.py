@@ -76,19 +76,83 @@ def profile_traffic(name: str):
     return float(m.group(1)) if m else None
 
 
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+# NVML clock-event reason bits (nvmlClocksEventReason*) of those four
+NVML_REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                    "hw_thermal_slowdown": 0x40}
+
+
+def clock_summary(rows, source):
+    """rows: (sm_mhz, max_sm_mhz, set of reason names) per sample."""
+    if not rows:
+        return None
+    reasons = sorted({r for _, _, rs in rows for r in rs})
+    return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows), "source": source}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock and throttle reasons sampled while the timed region runs.
+
+    Reads NVML (the driver's management library, as nvidia-smi does) from a
+    thread about every millisecond, so that short timed regions still get
+    samples; falls back to nvidia-smi at 50 ms when NVML cannot be loaded.
+    Read-only: no clock or other setting is changed."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_s: float = 0.001):
         self.index = index
+        self.period = period_s
         self.proc = None
         self.lines = []
+        self.rows = []
+        self.nvml = None
+        self.stop = threading.Event()
+        self.t = None
+
+    def _nvml_open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            lib.nvmlShutdown()
+            return False
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        if reasons_fn is None:
+            lib.nvmlShutdown()
+            return False
+        self.nvml = (lib, h, reasons_fn)
+        return True
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, h, reasons_fn = self.nvml
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and  # NVML_CLOCK_SM
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                    reasons_fn(h, ctypes.byref(rs)) == 0):
+                names = {n for n, b in NVML_REASON_BITS.items() if rs.value & b}
+                self.rows.append((float(clk.value), float(mx.value), names))
+            time.sleep(self.period)
 
     def __enter__(self):
+        if self._nvml_open():
+            self.t = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.t.start()
+            t0 = time.time()
+            while not self.rows and time.time() - t0 < 5:
+                time.sleep(0.001)
+            return self
         exe = shutil.which("nvidia-smi")
         if exe:
             self.proc = subprocess.Popen(
@@ -104,13 +168,17 @@ class ClockSampler:
 
     def mark(self):
         """Index of the next sample: samples from here on fall in the region."""
-        return len(self.lines)
+        return len(self.rows) if self.nvml else len(self.lines)
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        if self.nvml:
+            self.stop.set()
+            self.t.join(timeout=2)
+            self.nvml[0].nvmlShutdown()
         if self.proc:
             self.proc.terminate()
             try:
@@ -120,22 +188,20 @@ class ClockSampler:
             self.t.join(timeout=2)
 
     def summary(self, start: int = 0):
+        if self.nvml:
+            return clock_summary(list(self.rows[start:]), "nvml")
         rows = []
         for ln in self.lines[start:]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) != 6:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[2:]))
+                names = {REASON_NAMES[i] for i, v in enumerate(parts[2:])
+                         if v.lower() in ("active", "1")}
+                rows.append((float(parts[0]), float(parts[1]), names))
             except ValueError:
                 continue
-        if not rows:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
-                          if v.lower() in ("active", "1")})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        return clock_summary(rows, "nvidia-smi")
 
 
 # --------------------------------------------------------------- GPU arm ---
