@@ -332,7 +332,8 @@ fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, i
 
 static fp8_status gemm_common(const char *who, const uint8_t *A, const float *sa, const uint8_t *B,
                               const float *sb, int64_t M, int64_t N, int64_t K, fp8_recipe r,
-                              uint16_t *D, const char *mname, const char *nname, const char *kname) {
+                              uint16_t *D, const char *mname, const char *nname, const char *kname,
+                              bool device_check = true) {
     if (M <= 0 || N <= 0 || K <= 0)
         return fail(FP8_ERR_SHAPE, "%s: empty or negative GEMM [%s=%lld, %s=%lld, %s=%lld]", who,
                     mname, (long long)M, nname, (long long)N, kname, (long long)K);
@@ -357,7 +358,7 @@ static fp8_status gemm_common(const char *who, const uint8_t *A, const float *sa
     }
     if (r != FP8_RECIPE_DELAYED && r != FP8_RECIPE_DYNAMIC && r != FP8_RECIPE_BLOCK)
         return fail(FP8_ERR_SHAPE, "%s: recipe %d is not a GEMM recipe", who, (int)r);
-    return check_device(who);
+    return device_check ? check_device(who) : FP8_OK;
 }
 
 fp8_status fp8_linear_fprop(const uint8_t *xq, const float *x_scale, const uint8_t *wq,
@@ -419,7 +420,8 @@ fp8_status fp8_linear_dgrad_wgrad(const uint8_t *gq, const uint8_t *gqt, const f
     if (r == FP8_RECIPE_BLOCK)
         return fail(FP8_ERR_UNSUPPORTED,
                     "%s: the block recipe takes fp8_linear_dgrad and fp8_linear_wgrad", who);
-    FP8_TRY(gemm_common(who, gq, g_scale, wqt, w_scale, M, N, K, r, dx, "M", "N", "K"));
+    // both problems' arguments first, then the device
+    FP8_TRY(gemm_common(who, gq, g_scale, wqt, w_scale, M, N, K, r, dx, "M", "N", "K", false));
     FP8_TRY(gemm_common(who, gqt, g_scale, xqt, x_scale, M, N, K, r, dw, "M", "N", "K"));
     const char *why = nullptr;
     // dX [M,K] = Gq · (Wqᵀ)ᵀ (contraction N); dW [N,K] = Gqᵀ · (Xqᵀ)ᵀ (contraction M)

@@ -244,3 +244,77 @@ def test_recipe_steps_host_checks(lib):
     io.bias = None
     sc.g_scale_t = None
     assert lib.fp8_linear_step_block(ctypes.byref(io), ctypes.byref(sc), 128, 128, 128, None) == 1
+
+
+# Host checks of the remaining entry points.  The fake addresses below are
+# aligned (0x10000) or not (0x10004); none is dereferenced, because every
+# call fails its argument checks before the device is touched.
+OK_P, OFF_P = 0x10000, 0x10004
+
+
+def test_amax_host_checks(lib):
+    assert lib.fp8_amax(OK_P, -1, OK_P, None) == 2
+    assert lib.fp8_amax(OK_P, 8, None, None) == 1
+    assert lib.fp8_amax(None, 8, OK_P, None) == 1
+    assert lib.fp8_amax(OFF_P, 8, OK_P, None) == 3
+    assert "not 16-byte aligned" in lib.fp8_last_error().decode()
+
+
+def test_dgrad_host_checks(lib):
+    # dX [M,K] = Gq [M,N] . Wq [N,K]: each of M, N, K must be a multiple of 16
+    st = lib.fp8_linear_dgrad(OK_P, OK_P, OK_P, OK_P, 4096, 3858, 4096, 0, OK_P, None)
+    assert st == 3 and "Expected N to be divisible by 16, but got N=3858" in lib.fp8_last_error().decode()
+    assert lib.fp8_linear_dgrad(OK_P, OK_P, OK_P, OK_P, 256, 256, 256, 0, None, None) == 1
+    assert lib.fp8_linear_dgrad(OK_P, OK_P, OK_P, OK_P, 0, 256, 256, 0, OK_P, None) == 2
+    assert lib.fp8_linear_dgrad(OK_P, OK_P, OK_P, OK_P, 256, 256, 256, 7, OK_P, None) == 2
+    # block recipe: multiples of 128
+    st = lib.fp8_linear_dgrad(OK_P, OK_P, OK_P, OK_P, 256, 144, 256, 2, OK_P, None)
+    assert st == 3 and "divisible by 128" in lib.fp8_last_error().decode()
+
+
+def test_dgrad_wgrad_host_checks(lib):
+    args = [OK_P] * 7
+    st = lib.fp8_linear_dgrad_wgrad(*args, 256, 256, 256, 2, OK_P, OK_P, None)
+    assert st == 4 and "block recipe" in lib.fp8_last_error().decode()
+    assert lib.fp8_linear_dgrad_wgrad(*args, 256, 256, 264, 0, OK_P, OK_P, None) == 3
+    assert lib.fp8_linear_dgrad_wgrad(*args, 256, 256, 256, 0, OK_P, None, None) == 1
+    assert lib.fp8_linear_dgrad_wgrad(*args, 256, 256, 256, 0, OFF_P, OK_P, None) == 3
+
+
+def test_meta_init_and_refresh_host_checks(lib):
+    from scaled_linear_layers_gb300 import _lib
+    m = _lib.fp8_meta()
+    assert lib.fp8_meta_init(None, OK_P, 16, None) == 1
+    assert lib.fp8_meta_init(ctypes.byref(m), None, 16, None) == 1
+    assert lib.fp8_meta_init(ctypes.byref(m), OFF_P, 16, None) == 3
+    assert lib.fp8_meta_init(ctypes.byref(m), OK_P, 0, None) == 2
+    assert lib.fp8_meta_init(ctypes.byref(m), OK_P, 1025, None) == 2
+    assert m.dev is None  # nothing was initialised
+    assert lib.fp8_meta_refresh(None, None) == 1
+    assert lib.fp8_meta_refresh(ctypes.byref(m), None) == 1  # no device block
+    m.dev, m.interval = OK_P, 0
+    assert lib.fp8_meta_refresh(ctypes.byref(m), None) == 2
+
+
+def test_fused_dynamic_host_checks(lib):
+    assert lib.fp8_quantize_fused_workspace_bytes() == 16384
+    f = lib.fp8_quantize_fused_dynamic
+    assert f(OK_P, 100, 64, OK_P, OK_P, OK_P, None, OK_P, OK_P, None) == 3  # rows % 16
+    assert f(OK_P, -16, 64, OK_P, OK_P, OK_P, None, OK_P, OK_P, None) == 2
+    assert f(OK_P, 64, 64, OK_P, OK_P, None, None, OK_P, OK_P, None) == 1  # q and qt both NULL
+    assert "both NULL" in lib.fp8_last_error().decode()
+    assert f(OK_P, 64, 64, OK_P, OK_P, OK_P, None, OK_P, None, None) == 1  # no workspace
+    assert f(OK_P, 64, 64, OK_P, OK_P, OK_P, None, OK_P, OFF_P, None) == 3
+    assert f(OK_P, 64, 64, None, OK_P, OK_P, None, OK_P, OK_P, None) == 1  # no scale
+    g = lib.fp8_quantize_fused_dynamic_noalloc
+    assert g(OK_P, 100, 64, OK_P, OK_P, OK_P, None, OK_P, None) == 3
+    assert g(OK_P, 64, 64, OK_P, OK_P, None, None, OK_P, None) == 1
+
+
+def test_quantize_transpose_block_needs_column_scales(lib):
+    f = lib.fp8_quantize_transpose
+    # row+column tiles: the column-tile scales are required, the row-tile
+    # ones only when q is written
+    assert f(OK_P, 256, 256, 2, OK_P, OK_P, OK_P, OK_P, None, OK_P, None, None) == 1
+    assert f(OK_P, 256, 256, 2, None, None, OK_P, OK_P, OK_P, OK_P, None, None) == 1
+    assert f(OK_P, 256, 256, 9, OK_P, OK_P, OK_P, OK_P, OK_P, OK_P, None, None) == 2
