@@ -397,8 +397,8 @@ fp8_status fp8_linear_step_dynamic(const fp8_linear_step_io *io, float *scales, 
  * three GEMM calls with the BLOCK / BLOCK_2D recipes.  M, N, K multiples of
  * 128.  io->amax (nullable) receives the tensor amaxes of x, w, g; bias,
  * dbias and flags are not supported (NULL / 0).  Every scale array is
- * required (the forward-only step leaves the column-tile arrays of X
- * written but unused). */
+ * required and 16-byte aligned (the forward-only step leaves the column-tile
+ * arrays of X written but unused). */
 typedef struct {
     float *x_scale, *x_scale_inv;     /* [M, K/128]     row tiles of X (fprop)        */
     float *x_scale_t, *x_scale_inv_t; /* [M/128, K]     column tiles of X (wgrad)     */

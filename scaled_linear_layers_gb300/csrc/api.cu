@@ -812,8 +812,11 @@ fp8_status fp8_linear_step_block(const fp8_linear_step_io *io, const fp8_block_s
     const float *scs[] = {sc->x_scale, sc->x_scale_inv, sc->x_scale_t, sc->x_scale_inv_t,
                           sc->w_scale, sc->w_scale_inv, sc->g_scale, sc->g_scale_inv,
                           sc->g_scale_t, sc->g_scale_inv_t};
-    for (const float *p : scs)
+    for (const float *p : scs) {
         if (p == nullptr) return fail(FP8_ERR_NULL, "%s: a scale array is NULL", who);
+        if (!aligned16(p))  // the block GEMMs stage scales with 16-byte copies
+            return fail(FP8_ERR_ALIGNMENT, "%s: a scale array is not 16-byte aligned", who);
+    }
     const void *ptrs[] = {io->x, io->w, io->g, io->xq, io->xqt, io->wq, io->wqt,
                           io->gq, io->gqt, io->y, io->dx, io->dw};
     for (const void *p : ptrs)

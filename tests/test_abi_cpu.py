@@ -244,6 +244,9 @@ def test_recipe_steps_host_checks(lib):
     io.bias = None
     sc.g_scale_t = None
     assert lib.fp8_linear_step_block(ctypes.byref(io), ctypes.byref(sc), 128, 128, 128, None) == 1
+    sc.g_scale_t = good + 4  # misaligned: rejected before the quantisers are enqueued
+    assert lib.fp8_linear_step_block(ctypes.byref(io), ctypes.byref(sc), 128, 128, 128, None) == 3
+    assert "scale array is not 16-byte aligned" in lib.fp8_last_error().decode()
 
 
 # Host checks of the remaining entry points.  The fake addresses below are
