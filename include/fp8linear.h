@@ -10,8 +10,9 @@
  * with every operand quantised to E4M3 and every GEMM computed as
  * D = s_A · s_B · (A · B) with fp32 accumulation and a bf16 result.  Sources:
  * AstrAI "astrai/extension/fp8_state.py" (the comment above FP8TensorMeta:
- * "D = A_SCALE * B_SCALE * A * B", per-tensor scales amax/448, quantisation
- * multiplies by 1/scale; fp8_linear_forward / fp8_linear_backward), the
+ * the GEMM scales its product by both operands' scales, per-tensor scales are
+ * amax/448, quantisation multiplies by 1/scale; fp8_linear_forward /
+ * fp8_linear_backward), the
  * SpecForge "Add training.fp8_linear" page (dynamic tensorwise scaling; token
  * counts must be a multiple of 16) and the NeMo "Add FP8 support for
  * SALMAutomodel" page (TE recipe=block, padding appended at the end).
@@ -91,7 +92,8 @@ fp8_status fp8_amax(const uint16_t *x, int64_t n, float *amax_out, cudaStream_t 
  *            [rows/128, cols/128]; amax_out nullable.
  * Any rows, cols >= 0 for DELAYED/DYNAMIC (n = rows*cols need not be a
  * multiple of anything).  Source: AstrAI fp8_state.py, fp8_linear_forward
- * ("the quantize kernel emits the current amax"), _update_delayed_scale. */
+ * (its quantise kernel also yields the tensor's current amax),
+ * _update_delayed_scale. */
 fp8_status fp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, fp8_recipe r,
                         float *scale, float *scale_inv, uint8_t *q, float *amax_out,
                         cudaStream_t s);
@@ -187,8 +189,9 @@ fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, i
  * as passed (row-major [rows, contraction/128]) and w_scale is the 128x128
  * grid [N/128, K/128] of W.  Under BLOCK the scale pointers must also be
  * 16-byte aligned (else FP8_ERR_ALIGNMENT).
- * Source: AstrAI fp8_state.py comment "D = A_SCALE * B_SCALE * A * B" and
- * fp8_linear_forward / fp8_linear_backward. */
+ * Source: AstrAI fp8_state.py, the comment above FP8TensorMeta (the product
+ * is scaled by A's and B's scales) and fp8_linear_forward /
+ * fp8_linear_backward. */
 
 /* y [M,N] = bf16( x_scale·w_scale · xq[M,K] · wq[N,K]ᵀ + bias[N] ).
  * bias (bf16 [N]) is nullable; it is added in fp32 before the bf16 rounding.
