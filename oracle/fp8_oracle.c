@@ -10,11 +10,11 @@
  *     values for the nearest one, ties to the even code, saturating at 448.
  *     The format and its 448 maximum come from the AstrAI page
  *     "astrai/extension/fp8_state.py", module constant E4M3_MAX; the
- *     saturating round-to-nearest-even cast is the plainest reading of a
- *     "saturating E4M3 quantisation" where the pages name no rounding mode.
+ *     saturating round-to-nearest-even cast is the plainest reading of
+ *     saturating E4M3 quantisation where the pages name no rounding mode.
  *   - scale = amax/448 and scale_inv = 448/amax, each one IEEE fp32 division
- *     (same page, comment above FP8TensorMeta: D = A_SCALE * B_SCALE * A * B,
- *     quantisation multiplies by 1/scale; _update_delayed_scale clamps the
+ *     (same page, comment above FP8TensorMeta: the GEMM scales its product by
+ *     both operands' scales, quantisation multiplies by 1/scale; _update_delayed_scale clamps the
  *     amax to at least 1e-12 and computes scale_inv directly, not as 1/scale).
  *   - GEMMs are summed in fp64 over dequantised values.  Every product of two
  *     e4m3 values is exact in fp64 and every partial sum of up to 2^15 such
