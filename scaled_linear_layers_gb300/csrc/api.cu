@@ -657,7 +657,9 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     DelayedQuantJob jx{io->x, M, K, d + FP8_META_X_SCALE_INV, io->xq,
                        save_x ? io->xqt : nullptr, io->amax + 0};
     DelayedQuantJob jw{io->w, N, K, d + FP8_META_SCALE_INV, io->wq, io->wqt, io->amax + 1};
-    FP8_TRY(cuda_status(launch_quantize_delayed_pair(jx, jw, s, d + FP8_META_X_SCALE,
+    // W's tiles (q and qᵀ) take the launch's first CTAs and X's (q only) its
+    // last, so the partly filled last wave holds the cheaper tiles
+    FP8_TRY(cuda_status(launch_quantize_delayed_pair(jw, jx, s, d + FP8_META_X_SCALE,
                                                      d + FP8_META_X_SCALE_FWD),
                         who));
     if (overlap) {  // fork: the state update and the backward quantisation

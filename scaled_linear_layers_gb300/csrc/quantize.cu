@@ -429,10 +429,12 @@ __global__ void __launch_bounds__(256, 4) quantize_transpose_kernel(const QtJobs
             if (q != nullptr && gr < R && gc < C)
                 *reinterpret_cast<uint2 *>(q + (int64_t)gr * C + gc) = make_uint2(t0, t1);
         }
-        const int wcol = (chunk * 2) ^ (4 * (row >> 4));
-        *reinterpret_cast<uint2 *>(&tile[row * 32 + wcol]) = make_uint2(t0, t1);
+        if (qt != nullptr) {  // bytes for the transpose (the same for the whole CTA)
+            const int wcol = (chunk * 2) ^ (4 * (row >> 4));
+            *reinterpret_cast<uint2 *>(&tile[row * 32 + wcol]) = make_uint2(t0, t1);
+        }
     }
-    if (qt == nullptr) return;  // 2D-tile quantisation without the transpose
+    if (qt == nullptr) return;  // q only: no transpose
     __syncthreads();
 
     tile_transpose_store(tile, qt, R, C, r0, c0);
