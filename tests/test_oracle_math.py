@@ -161,6 +161,43 @@ def test_sqtiles_reduce_to_tensorwise_when_tile_amaxes_agree():
     assert np.array_equal(q, qd)
 
 
+def test_tile_scales_and_codes_worked_by_hand():
+    """Closed forms chosen so that every product is exact.  e4m3 code =
+    sign | exponent field (bias 7) << 3 | mantissa: 448 = 1.75 * 2^8 -> 0x7E,
+    112 = 1.75 * 2^6 -> 0x6E, 64 -> 0x68, 72 -> 0x69, 80 -> 0x6A.
+    Row tile 0 has amax 2.0 (scale_inv 448/2 = 224), row tile 1 amax 3.5
+    (scale_inv 128); in tile 1, 0.59375 * 128 = 76 and 0.53125 * 128 = 68 are
+    halfway between codes and go to the even mantissa (80 and 64)."""
+    vals = np.zeros((1, 256), np.float32)
+    vals[0, :128] = 0.5
+    vals[0, 5] = 2.0
+    vals[0, 7] = 0.30078125  # 0.3 in bf16; * 224 = 67.375 -> 64
+    vals[0, 128:] = 0.59375
+    vals[0, 130] = 3.5
+    vals[0, 131] = 0.53125
+    vals[0, 132] = -0.59375
+    x = synth.f32_to_bf16_bits(vals)
+    assert np.array_equal(_f32(x), vals)  # every value is exact in bf16
+    q, s, si = oracle.quantize_rowtiles(x, 128)
+    assert si[0, 0] == np.float32(224.0) and si[0, 1] == np.float32(128.0)
+    assert s[0, 0] == np.float32(1.0 / 224.0) and s[0, 1] == np.float32(3.5 / 448.0)
+    want = np.full(256, 0x6E, np.uint8)
+    want[5], want[7] = 0x7E, 0x68
+    want[128:] = 0x6A
+    want[130], want[131], want[132] = 0x7E, 0x68, 0xEA
+    assert np.array_equal(q[0], want), np.nonzero(q[0] != want)
+    # the same values down a column give the same codes in the transposed copy
+    qt, st, sit = oracle.quantize_coltiles_t(np.ascontiguousarray(x.T), 128)
+    assert np.array_equal(qt[0], want) and np.array_equal(sit[0], si[0])  # scales [cols, rows/128]
+    # one 128x128 weight tile whose largest magnitude is 1.0: scale_inv 448,
+    # -0.25 * 448 = -112 -> 0xEE
+    w = np.full((128, 128), -0.25, np.float32)
+    w[17, 99] = 1.0
+    qw, sw, siw = oracle.quantize_sqtiles(synth.f32_to_bf16_bits(w), 128)
+    assert siw[0, 0] == np.float32(448.0) and sw[0, 0] == np.float32(1.0 / 448.0)
+    assert qw[17, 99] == 0x7E and np.all(np.delete(qw.ravel(), 17 * 128 + 99) == 0xEE)
+
+
 def test_sqtile_amax_brute_force():
     x = synth.normal_with_outliers_bf16((256, 256), 0.02, seed=6, tensor="w")
     _, s, _ = oracle.quantize_sqtiles(x, 128)
