@@ -494,7 +494,7 @@ def oracle_sample_step(step_idx: int, w_h, state_meta, rows_q: int = M, panel: i
     oracle.gemm(xq[:panel], wq, meta.x_scale, meta.scale)            # Y panel
     tg = time.perf_counter() - tg0
     meta.record(amax_w)
-    meta.x_scale, meta.x_scale_inv = ost.lag_update(amax_x)
+    meta.note_x(amax_x)
     gq, amax_g = oracle.quantize(g, meta.g_scale_inv)
     xq2, _ = oracle.quantize(x, meta.x_scale_inv)
     tg0 = time.perf_counter()
@@ -503,7 +503,7 @@ def oracle_sample_step(step_idx: int, w_h, state_meta, rows_q: int = M, panel: i
     oracle.gemm(np.ascontiguousarray(oracle.transpose_u8(gq)[:panel]), oracle.transpose_u8(xq2),
                 meta.g_scale, meta.x_scale)                           # dW panel
     tg += time.perf_counter() - tg0
-    meta.g_scale, meta.g_scale_inv = ost.lag_update(amax_g)
+    meta.note_g(amax_g)
     spent = time.perf_counter() - t0
     full = (spent - tg) * (M / rows_q) + tg * (M / panel) * (M / rows_q)
     return spent, full
@@ -530,8 +530,8 @@ def reference_arm(args, rank, world):
     oracle.build()
     rows_q, panel = reference_sample_size(args.steps + args.warmup)
     w_h = synth.normal_bf16((N, K), CFG["w_sigma"], CFG["seed"], "w")
-    st = ost.State(16)
-    meta = st.new_meta()
+    st = ost.StepCounter(16)
+    meta = st.new_weight()
     for t in range(args.warmup):
         oracle_sample_step(t, w_h, (st, meta), rows_q, panel)
     spent_total, full_total = 0.0, 0.0
@@ -567,8 +567,8 @@ def cpu_baseline_for_gpu_line(steps: int = 2):
     from oracle import state as ost
     oracle.build()
     w_h = synth.normal_bf16((N, K), CFG["w_sigma"], CFG["seed"], "w")
-    st = ost.State(16)
-    meta = st.new_meta()
+    st = ost.StepCounter(16)
+    meta = st.new_weight()
     spent_total, full_total = 0.0, 0.0
     for t in range(steps):
         s, f = oracle_sample_step(t, w_h, (st, meta))

@@ -10,10 +10,11 @@ gcc and ``-ffp-contract=off`` so every fp32 multiply and divide is one IEEE
 operation).  This module is a thin numpy wrapper around it plus the scaling
 state machine in ``state.py``.
 
-Source of every rule: the AstrAI page "astrai/extension/fp8_state.py"
-(module constant E4M3_MAX = 448, the comment above FP8TensorMeta fixing
-D = A_SCALE * B_SCALE * A * B with scale = amax/448, and the functions
-FP8TensorMeta.record/refresh, FP8State.step and _update_delayed_scale).
+Source of every rule: the AstrAI page "astrai/extension/fp8_state.py": its
+E4M3 maximum of 448, its comment on the GEMM layout (D = A_SCALE * B_SCALE *
+A * B, so a tensor's scale is amax/448 and quantising multiplies by the
+inverse), its weight-meta and global-state classes and its delayed-scale
+update.
 """
 from __future__ import annotations
 
@@ -324,13 +325,15 @@ def bias_grad(g: np.ndarray):
 
 def bias_grad_tolerance_ok(got: np.ndarray, ref_bf16: np.ndarray, mag: np.ndarray, rows: int):
     """A GPU bias gradient summed in fp32 in a fixed order and rounded once to
-    bf16 passes if |got - bf16(ref)| <= 2^-8 |ref| + (17 + ceil(rows/128)) *
-    2^-23 * sum|g|: the bf16 rounding is at most half an ulp (2^-9 relative)
-    on each of got and bf16(ref), and a sum of k fp32 terms taken in at most
-    17 + rows/128 sequential additions errs by at most that many units of
-    2^-24 times the sum of magnitudes (doubled for slack)."""
+    bf16 passes if |got - bf16(ref)| <= 2^-7 (1 + 2^-7) |ref| + (17 +
+    ceil(rows/128)) * 2^-23 * sum|g|: bf16 keeps 8 significant bits, so each
+    of got and bf16(ref) is within 2^-8 of its magnitude of the value it
+    rounds, and a sum of k fp32 terms taken in at most 17 + rows/128
+    sequential additions errs by at most that many units of 2^-24 times the
+    sum of magnitudes (doubled for slack)."""
     got = np.asarray(got, np.float64)
-    bound = 2.0 ** -8 * np.abs(ref_bf16) + (17 + -(-rows // 128)) * 2.0 ** -23 * mag
+    bound = (2.0 ** -7 * (1 + 2.0 ** -7) * np.abs(ref_bf16)
+             + (17 + -(-rows // 128)) * 2.0 ** -23 * mag)
     return np.abs(got - ref_bf16) <= bound
 
 
@@ -338,3 +341,27 @@ def gemm_tolerance_ok(d_gpu: np.ndarray, d_ref_bf16: np.ndarray, bound: np.ndarr
     """The stated GEMM bar: |D_gpu - bf16(D_ref)| <= 1e-2 * bound + 1e-3."""
     err = np.abs(d_gpu.astype(np.float64) - d_ref_bf16)
     return err <= 1e-2 * bound + 1e-3
+
+
+def gemm_derived_ok(d_gpu: np.ndarray, d_ref_bf16: np.ndarray, bound: np.ndarray, k: int):
+    """A tighter bar derived from the arithmetic of a scaled FP8 GEMM with an
+    fp32 accumulator and a bf16 result:
+
+        |D_gpu - bf16(D)| <= 2^-7 (1 + 2^-7) |bf16(D)| + (1 + 2^-8) k 2^-23 bound
+
+    with D the exact result and bound = s_a s_b sum_k |a||b|.  Each product of
+    two e4m3 values is exact in fp32; summing k of them in fp32 in any order
+    with round-to-nearest errs by at most (k-1) 2^-24 / (1 - (k-1) 2^-24) times
+    the sum of magnitudes, under k 2^-23 for any k below 2^22; the fp32
+    product of the two scales and the fp32 multiply of the sum by it add two
+    more relative roundings of 2^-24 (and a bias add in fp32 a third), which
+    the (1 + 2^-7) factor covers.  bf16 keeps 8 significant bits, so rounding
+    to it moves a value by at most 2^-8 of its magnitude; the two roundings
+    (of the GPU's fp32 value and of D) together add 2^-7 |D|, and
+    |D| <= |bf16(D)| / (1 - 2^-8).  The block recipe (per-128 partials scaled
+    and summed in fp32) satisfies the same bound when bound carries the
+    per-tile scales."""
+    ref = np.asarray(d_ref_bf16, np.float64)
+    err = np.abs(np.asarray(d_gpu, np.float64) - ref)
+    lim = 2.0 ** -7 * (1 + 2.0 ** -7) * np.abs(ref) + (1 + 2.0 ** -8) * k * 2.0 ** -23 * bound
+    return err <= lim
