@@ -16,10 +16,14 @@ Metric: GEMM TFLOP/s of the whole step (3 x 2*4096^3 FLOP per step divided by
 the step time), plus per-kernel achieved TFLOP/s and GB/s (CUDA events at the
 kernel boundaries of every 10th step), the roofline of the dgrad+wgrad launch,
 an end-to-end figure with host copies, SM clocks sampled during the timed
-region, and the CPU oracle's time on a bounded sample.
+region, and the CPU oracle's time on a bounded sample.  On one GPU the line
+also carries `workloads`: configuration 1's latency (quantise X, W + fprop at
+64x256x256), the MLP block, the packed THD batch and the block recipe
+(whole-step TFLOP/s and each one's dominant kernel), and the quantisers at
+2^30 elements.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-    python bench.py --workload mlp|thd|block|sweep   (the other configurations)
+    python bench.py --workload mlp|thd|block|sweep|config1   (one configuration)
 
 With N > 1 (torchrun), every rank runs an independent replica on its own
 GPU (weak scaling; the path has no exchange on one GPU) and rank 0 reports
@@ -279,6 +283,15 @@ def max_over_ranks(values, device=None):
     return t.tolist()
 
 
+def headline_config(world: int) -> dict:
+    """The headline workload's config, the same dict on both arms."""
+    return {"workload": "one FP8 linear fwd+dgrad+wgrad, delayed scaling, M=N=K=4096, "
+                        "16-step amax history, fresh X/G per step",
+            "M": M, "N": N, "K": K, "recipe": "delayed", "input_sets": N_SETS,
+            "l2": "inputs rotate over 20 X/G sets (1.25 GiB) > 129 MB L2",
+            "parallelism": f"replicas x{world}"}
+
+
 def whole_job_tflops(ms_step: float, world: int) -> float:
     """Every rank runs one full 4096^3 step per step (replicas, weak
     scaling): the job's FLOPs over the slowest rank's step time."""
@@ -435,11 +448,7 @@ def gpu_arm(args, rank, world):
         "vs_baseline": None,
         "dtype": "e4m3 operands, fp32 accumulate, bf16 out",
         "data": "synthetic (seeded normal inputs of the configuration's shapes)",
-        "config": {"workload": "one FP8 linear fwd+dgrad+wgrad, delayed scaling, M=N=K=4096, "
-                               "16-step amax history, fresh X/G per step",
-                   "M": M, "N": N, "K": K, "recipe": "delayed", "input_sets": N_SETS,
-                   "l2": "inputs rotate over 20 X/G sets (1.25 GiB) > 129 MB L2",
-                   "parallelism": f"replicas x{world}"},
+        "config": headline_config(world),
         "roofline": {"bound": "tensor",
                      "achieved": None if gemm_tflops is None else round(gemm_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
@@ -550,9 +559,7 @@ def reference_arm(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 GEMM on decoded e4m3, fp32 scales", "data": "synthetic",
-        "config": {"workload": "one FP8 linear fwd+dgrad+wgrad, delayed scaling, M=N=K=4096, "
-                               "16-step amax history, fresh X/G per step",
-                   "M": M, "N": N, "K": K, "recipe": "delayed"},
+        "config": headline_config(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                          "sample": sample, "cpu_seconds": round(spent_total, 2)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -584,11 +591,13 @@ def cpu_baseline_for_gpu_line(steps: int = 2):
 
 
 # ------------------------------------------------- the other workloads ---
-# `--workload mlp|thd|block|sweep` measures the remaining configurations
-# (one JSON line each; the default line above is the headline workload).
-# Inputs are drawn on the device from a seeded torch generator with the
-# configurations' shapes and distributions (parity of the same paths on
-# host-generated inputs is in tests/test_gpu_configs.py).
+# `--workload mlp|thd|block|sweep|config1` measures one remaining
+# configuration as a line of its own; the default run also carries all of
+# them, briefly, in its line's `workloads` object.  Inputs are drawn on the
+# device from a seeded torch generator with the configurations' shapes and
+# distributions (configuration 1 uses the host generator of the tests);
+# parity of the same paths on host-generated inputs is in
+# tests/test_gpu_configs.py.
 
 def _timed(torch, fn, steps, warmup):
     for t in range(warmup):
@@ -601,6 +610,22 @@ def _timed(torch, fn, steps, warmup):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps  # ms per step
+
+
+def _segments(torch, calls, reps):
+    """Mean ms of each (name, fn) segment over reps runs of the sequence, with
+    an event between consecutive segments (which stops their overlap)."""
+    acc = {n: [] for n, _ in calls}
+    for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        ev[0].record()
+        for i, (_, fn) in enumerate(calls):
+            fn()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        for i, (n, _) in enumerate(calls):
+            acc[n].append(ev[i].elapsed_time(ev[i + 1]))
+    return {n: statistics.mean(v) for n, v in acc.items()}
 
 
 def _seeded_normal(torch, shape, sigma, seed, dev, outliers=None):
@@ -621,12 +646,38 @@ class _DynLinear:
 
     def __init__(self, fp8, torch, dev, M, N, K, x, w, g):
         self.fp8, self.M, self.N, self.K = fp8, M, N, K
+        self.x, self.w, self.g = x, w, g
         self.step = fp8.LinearStep(M, N, K, device=dev)
         self.step.set_inputs(x, w, g)
         self.state = fp8.DynamicStepState(device=dev)
 
     def run(self):
         self.fp8.fp8_linear_step_dynamic(self.state, self.step)
+
+    def calls(self):
+        """The step's launches as the public single calls it is made of (same
+        kernels, same workspaces), in segments: X and W quantised, fprop, G
+        quantised, dgrad and wgrad in one launch."""
+        fp8, io, sc = self.fp8, self.step, self.state.scales
+        M, N, K = self.M, self.N, self.K
+        n = fp8.fp8_quantize_fused_workspace_bytes() // 4
+        ws = [self.state.workspace[i * n:(i + 1) * n] for i in range(3)]
+
+        def quant_xw():
+            fp8.fp8_quantize_fused_dynamic(self.x, sc[0:1], sc[1:2], io.xq, io.xqt, io.amax[0:1],
+                                           ws[0])
+            fp8.fp8_quantize_fused_dynamic(self.w, sc[2:3], sc[3:4], io.wq, io.wqt, io.amax[1:2],
+                                           ws[1])
+        return [
+            ("quant_x_w", quant_xw),
+            ("fprop", lambda: fp8.fp8_linear_fprop(io.xq, sc[0:1], io.wq, sc[2:3], M, N, K,
+                                                   fp8.DYNAMIC, None, io.y)),
+            ("quant_g", lambda: fp8.fp8_quantize_fused_dynamic(self.g, sc[4:5], sc[5:6], io.gq,
+                                                               io.gqt, io.amax[2:3], ws[2])),
+            ("dgrad_wgrad", lambda: fp8.fp8_linear_dgrad_wgrad(io.gq, io.gqt, sc[4:5], io.wqt,
+                                                               sc[2:3], io.xqt, sc[0:1], M, N, K,
+                                                               fp8.DYNAMIC, io.dx, io.dw)),
+        ]
 
 
 def _gemm_line(metric_name, value_tflops, ms, flop, workload, extra, peaks):
@@ -638,7 +689,37 @@ def _gemm_line(metric_name, value_tflops, ms, flop, workload, extra, peaks):
             "config": {"workload": workload, **extra}}
 
 
-def workload_mlp(args):
+def _dominant(kernels, peaks):
+    """The kernel (segment) with the largest time, with its roofline fraction."""
+    name = max(kernels, key=lambda k: kernels[k]["us"])
+    d = dict(kernels[name], kernel=name)
+    if "tflops" in d:
+        d["frac_of_fp8_peak"] = round(d["tflops"] / (peaks["bf16"] * FP8_PER_BF16), 3)
+    if "gbs" in d:
+        d["frac_hbm"] = round(d["gbs"] / peaks["hbm"], 3)
+    return d
+
+
+def _dyn_kernels(torch, projs, reps):
+    """Per-segment µs and TFLOP/s of dynamic-scaling projections, summed over
+    the projections of one step."""
+    tot = {}
+    flops = {"fprop": 0.0, "dgrad_wgrad": 0.0}
+    for p in projs:
+        seg = _segments(torch, p.calls(), reps)
+        for k, v in seg.items():
+            tot[k] = tot.get(k, 0.0) + v
+        flops["fprop"] += 2.0 * p.M * p.N * p.K
+        flops["dgrad_wgrad"] += 4.0 * p.M * p.N * p.K
+    out = {}
+    for k, ms in tot.items():
+        out[k] = {"us": round(ms * 1e3, 1)}
+        if k in flops:
+            out[k]["tflops"] = round(flops[k] / (ms * 1e-3) / 1e12, 1)
+    return out
+
+
+def workload_mlp(args, steps=None, warmup=None):
     import torch
     import scaled_linear_layers_gb300 as fp8
     c = synth.CONFIG3
@@ -651,15 +732,21 @@ def workload_mlp(args):
         g = _seeded_normal(torch, (M, N), c["g_sigma"], 10 * i + 3, dev)
         projs.append(_DynLinear(fp8, torch, dev, M, N, K, x, w, g))
     flop = sum(6.0 * p.M * p.N * p.K for p in projs)
-    ms = _timed(torch, lambda t: [p.run() for p in projs], args.steps, args.warmup)
+    ms = _timed(torch, lambda t: [p.run() for p in projs], steps or args.steps,
+                warmup or args.warmup)
+    kernels = _dyn_kernels(torch, projs, 3)
     fp8.fp8_check_device_status()
-    return _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
+    peaks = load_peaks()
+    line = _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
                       "transformer MLP block, tokens 16384, hidden 4096, FFN 14336 (gate/up "
                       "4096->28672, down 14336->4096), dynamic scaling, fwd+dgrad+wgrad",
-                      {"M": M, "hidden": H, "ffn": F, "recipe": "dynamic"}, load_peaks())
+                      {"M": M, "hidden": H, "ffn": F, "recipe": "dynamic"}, peaks)
+    line["kernels"] = kernels
+    line["dominant_kernel"] = _dominant(kernels, peaks)
+    return line
 
 
-def workload_thd(args):
+def workload_thd(args, steps=None, warmup=None):
     import torch
     import scaled_linear_layers_gb300 as fp8
     c = synth.CONFIG4
@@ -679,16 +766,24 @@ def workload_thd(args):
         fp8.fp8_pad_tokens(x, c["multiple"], xp)
         lin.run()
     flop = 6.0 * Tp * N * K
-    ms = _timed(torch, step, args.steps, args.warmup)
+    ms = _timed(torch, step, steps or args.steps, warmup or args.warmup)
+    pad = _segments(torch, [("pad", lambda: fp8.fp8_pad_tokens(x, c["multiple"], xp))], 3)
+    kernels = _dyn_kernels(torch, [lin], 3)
+    kernels["pad"] = {"us": round(pad["pad"] * 1e3, 1),
+                      "gbs": round(4.0 * T * K / (pad["pad"] * 1e-3) / 1e9, 1)}
     fp8.fp8_check_device_status()
-    return _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
+    peaks = load_peaks()
+    line = _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
                       "packed THD batch, 64 sequences of 128..4096 tokens, zero-padded to a "
                       "multiple of 16, linear 4096->4096, dynamic scaling, pad + fwd+dgrad+wgrad",
                       {"tokens": T, "padded_tokens": Tp, "K": K, "N": N, "recipe": "dynamic"},
-                      load_peaks())
+                      peaks)
+    line["kernels"] = kernels
+    line["dominant_kernel"] = _dominant(kernels, peaks)
+    return line
 
 
-def workload_block(args):
+def workload_block(args, steps=None, warmup=None):
     import torch
     import scaled_linear_layers_gb300 as fp8
     c = synth.CONFIG5
@@ -711,47 +806,63 @@ def workload_block(args):
     y, dx, dw = (torch.empty((M, N), dtype=torch.bfloat16, device=dev),
                  torch.empty((M, K), dtype=torch.bfloat16, device=dev),
                  torch.empty((N, K), dtype=torch.bfloat16, device=dev))
-    ev = {}
 
-    def mark(name):
-        e = torch.cuda.Event(enable_timing=True)
-        e.record()
-        ev.setdefault(name, []).append(e)
-
-    def step(t):
-        mark("quant")
+    def quant():
         fp8.fp8_quantize_transpose(x, fp8.BLOCK, xs, xsi, xq, xqt, xst, xsit)
         fp8.fp8_quantize_transpose(w, fp8.BLOCK_2D, ws, wsi, wq, wqt)
         fp8.fp8_quantize_transpose(g, fp8.BLOCK, gs, gsi, gq, gqt, gst, gsit)
-        mark("fprop")
-        fp8.fp8_linear_fprop(xq, xs, wq, ws, M, N, K, fp8.BLOCK, None, y)
-        mark("dgrad")
-        fp8.fp8_linear_dgrad(gq, gs, wqt, ws, M, N, K, fp8.BLOCK, dx)
-        mark("wgrad")
-        fp8.fp8_linear_wgrad(gqt, gst, xqt, xst, M, N, K, fp8.BLOCK, dw)
-        mark("end")
+    calls = [
+        ("quant_block_x_w_g", quant),
+        ("fprop", lambda: fp8.fp8_linear_fprop(xq, xs, wq, ws, M, N, K, fp8.BLOCK, None, y)),
+        ("dgrad", lambda: fp8.fp8_linear_dgrad(gq, gs, wqt, ws, M, N, K, fp8.BLOCK, dx)),
+        ("wgrad", lambda: fp8.fp8_linear_wgrad(gqt, gst, xqt, xst, M, N, K, fp8.BLOCK, dw)),
+    ]
     flop = 6.0 * M * N * K
-    ms = _timed(torch, step, args.steps, args.warmup)
+    ms = _timed(torch, lambda t: [fn() for _, fn in calls], steps or args.steps,
+                warmup or args.warmup)
+    seg = _segments(torch, calls, 3)
     fp8.fp8_check_device_status()
-    names = ["quant", "fprop", "dgrad", "wgrad", "end"]
-    seg = {n: statistics.mean(a.elapsed_time(b) for a, b in
-                              zip(ev[n][args.warmup:], ev[names[i + 1]][args.warmup:]))
-           for i, n in enumerate(names[:-1])}
+    peaks = load_peaks()
     line = _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
                       "block-scaled recipe (1x128 activation/gradient tiles, 128x128 weight "
                       "tiles), M=32768, K=N=8192, 1% outliers x50, fwd+dgrad+wgrad",
-                      {"M": M, "N": N, "K": K, "recipe": "block"}, load_peaks())
+                      {"M": M, "N": N, "K": K, "recipe": "block"}, peaks)
     gflop = 2.0 * M * N * K
     qbytes = 4 * M * K + 4 * N * K + 4 * M * N + 16 * (M * K + M * N) // 128 + 8 * (N * K) // (128 * 128)
     line["kernels"] = {k: {"us": round(seg[k] * 1e3, 1),
                            "tflops": round(gflop / (seg[k] * 1e-3) / 1e12, 1)}
                        for k in ("fprop", "dgrad", "wgrad")}
-    line["kernels"]["quant_block_x_w_g"] = {"us": round(seg["quant"] * 1e3, 1),
-                                            "gbs": round(qbytes / (seg["quant"] * 1e-3) / 1e9, 1)}
+    qs = seg["quant_block_x_w_g"]
+    line["kernels"]["quant_block_x_w_g"] = {"us": round(qs * 1e3, 1),
+                                            "gbs": round(qbytes / (qs * 1e-3) / 1e9, 1)}
+    line["dominant_kernel"] = _dominant(line["kernels"], peaks)
     return line
 
 
-def workload_sweep(args):
+def _graph_time(torch, fn, reps=20):
+    """Seconds per call of fn, replayed from a CUDA graph of `reps` calls (no
+    host gaps); plain stream launches where a launch form cannot be captured."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        fn(0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e-3, "graph"
+    except Exception:  # a launch form the capture does not take: time it plainly
+        torch.cuda.synchronize()
+        return _timed(torch, fn, reps, 3) * 1e-3, "stream"
+
+
+def workload_sweep(args, lgs=range(20, 31, 2), multi=True, only=None):
     """Quantise-only sweep, n = 2^20 .. 2^30 bf16 elements ([n/4096, 4096]),
     each kernel replayed from a CUDA graph of 20 launches (no host gaps)."""
     import torch
@@ -759,7 +870,7 @@ def workload_sweep(args):
     dev = torch.device("cuda", 0)
     peaks = load_peaks()
     rows_out = []
-    for lg in range(20, 31, 2):
+    for lg in lgs:
         n = 1 << lg
         R, C = n // 4096, 4096
         nbuf = 2 if n >= (1 << 26) else 8
@@ -786,27 +897,9 @@ def workload_sweep(args):
         }
         row = {"n": n}
         for name, (bpe, fn) in cases.items():
-            reps = 20
-            try:
-                g = torch.cuda.CUDAGraph()
-                fn(0)
-                torch.cuda.synchronize()
-                with torch.cuda.graph(g):
-                    for i in range(reps):
-                        fn(i)
-                g.replay()
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                g.replay()
-                e1.record()
-                torch.cuda.synchronize()
-                t = e0.elapsed_time(e1) / reps * 1e-3
-                mode = "graph"
-            except Exception:  # a launch form the capture does not take: time it plainly
-                torch.cuda.synchronize()
-                t = _timed(torch, fn, reps, 3) * 1e-3
-                mode = "stream"
+            if only is not None and name not in only:
+                continue
+            t, mode = _graph_time(torch, fn)
             gbs = bpe * n / t / 1e9
             row[name] = {"us": round(t * 1e6, 2), "gbs": round(gbs, 1),
                          "frac_hbm": round(gbs / peaks["hbm"], 3),
@@ -814,6 +907,14 @@ def workload_sweep(args):
         rows_out.append(row)
         del xs
         torch.cuda.empty_cache()
+    line = {"metric": "quantize GB/s (algorithmic bytes) vs HBM",
+            "value": max(r["cast_transpose_delayed"]["gbs"] for r in rows_out
+                         if "cast_transpose_delayed" in r),
+            "unit": "GB/s", "higher_is_better": True, "data": "synthetic (seeded, on device)",
+            "config": {"workload": "quantise-only sweep, 2^20..2^30 bf16 elements, [n/4096, 4096]"},
+            "hbm_peak_measured": peaks["hbm"], "sweep": rows_out}
+    if not multi:
+        return line
     # many weights in one pass: the MLP block's two weights (gate/up
     # [28672, 4096], down [4096, 14336]) plus 64 [1024, 1024] weights
     ws_multi = [_seeded_normal(torch, (28672, 4096), 0.02, 70, dev),
@@ -823,17 +924,103 @@ def workload_sweep(args):
     am, sm, sim = (torch.empty(nm, dtype=torch.float32, device=dev) for _ in range(3))
     ms = _timed(torch, lambda t: fp8.fp8_multi_amax_scales(ws_multi, am, sm, sim), 20, 3)
     nbytes = 2 * sum(w.numel() for w in ws_multi)
-    multi = {"tensors": nm, "bytes": nbytes, "us": round(ms * 1e3, 2),
-             "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-             "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"], 3)}
+    line["multi_amax_scales"] = {"tensors": nm, "bytes": nbytes, "us": round(ms * 1e3, 2),
+                                 "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                 "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"], 3)}
     del ws_multi
     fp8.fp8_check_device_status()
-    best = max(r["cast_transpose_delayed"]["gbs"] for r in rows_out)
-    return {"metric": "quantize GB/s (algorithmic bytes) vs HBM", "value": best, "unit": "GB/s",
-            "higher_is_better": True, "data": "synthetic (seeded, on device)",
-            "config": {"workload": "quantise-only sweep, 2^20..2^30 bf16 elements, [n/4096, 4096]"},
-            "hbm_peak_measured": peaks["hbm"], "sweep": rows_out,
-            "multi_amax_scales": multi}
+    return line
+
+
+def workload_config1(args, iters=1000):
+    """Configuration 1, the latency case: X [64,256] ~N(0,1), W [256,256]
+    ~N(0,0.02), seed 0, both quantised by the single-launch dynamic quantiser,
+    then fprop: three launches.  Median µs per iteration over `iters`
+    iterations, each bracketed by events (eager: host launch gaps included),
+    and per iteration of a CUDA graph of the three launches replayed
+    back to back (device time only).  A bf16 torch.matmul (cuBLAS) of the
+    same shape is timed the same way as context: the pages report FP8 slower
+    than bf16 on small matmuls."""
+    import torch
+    import scaled_linear_layers_gb300 as fp8
+    c = synth.CONFIG1
+    dev = torch.device("cuda", 0)
+    Mc, Kc, Nc = c["M"], c["K"], c["N"]
+
+    def to_dev(h):
+        return torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
+    x = to_dev(synth.normal_bf16((Mc, Kc), c["x_sigma"], c["seed"], "x"))
+    w = to_dev(synth.normal_bf16((Nc, Kc), c["w_sigma"], c["seed"], "w"))
+    f32 = dict(dtype=torch.float32, device=dev)
+    sc = torch.empty(6, **f32)
+    xq = torch.empty((Mc, Kc), dtype=torch.uint8, device=dev)
+    wq = torch.empty((Nc, Kc), dtype=torch.uint8, device=dev)
+    y = torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev)
+    n = fp8.fp8_quantize_fused_workspace_bytes() // 4
+    wsp = torch.zeros(2 * n, dtype=torch.int32, device=dev)
+
+    def run(_=0):
+        fp8.fp8_quantize_fused_dynamic(x, sc[0:1], sc[1:2], xq, None, sc[4:5], wsp[:n])
+        fp8.fp8_quantize_fused_dynamic(w, sc[2:3], sc[3:4], wq, None, sc[5:6], wsp[n:])
+        fp8.fp8_linear_fprop(xq, sc[0:1], wq, sc[2:3], Mc, Nc, Kc, fp8.DYNAMIC, None, y)
+
+    def median_us(fn):
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)]
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+    eager = median_us(run)
+    t_graph, mode = _graph_time(torch, run, reps=100)
+    fp8.fp8_check_device_status()
+    bf16 = median_us(lambda: torch.matmul(x, w.t()))
+    flop = 2.0 * Mc * Nc * Kc
+    return {"metric": "latency of quantise X, W (dynamic) + fprop", "value": round(eager, 2),
+            "unit": "us", "higher_is_better": False,
+            "config": {"workload": "single FP8 linear fprop, dynamic tensorwise scaling, "
+                                   "X [64,256], W [256,256], seed 0", "M": Mc, "N": Nc, "K": Kc},
+            "launches_per_iteration": 3, "iterations": iters,
+            "median_us_eager": round(eager, 2),
+            "us_per_iteration_graph": round(t_graph * 1e6, 2), "graph_timing": mode,
+            "tflops_graph": round(flop / t_graph / 1e12, 3),
+            "bf16_torch_matmul_median_us": round(bf16, 2),
+            "note": "latency-bound: roofline fractions are not meaningful at this size"}
+
+
+def workloads_summary(args):
+    """Every configuration besides the headline one, briefly, for the default
+    line (rank 0, one GPU): configuration 1's latency, the MLP block, the
+    packed THD batch and the block recipe (whole-step TFLOP/s and the
+    dominant kernel), and the 2^30-element quantisers."""
+    import torch
+    out = {}
+    for key, fn in (("config1_fprop_64x256x256", lambda: workload_config1(args)),
+                    ("config3_mlp_16384x4096x14336", lambda: workload_mlp(args, 5, 3)),
+                    ("config4_thd_64seq_4096", lambda: workload_thd(args, 5, 3)),
+                    ("config5_block_32768x8192x8192", lambda: workload_block(args, 5, 3)),
+                    ("quantize_2^30", lambda: workload_sweep(
+                        args, lgs=[30], multi=False,
+                        only=("amax", "quantize_delayed", "cast_transpose_delayed",
+                              "block_1x128")))):
+        with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+            first = clk.mark()
+            line = fn()
+            clocks = clk.summary(first)
+        for k in ("metric", "higher_is_better", "data", "fp8_peak", "hbm_peak_measured"):
+            line.pop(k, None)
+        line["clocks"] = clocks
+        out[key] = line
+        torch.cuda.empty_cache()
+    if "quantize_2^30" in out:
+        q = out["quantize_2^30"]
+        q["sweep"] = q["sweep"][0]
+    return out
 
 
 def main():
@@ -849,7 +1036,9 @@ def main():
                     help="record kernel-boundary events on every n-th timed step: an event "
                          "between two kernels stops the second from overlapping the first")
     ap.add_argument("--workload", default="linear4096",
-                    choices=["linear4096", "mlp", "thd", "block", "sweep"])
+                    choices=["linear4096", "mlp", "thd", "block", "sweep", "config1"])
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="leave the other configurations out of the default line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -859,7 +1048,7 @@ def main():
         if rank != 0:
             return
         fn = {"mlp": workload_mlp, "thd": workload_thd, "block": workload_block,
-              "sweep": workload_sweep}[args.workload]
+              "sweep": workload_sweep, "config1": workload_config1}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return
     if args.impl == "reference":
@@ -872,6 +1061,8 @@ def main():
         line = gpu_arm(args, rank, world)
         if line is not None:
             line["cpu_baseline"] = cpu
+            if world == 1 and not args.no_workloads:
+                line["workloads"] = workloads_summary(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -166,14 +166,16 @@ fp8_status fp8_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t c
  * fp8_quantize_fused_dynamic.  Its scratch is a 4 KiB array in the library's
  * own static device memory (barrier words plus one partial amax for each of
  * at most 1008 CTAs), which every GPU that loads the library keeps until the
- * process exits; the call returns FP8_ERR_UNSUPPORTED if this GPU's
- * persistent grid would need more slots than that.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress), so make
- * that first call before any stream capture.  Every call clears the barrier
- * words on `s`, and all calls share the one array, so calls that may overlap
- * on the GPU (other streams, other host threads) race: issue them in one
- * stream order.  Nothing here calls cudaMalloc, cudaFree or any allocating
- * routine. */
+ * process exits.  The persistent grid is clamped to those 1008 CTAs (fewer
+ * CTAs walk more tiles each and give the same bytes), so every tensor size
+ * the call accepts fits the array; shapes with more than 2^31 - 1 tiles of
+ * 128 x 128 are rejected with FP8_ERR_SHAPE.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  Every call clears the barrier words
+ * on `s` first (so a call after an FP8_ERR_TIMEOUT starts clean), and all
+ * calls share the one array, so calls that may overlap on the GPU (other
+ * streams, other host threads) race: issue them in one stream order.
+ * Nothing here calls cudaMalloc, cudaFree or any allocating routine. */
 fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, int64_t cols,
                                               float *scale, float *scale_inv, uint8_t *q,
                                               uint8_t *qt, float *amax_out, cudaStream_t s);
@@ -484,6 +486,18 @@ fp8_status fp8_check_device_status(cudaStream_t s);
  * handle FP8_ERR_CUDA; n = 0 clears it.  Entry points that launch several
  * kernels may have enqueued the earlier ones before the failing launch. */
 fp8_status fp8_inject_launch_failures(int32_t n);
+
+/* Limit of every bounded wait in the library's kernels (mbarrier waits of the
+ * GEMMs, the grid barrier of the single-launch dynamic quantiser), in
+ * nanoseconds of the GPU's global timer; default 2 s, and 0 restores the
+ * default.  Returns the previous limit.  A process-wide setting, read when a
+ * kernel is launched (launches already enqueued keep theirs).  A wait that
+ * runs out sets the device status word (FP8_ERR_TIMEOUT from
+ * fp8_check_device_status) and its kernel returns without finishing its
+ * outputs.  For callers that want faster failure detection, and for tests
+ * that drive a wait into its timeout path without faulting or hanging the
+ * GPU.  Host only, no GPU work. */
+uint64_t fp8_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Diagnostic: launches one block that waits on a barrier nothing will ever
  * complete, with a wait limit of timeout_us microseconds (1..1000000); the

@@ -27,7 +27,8 @@ __all__ = [
     "fp8_linear_step_dynamic", "DynamicStepState", "fp8_linear_step_block", "BlockStepScales",
     "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
-    "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_version", "Fp8Meta",
+    "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_set_wait_limit_ns",
+    "fp8_version", "Fp8Meta",
     "fp8_linear_step_delayed", "LinearStep", "fp8_quantize_fused_dynamic",
     "fp8_quantize_fused_workspace_bytes", "fp8_quantize_fused_dynamic_noalloc",
     "Fp8Error", "DELAYED", "DYNAMIC", "BLOCK", "BLOCK_2D", "SLOT_W", "SLOT_X", "SLOT_G",
@@ -393,3 +394,9 @@ def fp8_check_device_status(stream=None):
 
 def fp8_selftest_wait_timeout(timeout_us: int, stream=None):
     _check(_LIB.fp8_selftest_wait_timeout(timeout_us, _stream(stream)))
+
+
+def fp8_set_wait_limit_ns(limit_ns: int) -> int:
+    """Limit of the kernels' bounded waits (0 restores the 2 s default);
+    returns the previous limit."""
+    return int(_LIB.fp8_set_wait_limit_ns(int(limit_ns)))

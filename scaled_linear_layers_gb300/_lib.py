@@ -88,6 +88,7 @@ SIGNATURES = {
     "fp8_check_device_status": (S, [P]),
     "fp8_inject_launch_failures": (S, [I32]),
     "fp8_selftest_wait_timeout": (S, [U32, P]),
+    "fp8_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "fp8_last_error": (ctypes.c_char_p, []),
     "fp8_version": (ctypes.c_char_p, []),
 }

@@ -8,12 +8,14 @@
 #include <cstdio>
 #include <cstring>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace fp8 {
 
-extern uint64_t g_wait_limit_ns;
+extern std::atomic<uint64_t> g_wait_limit_ns;
 
 namespace {
 
@@ -282,6 +284,9 @@ fp8_status fp8_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t c
     if (rows < 0 || cols < 0 || rows > 0x7FFFFFFF || cols > 0x7FFFFFFF)
         return fail(FP8_ERR_SHAPE, "%s: bad shape [%lld, %lld]", who, (long long)rows,
                     (long long)cols);
+    if (!fused_tiles_fit(rows, cols))
+        return fail(FP8_ERR_SHAPE, "%s: [%lld, %lld] has more 128x128 tiles than 2^31 - 1", who,
+                    (long long)rows, (long long)cols);
     FP8_TRY(check_dim16(who, "rows", rows, 16));
     FP8_TRY(check_dim16(who, "cols", cols, 16));
     if (rows * cols > 0) {
@@ -309,6 +314,9 @@ fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, i
     if (rows < 0 || cols < 0 || rows > 0x7FFFFFFF || cols > 0x7FFFFFFF)
         return fail(FP8_ERR_SHAPE, "%s: bad shape [%lld, %lld]", who, (long long)rows,
                     (long long)cols);
+    if (!fused_tiles_fit(rows, cols))
+        return fail(FP8_ERR_SHAPE, "%s: [%lld, %lld] has more 128x128 tiles than 2^31 - 1", who,
+                    (long long)rows, (long long)cols);
     FP8_TRY(check_dim16(who, "rows", rows, 16));
     FP8_TRY(check_dim16(who, "cols", cols, 16));
     if (rows * cols > 0) {
@@ -325,8 +333,6 @@ fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, i
     const char *why = nullptr;
     cudaError_t e = launch_quantize_fused_dynamic_noalloc(x, rows, cols, scale, scale_inv, q, qt,
                                                           amax_out, s, &why);
-    if (e == cudaErrorInvalidValue && why != nullptr)
-        return fail(FP8_ERR_UNSUPPORTED, "%s: %s", who, why);
     return cuda_status(e, who, why);
 }
 
@@ -965,6 +971,11 @@ fp8_status fp8_check_device_status(cudaStream_t s) {
                 (v & kStatusTimeoutEpilogue) ? "epilogue " : "",
                 (v & kStatusTimeoutSelftest) ? "selftest " : "",
                 (v & kStatusTimeoutBarrier) ? "grid-barrier" : "");
+}
+
+uint64_t fp8_set_wait_limit_ns(uint64_t limit_ns) {
+    const uint64_t v = limit_ns == 0 ? kDefaultWaitLimitNs : limit_ns;
+    return g_wait_limit_ns.exchange(v, std::memory_order_relaxed);
 }
 
 fp8_status fp8_selftest_wait_timeout(uint32_t timeout_us, cudaStream_t s) {

@@ -23,6 +23,8 @@
 
 #include <cstdlib>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 
 namespace {
 
@@ -276,7 +278,7 @@ cudaError_t launch_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, 
                       const float *sa, const float *sb, const uint16_t *bias, uint16_t *D,
                       cudaStream_t s, const char **why) {
     using C = TileCfg<BN>;
-    static bool attr_done[64] = {};
+    static std::atomic<bool> attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
@@ -300,7 +302,7 @@ cudaError_t launch_bn(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, 
     args.bias = bias;
     args.d = D;
     args.ldd = N;
-    args.wait_limit_ns = g_wait_limit_ns;
+    args.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     args.status = device_status_word();
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = (int)(tiles < num_sms() ? tiles : num_sms());

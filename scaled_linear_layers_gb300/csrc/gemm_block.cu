@@ -30,13 +30,15 @@
 // streams half of B's bytes, with the same promotion work per SM.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
 
 namespace fp8 {
 
-extern uint64_t g_wait_limit_ns;
+extern std::atomic<uint64_t> g_wait_limit_ns;
 
 namespace {
 
@@ -676,6 +678,443 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Sixteen epilogue warps.  The 128 x 256 tile's fp32 accumulators (128 KB of
+// registers per SM) spread over four warps per SM sub-partition instead of
+// two, 64 per thread, so that while one warp waits on a TMEM load or a
+// barrier three others have promotion work to issue: with two warps the
+// epilogue left the FMA pipe, the issue slots and the tensor pipe all under
+// 55 % busy.  Warp w = 4..19 reads TMEM lanes 32*(w%4).. of columns
+// 64*((w-4)/4)..+63 as four-row fragments (16-lane loads, 16 columns per
+// load pair): thread t holds rows 8i + t/4 of its lane quarter and columns
+// 16c + 8j + 2(t%4), +1 (c < 4, j < 2).  Warp 2 stages each contraction
+// block's scales (this CTA's 128 A rows, and B's 256 rows or two tile
+// scales) into a shared-memory ring with cp.async, whose completion arrives
+// on the ring slot's barrier, running up to SC_SLOTS blocks ahead; the
+// epilogue reads them from there.  Registers: the first warpgroup (TMA, MMA,
+// scale stager, one idle warp) drops to REGS_LOW with setmaxnreg and the four
+// epilogue warpgroups rise to REGS_HIGH, 128 * REGS_LOW + 512 * REGS_HIGH =
+// 640 * 96, the launch's allocation.
+template <bool kPair> struct Shape16 {
+    static constexpr int BN = 256;
+    static constexpr int B_ROWS = kPair ? BN / 2 : BN;
+    static constexpr int A_STAGE = A_BLK, B_STAGE = B_ROWS * BK;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+    static constexpr int SC_SLOTS = 4;
+    static constexpr int SC_FLOATS = BM + BN;  // A rows, then B rows (or B's two tile scales)
+    static constexpr int SC_BYTES = SC_SLOTS * SC_FLOATS * 4;
+    static constexpr int STAGES_FIT = (int)((227 * 1024 - 1024 - SC_BYTES - 512) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr uint32_t IDESC = idesc_f8_f32(kPair ? 2 * BM : BM, BN);
+    static constexpr int EPI_WARPS = 16, EPI0 = 4;
+    static constexpr int THREADS = 32 * (EPI0 + EPI_WARPS);
+    static constexpr int REGS_LAUNCH = 96, REGS_LOW = 32, REGS_HIGH = 112;
+    static_assert(128 * REGS_LOW + (THREADS - 128) * REGS_HIGH <= THREADS * REGS_LAUNCH,
+                  "the register split fits the 640-thread launch's allocation");
+    static constexpr uint32_t TMEM_COLS = GSLOTS * BN;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + SC_BYTES + 512;
+    static_assert(STAGES >= 3, "TMA ring depth");
+    static_assert(SMEM <= 227 * 1024, "smem");
+    static_assert(TMEM_COLS == 512, "two 256-column slots");
+};
+
+template <bool kPerRowB, bool kPair>
+__device__ __forceinline__ void block16_body(const CUtensorMap &tma_a, const CUtensorMap &tma_b,
+                                             const BlockArgs &p) {
+    using S = Shape16<kPair>;
+    constexpr int STAGES = S::STAGES, A_STAGE = S::A_STAGE, B_STAGE = S::B_STAGE, BN = S::BN;
+    constexpr int SC = S::SC_SLOTS, SCF = S::SC_FLOATS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_STAGE;
+    float *sring = reinterpret_cast<float *>(smem + STAGES * S::STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sring + SC * SCF);
+    uint64_t *full = bars;                 // [STAGES] TMA -> MMA
+    uint64_t *empty = bars + STAGES;       // [STAGES] MMA -> TMA
+    uint64_t *sfull = bars + 2 * STAGES;   // [GSLOTS] MMA -> epilogue
+    uint64_t *sempty = sfull + GSLOTS;     // [GSLOTS] epilogue -> MMA (the leader's, in a pair)
+    uint64_t *scfull = sempty + GSLOTS;    // [SC] scale copies landed
+    uint64_t *scempty = scfull + SC;       // [SC] scale slot read by every epilogue warp
+    uint64_t *drain = scempty + SC;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    constexpr int TM = kPair ? 2 * BM : BM;
+    const int m_tiles = (p.M + TM - 1) / TM, n_tiles = (p.N + BN - 1) / BN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int nk = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < GSLOTS; ++s) {
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sempty[s], kPair ? 2 * S::EPI_WARPS : S::EPI_WARPS);
+        }
+        for (int s = 0; s < SC; ++s) {
+            mbar_init(&scfull[s], 32);  // one cp.async-completion arrive per stager lane
+            mbar_init(&scempty[s], S::EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+    }
+    if (warp == 1) {
+        if constexpr (kPair) {
+            tmem_alloc_pair(tmem_holder, S::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_holder, S::TMEM_COLS);
+            tmem_relinquish();
+        }
+    }
+    tc_fence_before();
+    if constexpr (kPair)
+        cluster_sync_all();
+    else
+        __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    pdl_wait_prior();
+    pdl_allow_next();
+
+    if (warp < S::EPI0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::REGS_LOW));
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = unit; tile < num_tiles && ok; tile += units) {
+                int tm, tn;
+                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+                const int arow = tm * TM + (int)rank * BM;
+                const int brow = tn * BN + (int)rank * S::B_ROWS;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded<true>(&empty[stage], phase ^ 1u, abort_flag,
+                                                 p.wait_limit_ns, kStatusTimeoutTma, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if constexpr (kPair) {
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (A_STAGE + B_STAGE));
+                        const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
+                        tma_load_2d_pair(sA + stage * A_STAGE, &tma_a, leader_full, kb * BK, arow);
+                        tma_load_2d_pair(sB + stage * B_STAGE, &tma_b, leader_full, kb * BK, brow);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], A_STAGE + B_STAGE);
+                        tma_load_2d(sA + stage * A_STAGE, &tma_a, &full[stage], kb * BK, arow);
+                        tma_load_2d(sB + stage * B_STAGE, &tma_b, &full[stage], kb * BK, brow);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && rank == 0) {
+                for (int s = 0; s < STAGES; ++s) {
+                    stage = stage == 0 ? STAGES - 1 : stage - 1;
+                    if (stage == STAGES - 1) phase ^= 1u;
+                    volatile int no_abort = 0;
+                    mbar_wait_bounded(&full[stage], phase, &no_abort, 10000000ull,
+                                      kStatusTimeoutTma, p.status);
+                }
+            }
+        } else if (warp == 1 && lane == 0 && rank == 0) {
+            // ------------------------------------------- MMA issuer (leader)
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t g = 0;
+            bool ok = true;
+            for (int tile = unit; tile < num_tiles && ok; tile += units) {
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const uint32_t gs = g % GSLOTS, gphase = (g / GSLOTS) & 1u;
+                    if (!mbar_wait_bounded<true>(&sempty[gs], gphase ^ 1u, abort_flag,
+                                                 p.wait_limit_ns, kStatusTimeoutMma, p.status) ||
+                        !mbar_wait_bounded<true>(&full[stage], phase, abort_flag, p.wait_limit_ns,
+                                                 kStatusTimeoutMma, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
+                    const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+                    const uint32_t d_tmem = tmem_base + gs * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k) {
+                        if constexpr (kPair)
+                            mma_f8_pair(d_tmem, smem_desc_sw128(a0 + 32 * k),
+                                        smem_desc_sw128(b0 + 32 * k), S::IDESC, k != 0);
+                        else
+                            mma_f8(d_tmem, smem_desc_sw128(a0 + 32 * k),
+                                   smem_desc_sw128(b0 + 32 * k), S::IDESC, k != 0);
+                    }
+                    if constexpr (kPair) {
+                        mma_commit_pair(&empty[stage], 0x3);
+                        mma_commit_pair(&sfull[gs], 0x3);
+                    } else {
+                        mma_commit(&empty[stage]);
+                        mma_commit(&sfull[gs]);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if constexpr (kPair)
+                mma_commit_pair(drain, 0x1);
+            else
+                mma_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(drain, 0, &no_abort, p.wait_limit_ns, kStatusTimeoutMma, p.status);
+        } else if (warp == 2) {
+            // ------------------------------------------------ scale stager
+            // lane l copies A rows l + 32i of this CTA's 128 and B rows
+            // l + 32i of the tile's 256 (per-row B) or, in lanes 0 and 1,
+            // the scale of the tile's first and second 128-row half of B
+            const BlockScales &sc = p.sc;
+            int slot = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = unit; tile < num_tiles && ok; tile += units) {
+                int tm, tn;
+                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+                const int r0 = tm * TM + (int)rank * BM, c0 = tn * BN;
+                const float *arow[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    arow[i] = sc.sa + (int64_t)min(r0 + lane + 32 * i, p.M - 1) * sc.sa_row;
+                for (int kb = 0; kb < nk; ++kb) {
+                    bool w = mbar_wait_bounded<true>(&scempty[slot], ph ^ 1u, abort_flag,
+                                                     p.wait_limit_ns, kStatusTimeoutEpilogue,
+                                                     p.status);
+                    if (!__all_sync(0xFFFFFFFFu, w)) {
+                        ok = false;
+                        break;
+                    }
+                    float *dst = sring + slot * SCF;
+                    const int64_t ka = (int64_t)kb * sc.sa_k, kbo = (int64_t)kb * sc.sb_k;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cp_async4(dst + lane + 32 * i, arow[i] + ka);
+                    if constexpr (kPerRowB) {
+#pragma unroll
+                        for (int i = 0; i < BN / 32; ++i) {
+                            const int col = min(c0 + lane + 32 * i, p.N - 1);
+                            cp_async4(dst + BM + lane + 32 * i, sc.sb + (int64_t)col * sc.sb_row + kbo);
+                        }
+                    } else if (lane < 2) {
+                        const int col = min(c0 + 128 * lane, p.N - 1);
+                        cp_async4(dst + BM + lane,
+                                  sc.sb + (int64_t)(col / sc.b_rows) * sc.sb_row + kbo);
+                    }
+                    cp_async_arrive_noinc(&scfull[slot]);
+                    if (++slot == SC) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            cp_async_wait_all();
+        }
+    } else {
+        // --------------------------------------------- epilogue (16 warps)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::REGS_HIGH));
+        const int quarter = warp & 3;
+        const int cg = (warp - S::EPI0) >> 2;  // columns 64*cg .. +63 of the tile
+        const int fr = lane >> 2, fc = lane & 3;
+        uint32_t g = 0;
+        int slot = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = unit; tile < num_tiles; tile += units) {
+            int tm, tn;
+            grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+            const int row0 = tm * TM + (int)rank * BM + quarter * 32 + fr;  // rows row0 + 8i
+            const int col0 = tn * BN + 64 * cg + 2 * fc;  // columns col0 + 16c + 8j, +1
+            uint64_t acc[4][8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = 0ull;
+            for (int kb = 0; kb < nk; ++kb, ++g) {
+                const uint32_t gs = g % GSLOTS, gphase = (g / GSLOTS) & 1u;
+                if (ok)
+                    ok = mbar_wait_bounded<true>(&scfull[slot], ph, abort_flag, p.wait_limit_ns,
+                                                 kStatusTimeoutEpilogue, p.status) &&
+                         mbar_wait_bounded<true>(&sfull[gs], gphase, abort_flag, p.wait_limit_ns,
+                                                 kStatusTimeoutEpilogue, p.status);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                const float *scs = sring + slot * SCF;
+                if (++slot == SC) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+                if (!ok) continue;  // outputs invalid; keep the loop shape
+                tc_fence_after();
+                uint64_t f2[4];  // per-row B: (sa, sa); per-tile B: (sa*sb, sa*sb)
+                float sbt = 1.f;
+                if constexpr (!kPerRowB) sbt = scs[BM + (cg >> 1)];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float a = scs[quarter * 32 + fr + 8 * i];
+                    const float f = kPerRowB ? a : a * sbt;
+                    f2[i] = pack2(f, f);
+                }
+                const float *sbc = scs + BM + 64 * cg + 2 * fc;
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + gs * BN +
+                                       (uint32_t)(64 * cg);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t ra[8], rb[8];
+                    tmem_ld_16x256b_x2(taddr + 16 * c, ra);
+                    tmem_ld_16x256b_x2(taddr + (16u << 16) + 16 * c, rb);
+                    tmem_ld_wait();
+                    tmem_regs_ready(ra);
+                    tmem_regs_ready(rb);
+                    if (c == 3) {  // the block's partial is in registers: hand the slot back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (kPair)
+                                mbar_arrive_cluster(mapa_shared(smem_u32(&sempty[gs]), 0));
+                            else
+                                mbar_arrive(&sempty[gs]);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        uint64_t m2[4];
+                        if constexpr (kPerRowB) {
+                            const float2 sbv = *reinterpret_cast<const float2 *>(sbc + 16 * c + 8 * j);
+                            const uint64_t sb2 = pack2(sbv.x, sbv.y);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) m2[i] = mul2(sb2, f2[i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) m2[i] = f2[i];
+                        }
+                        const int a = 2 * c + j;
+                        acc[0][a] = fma2(pack2(__uint_as_float(ra[4 * j]), __uint_as_float(ra[4 * j + 1])),
+                                         m2[0], acc[0][a]);
+                        acc[1][a] = fma2(pack2(__uint_as_float(ra[4 * j + 2]), __uint_as_float(ra[4 * j + 3])),
+                                         m2[1], acc[1][a]);
+                        acc[2][a] = fma2(pack2(__uint_as_float(rb[4 * j]), __uint_as_float(rb[4 * j + 1])),
+                                         m2[2], acc[2][a]);
+                        acc[3][a] = fma2(pack2(__uint_as_float(rb[4 * j + 2]), __uint_as_float(rb[4 * j + 3])),
+                                         m2[3], acc[3][a]);
+                    }
+                }
+                __syncwarp();  // every lane's reads of this slot's scales are done
+                if (lane == 0) mbar_arrive(&scempty[slot == 0 ? SC - 1 : slot - 1]);
+            }
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = row0 + 8 * i;
+                    if (row >= p.M) continue;
+                    uint16_t *drow = p.d + (int64_t)row * p.ldd;
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) {
+                        const int col = col0 + 16 * (a >> 1) + 8 * (a & 1);
+                        if (col < p.N) {
+                            float lo, hi;
+                            unpack2(acc[i][a], lo, hi);
+                            *reinterpret_cast<uint32_t *>(drow + col) = pack_bf16x2(lo, hi);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    if constexpr (kPair)
+        cluster_sync_all();
+    else
+        __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, S::TMEM_COLS);
+    }
+}
+
+template <bool kPerRowB>
+__global__ void __launch_bounds__(Shape16<false>::THREADS, 1)
+    gemm_f8_block16_kernel(const __grid_constant__ CUtensorMap tma_a,
+                           const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
+    block16_body<kPerRowB, false>(tma_a, tma_b, p);
+}
+
+template <bool kPerRowB>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape16<true>::THREADS, 1)
+    gemm_f8_block16_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
+                                const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
+    block16_body<kPerRowB, true>(tma_a, tma_b, p);
+}
+
+template <bool kPerRowB, bool kPair>
+cudaError_t launch_block16(const CUtensorMap &ta, const CUtensorMap &tb, const BlockArgs &args,
+                           int grid, cudaStream_t s, const char **why) {
+    using S = Shape16<kPair>;
+    auto kernel = kPair ? gemm_f8_block16_pair_kernel<kPerRowB> : gemm_f8_block16_kernel<kPerRowB>;
+    static std::atomic<bool> attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        // setmaxnreg.inc waits until the CTA's launch allocation can supply
+        // the raised counts: refuse a build whose register count at launch
+        // would leave it waiting
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        if ((int64_t)fa.numRegs * S::THREADS <
+            (int64_t)128 * S::REGS_LOW + (int64_t)(S::THREADS - 128) * S::REGS_HIGH) {
+            *why = "block GEMM: the register split does not fit the kernel's launch allocation";
+            return cudaErrorInvalidConfiguration;
+        }
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    return launch_pdl(kernel, grid, S::THREADS, S::SMEM, s, ta, tb, args);
+}
+
+template <bool kPair>
+cudaError_t launch_shape16(const uint8_t *A, const uint8_t *B, const BlockArgs &args,
+                           cudaStream_t s, const char **why) {
+    CUtensorMap ta, tb;
+    if (!make_tmap_k128(&ta, A, args.M, args.K, BM) ||
+        !make_tmap_k128(&tb, B, args.N, args.K, Shape16<kPair>::B_ROWS)) {
+        *why = "cuTensorMapEncodeTiled failed";
+        return cudaErrorInvalidValue;
+    }
+    const int64_t tm = kPair ? 2 * BM : BM;
+    const int64_t tiles = ((args.M + tm - 1) / tm) * ((args.N + 255) / 256);
+    const int64_t units = kPair ? num_sms() / 2 : num_sms();
+    const int grid = (int)(tiles < units ? tiles : units) * (kPair ? 2 : 1);
+    if (args.sc.b_rows == 1) return launch_block16<true, kPair>(ta, tb, args, grid, s, why);
+    if (args.sc.b_rows == 128) return launch_block16<false, kPair>(ta, tb, args, grid, s, why);
+    *why = "B scales must be per row or per 128-row tile";
+    return cudaErrorInvalidValue;
+}
+
 template <bool kPerRowB, int kBN>
 __global__ void __launch_bounds__(Shape<false, kBN>::THREADS, 1)
     gemm_f8_block_kernel(const __grid_constant__ CUtensorMap tma_a,
@@ -697,7 +1136,7 @@ cudaError_t launch_block(const CUtensorMap &ta, const CUtensorMap &tb, const Blo
     auto kernel = kPair ? gemm_f8_block_pair_kernel<kPerRowB, kBN>
                         : gemm_f8_block_kernel<kPerRowB, kBN>;
     constexpr size_t smem = S::SMEM;
-    static bool attr_done[64] = {};
+    static std::atomic<bool> attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
@@ -761,13 +1200,18 @@ cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int
     args.sc = sc;
     args.d = D;
     args.ldd = N;
-    args.wait_limit_ns = g_wait_limit_ns;
+    args.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     args.status = device_status_word();
     const char *pe = getenv("FP8LINEAR_BLOCK_PAIR");
     const char *be = getenv("FP8LINEAR_BLOCK_BN");
+    const char *ee = getenv("FP8LINEAR_BLOCK_EPI");
     const bool wide = be != nullptr ? atoi(be) == 256
                                     : ((M + 127) / 128) * ((N + 255) / 256) >= num_sms();
     const bool pair = pe != nullptr && atoi(pe) == 1;
+    const bool epi16 = ee != nullptr && atoi(ee) == 16;
+    if (wide && epi16)
+        return pair ? launch_shape16<true>(A, B, args, s, why)
+                    : launch_shape16<false>(A, B, args, s, why);
     if (wide)
         return pair ? launch_shape<true, 256>(A, B, args, s, why)
                     : launch_shape<false, 256>(A, B, args, s, why);

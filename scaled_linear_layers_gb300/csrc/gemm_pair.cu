@@ -22,13 +22,15 @@
 // CTAs of a pair meet at cluster barriers after set-up and before teardown.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
 
 namespace fp8 {
 
-extern uint64_t g_wait_limit_ns;
+extern std::atomic<uint64_t> g_wait_limit_ns;
 
 namespace {
 
@@ -312,7 +314,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 template <int BN>
 cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char **why) {
     using C = PairCfg<BN>;
-    static bool attr_done[64] = {};
+    static std::atomic<bool> attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
@@ -346,7 +348,7 @@ cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char 
         pr.tiles = i < n ? pr.m_tiles * pr.n_tiles : 0;
         tiles += pr.tiles;
     }
-    args.wait_limit_ns = g_wait_limit_ns;
+    args.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     args.status = device_status_word();
     const int64_t pairs = num_sms() / 2;
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);

@@ -82,6 +82,9 @@ cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const floa
 cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols,
                                           float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
                                           float *amax_out, unsigned int *workspace, cudaStream_t s);
+// The fused kernel indexes 128x128 tiles with 32-bit ints: false when a
+// [rows, cols] tensor has more tiles than that.
+bool fused_tiles_fit(int64_t rows, int64_t cols);
 // The same with a static scratch array instead of a workspace (no allocation).
 cudaError_t launch_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, int64_t cols,
                                                   float *scale, float *scale_inv, uint8_t *q,

@@ -7,13 +7,15 @@
 // the tile still in registers, then its other tiles in reverse order, so the
 // re-reads hit the L2 (129 MB) whenever the tensor fits there.  The barrier
 // and the per-CTA partial amaxes live in a small caller-owned workspace.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "qtile.cuh"
 
 namespace fp8 {
 
-extern uint64_t g_wait_limit_ns;
+extern std::atomic<uint64_t> g_wait_limit_ns;
 
 namespace {
 
@@ -127,35 +129,57 @@ static __device__ __align__(256) unsigned int g_noalloc_scratch[kWsHeader + kSta
 
 }  // namespace
 
-cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols,
-                                          float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
-                                          float *amax_out, unsigned int *workspace,
-                                          cudaStream_t s) {
-    static int occ_cache[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int occ = (dev >= 0 && dev < 64) ? occ_cache[dev] : 0;
-    if (occ == 0) {
+// Resident CTAs per SM of the fused kernel on device `dev`, looked up once per
+// device.  Host threads may race on the first lookup; they store the same
+// value, and the atomic makes the race well defined.
+static cudaError_t fused_occupancy(int dev, int *occ) {
+    static std::atomic<int> cache[64];
+    int v = (dev >= 0 && dev < 64) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (v == 0) {
         cudaError_t e =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_fused_dynamic_kernel, 256, 0);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, quantize_fused_dynamic_kernel, 256, 0);
         if (e != cudaSuccess) return e;
-        if (occ < 1) return cudaErrorInvalidConfiguration;
-        if (dev >= 0 && dev < 64) occ_cache[dev] = occ;
+        if (v < 1) return cudaErrorInvalidConfiguration;
+        if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
     }
+    *occ = v;
+    return cudaSuccess;
+}
+
+static FusedArgs fused_args(const uint16_t *x, int64_t rows, int64_t cols, float *scale,
+                            float *scale_inv, uint8_t *q, uint8_t *qt, float *amax_out,
+                            unsigned int *ws) {
     FusedArgs a;
     a.x = x;
     a.R = (int)rows;
     a.C = (int)cols;
     a.tiles_x = (int)((cols + 127) / 128);
-    a.tiles = rows * cols == 0 ? 0 : a.tiles_x * (int)((rows + 127) / 128);
+    a.tiles = rows * cols == 0 ? 0 : (int)(a.tiles_x * ((rows + 127) / 128));
     a.scale = scale;
     a.scale_inv = scale_inv;
     a.amax_out = amax_out;
     a.q = q;
     a.qt = qt;
-    a.ws = workspace;
-    a.wait_limit_ns = g_wait_limit_ns;
+    a.ws = ws;
+    a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     a.status = device_status_word();
+    return a;
+}
+
+bool fused_tiles_fit(int64_t rows, int64_t cols) {
+    return ((cols + 127) / 128) * ((rows + 127) / 128) <= 0x7FFFFFFF;
+}
+
+cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64_t cols,
+                                          float *scale, float *scale_inv, uint8_t *q, uint8_t *qt,
+                                          float *amax_out, unsigned int *workspace,
+                                          cudaStream_t s) {
+    int dev = 0, occ = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = fused_occupancy(dev, &occ);
+    if (e != cudaSuccess) return e;
+    FusedArgs a = fused_args(x, rows, cols, scale, scale_inv, q, qt, amax_out, workspace);
     int64_t grid = (int64_t)num_sms() * occ;
     if (grid > a.tiles) grid = a.tiles;
     if (grid > kMaxGrid) grid = kMaxGrid;
@@ -168,60 +192,42 @@ cudaError_t launch_quantize_fused_dynamic(const uint16_t *x, int64_t rows, int64
 // The same kernel with its scratch in g_noalloc_scratch instead of a caller
 // workspace.  In host code the array's name is only a stand-in for the device
 // object, so its device address is looked up with cudaGetSymbolAddress once
-// per device (with that device current) on the first call there.  Returns
-// cudaErrorInvalidValue with *why set when the grid this GPU would run needs
-// more partial slots than the array holds.
+// per device (with that device current) on the first call there.  The grid is
+// clamped to the array's kStaticMaxGrid partial slots (CTAs walk their tiles
+// with a grid stride, so fewer CTAs than the GPU could hold give the same
+// result), so no tensor size needs more scratch than the array has.
 cudaError_t launch_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, int64_t cols,
                                                   float *scale, float *scale_inv, uint8_t *q,
                                                   uint8_t *qt, float *amax_out, cudaStream_t s,
                                                   const char **why) {
-    static unsigned int *scratch_addr[64] = {};
-    static int occ_cache[64] = {};
-    int dev = 0;
+    // per-device address of the array; host threads that race on a device's
+    // first call store the same address
+    static std::atomic<unsigned int *> scratch_addr[64];
+    int dev = 0, occ = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) {
         *why = "device index out of range";
         return cudaErrorInvalidDevice;
     }
-    if (scratch_addr[dev] == nullptr) {
+    unsigned int *ws = scratch_addr[dev].load(std::memory_order_acquire);
+    if (ws == nullptr) {
         void *ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess) {
             *why = "cudaGetSymbolAddress of the static scratch failed";
             return e;
         }
-        scratch_addr[dev] = static_cast<unsigned int *>(ptr);
+        ws = static_cast<unsigned int *>(ptr);
+        scratch_addr[dev].store(ws, std::memory_order_release);
     }
-    if (occ_cache[dev] == 0) {
-        int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_fused_dynamic_kernel, 256, 0);
-        if (e != cudaSuccess) return e;
-        if (occ < 1) return cudaErrorInvalidConfiguration;
-        occ_cache[dev] = occ;
-    }
-    FusedArgs a;
-    a.x = x;
-    a.R = (int)rows;
-    a.C = (int)cols;
-    a.tiles_x = (int)((cols + 127) / 128);
-    a.tiles = rows * cols == 0 ? 0 : a.tiles_x * (int)((rows + 127) / 128);
-    a.scale = scale;
-    a.scale_inv = scale_inv;
-    a.amax_out = amax_out;
-    a.q = q;
-    a.qt = qt;
-    a.ws = scratch_addr[dev];
-    a.wait_limit_ns = g_wait_limit_ns;
-    a.status = device_status_word();
-    int64_t grid = (int64_t)num_sms() * occ_cache[dev];
+    e = fused_occupancy(dev, &occ);
+    if (e != cudaSuccess) return e;
+    FusedArgs a = fused_args(x, rows, cols, scale, scale_inv, q, qt, amax_out, ws);
+    int64_t grid = (int64_t)num_sms() * occ;
     if (grid > a.tiles) grid = a.tiles;
+    if (grid > kStaticMaxGrid) grid = kStaticMaxGrid;
     if (grid < 1) grid = 1;
-    if (grid > kStaticMaxGrid) {
-        *why = "this GPU's persistent grid needs more partial slots than the static scratch "
-               "holds (1008)";
-        return cudaErrorInvalidValue;
-    }
     // the arrival count must start at zero; a previous call that timed out
     // may have left it otherwise (a memset, not an allocation)
     e = cudaMemsetAsync(a.ws, 0, 2 * sizeof(unsigned int), s);

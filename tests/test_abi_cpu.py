@@ -321,3 +321,20 @@ def test_quantize_transpose_block_needs_column_scales(lib):
     assert f(OK_P, 256, 256, 2, OK_P, OK_P, OK_P, OK_P, None, OK_P, None, None) == 1
     assert f(OK_P, 256, 256, 2, None, None, OK_P, OK_P, OK_P, OK_P, None, None) == 1
     assert f(OK_P, 256, 256, 9, OK_P, OK_P, OK_P, OK_P, OK_P, OK_P, None, None) == 2
+
+
+def test_wait_limit_setter_returns_the_previous_limit(lib):
+    default = 2_000_000_000
+    prev = lib.fp8_set_wait_limit_ns(5000)
+    assert prev == default
+    assert lib.fp8_set_wait_limit_ns(0) == 5000       # 0 restores the default
+    assert lib.fp8_set_wait_limit_ns(default) == default
+
+
+def test_fused_dynamic_rejects_more_tiles_than_int32(lib):
+    p = ctypes.c_void_p(0x1000)
+    rows = cols = 1 << 24   # 2^34 tiles of 128 x 128
+    for fn in (lib.fp8_quantize_fused_dynamic_noalloc,):
+        assert fn(p, rows, cols, p, p, p, None, p, None) == 2   # FP8_ERR_SHAPE
+    assert lib.fp8_quantize_fused_dynamic(p, rows, cols, p, p, p, None, p, p, None) == 2
+    assert "tiles" in lib.fp8_last_error().decode()
