@@ -194,9 +194,11 @@ fp8_status fp8_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t rows, i
  * Kernel choice is automatic.  For tests and tuning, environment variables
  * read at each call override it: FP8LINEAR_GEMM_PAIR=0/1 (tensorwise: one-CTA
  * or 2-SM pair kernel), FP8LINEAR_GEMM_BN=256/224/192/160/128 (tensorwise N
- * tile), FP8LINEAR_BLOCK_PAIR=0/1 and FP8LINEAR_BLOCK_BN=128/256 (block
- * recipe: one CTA or a CTA pair, tile width).  Every setting computes the same
- * products; the tests run each against the oracle.
+ * tile), FP8LINEAR_BLOCK_PAIR=0/1, FP8LINEAR_BLOCK_BN=128/256,
+ * FP8LINEAR_BLOCK_ACC=0/1 (block recipe: one CTA or a CTA pair, tile width,
+ * packed or scalar fp32 accumulators) and FP8LINEAR_BLOCK_GROUP=<row tiles>
+ * (block recipe raster).  Every setting computes the same products in the
+ * same order; the tests run each against the oracle.
  * Source: AstrAI fp8_state.py, the comment above FP8TensorMeta (the product
  * is scaled by A's and B's scales) and fp8_linear_forward /
  * fp8_linear_backward. */

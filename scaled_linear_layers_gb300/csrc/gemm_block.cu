@@ -31,6 +31,7 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -45,11 +46,7 @@ namespace {
 constexpr int BM = 128, BK = 128;
 constexpr int GSLOTS = 2;  // group slots of KG TMEM slots each
 constexpr int A_BLK = BM * BK;
-#ifndef FP8_BLOCK_EPI_WARPS
-#define FP8_BLOCK_EPI_WARPS 8
-#endif
-constexpr int EPI_WARPS = FP8_BLOCK_EPI_WARPS;  // 8 or 16
-constexpr int GROUP_M = 8;
+constexpr int EPI_WARPS = 8;
 // Scales are fetched PD groups ahead of their use.  One group (about 0.7 us
 // at the block workload's speed) measured best: deeper prefetch costs
 // registers the promotion needs (32768 x 8192 x 8192, PD 1/2/3: fprop 1828 /
@@ -105,7 +102,7 @@ template <bool kPair, int kBN> struct Shape {
     static constexpr int EPI0 = SPLIT_REGS ? 4 : 2;  // first epilogue warp
     static constexpr int THREADS = 32 * (EPI0 + EPI_WARPS);
     static constexpr int REGS_LOW = 40, REGS_HIGH = 232;
-    static_assert(!SPLIT_REGS || (EPI_WARPS == 8 && 128 * REGS_LOW + 256 * REGS_HIGH <= 384 * 168),
+    static_assert(!SPLIT_REGS || 128 * REGS_LOW + 256 * REGS_HIGH <= 384 * 168,
                   "the register split fits the 384-thread launch's allocation");
     // per-warp B-row scales: [PD + 1 groups in flight][KG blocks][COLS]
     static constexpr int SBUF_FLOATS = EPI_WARPS * (PD + 1) * KG * COLS;
@@ -123,6 +120,7 @@ struct BlockArgs {
     BlockScales sc;
     uint16_t *d;
     int64_t ldd;
+    int group_m;  // row tiles per raster group (block_raster_group)
     uint64_t wait_limit_ns;
     unsigned int *status;
 };
@@ -151,9 +149,42 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-template <bool kPerRowB, bool kPair, int kBN>
+// A pair of fp32 accumulators, kept either packed in one 64-bit register
+// (folded in with one fma.rn.f32x2, whose first operand, two TMEM values,
+// must first be moved into an aligned register pair) or as two scalars
+// (folded in with two fma.rn on the TMEM registers as they are).  Both do the
+// same two IEEE fmas, so the results are identical.
+struct F2 {
+    float x, y;
+};
+
+__device__ __forceinline__ void acc_zero(uint64_t &a) { a = 0ull; }
+__device__ __forceinline__ void acc_zero(F2 &a) { a.x = a.y = 0.f; }
+
+// a += (p0, p1) * f2, lane by lane
+__device__ __forceinline__ void acc_fma(uint64_t &a, uint32_t p0, uint32_t p1, uint64_t f2) {
+    uint64_t pv;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pv) : "r"(p0), "r"(p1));
+    a = fma2(pv, f2, a);
+}
+__device__ __forceinline__ void acc_fma(F2 &a, uint32_t p0, uint32_t p1, uint64_t f2) {
+    float f0, f1;
+    unpack2(f2, f0, f1);
+    a.x = __fmaf_rn(__uint_as_float(p0), f0, a.x);
+    a.y = __fmaf_rn(__uint_as_float(p1), f1, a.y);
+}
+
+__device__ __forceinline__ uint32_t acc_bf16x2(uint64_t a) {
+    float lo, hi;
+    unpack2(a, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
+__device__ __forceinline__ uint32_t acc_bf16x2(const F2 &a) { return pack_bf16x2(a.x, a.y); }
+
+template <bool kPerRowB, bool kPair, int kBN, bool kScalar = false>
 __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const CUtensorMap &tma_b,
                                                 const BlockArgs &p) {
+    using AccT = typename std::conditional<kScalar, F2, uint64_t>::type;
     using S = Shape<kPair, kBN>;
     constexpr int STAGES = S::STAGES, A_STAGE = S::A_STAGE, B_STAGE = S::B_STAGE;
     constexpr int B_BLK = S::B_BLK, BN = S::BN, KG = S::KG, COLS = S::COLS, CH = S::CH;
@@ -236,7 +267,7 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
             bool ok = true;
             for (int tile = unit; tile < num_tiles && ok; tile += units) {
                 int tm, tn;
-                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+                grouped_tile(tile, m_tiles, n_tiles, p.group_m, tm, tn);
                 const int arow = tm * TM + (int)rank * BM;
                 const int brow = tn * BN + (int)rank * S::B_ROWS;
                 for (int q = 0; q < ngroups; ++q) {
@@ -359,7 +390,7 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
             const int fr = lane >> 2, fc = lane & 3;
             for (int tile = unit; tile < num_tiles; tile += units) {
                 int tm, tn;
-                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+                grouped_tile(tile, m_tiles, n_tiles, p.group_m, tm, tn);
                 const int row0 = tm * TM + (int)rank * BM + quarter * 32 + fr;
                 const int j0 = tn * BN + group * COLS;
                 const float *sa_rows[4];
@@ -368,11 +399,11 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                     sa_rows[i] = sc.sa + (int64_t)min(row0 + 8 * i, p.M - 1) * sc.sa_row;
                 const float *sb_ptr =
                     sc.sb + (int64_t)min(j0 + PER_LANE * lane, p.N - PER_LANE) * sc.sb_row;
-                uint64_t acc[4][COLS / 8];
+                AccT acc[4][COLS / 8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < COLS / 8; ++j) acc[i][j] = 0ull;
+                    for (int j = 0; j < COLS / 8; ++j) acc_zero(acc[i][j]);
                 float sa_pf[PD][4];
                 auto fetch = [&](int qn, float (&sa)[4]) {
                     const int kb = min(qn, nk - 1);
@@ -415,7 +446,6 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                     const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                            gs * BN + (uint32_t)(group * COLS);
                     const float *buf = wbuf + (q % (PD + 1)) * COLS + 2 * fc;
-                    constexpr int NC = COLS / 32;
                     auto hand_back = [&] {  // the block's partial is in registers
                         tc_fence_before();
                         __syncwarp();
@@ -428,11 +458,23 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                     };
                     // chunk c's lanes +0..15 / +16..31 of the quarter in
                     // ra / rb [c % 2]; with FP8_BLOCK_PIPE the load of chunk
-                    // c + 1 is in flight while chunk c is folded in
-                    uint32_t ra[2][16], rb[2][16];
+                    // c + 1 is in flight while chunk c is folded in.  Scalar
+                    // accumulators take 16-column chunks (8 registers per
+                    // load instead of 16), which keeps the per-thread total
+                    // of 128 accumulators plus the two chunks in flight
+                    // within the 232 registers of the epilogue warps.
+                    constexpr int CW = kScalar ? 16 : 32;  // columns per chunk
+                    constexpr int NC = COLS / CW, JJ = CW / 8, R = CW / 2;
+                    auto ld = [&](uint32_t addr, uint32_t(&r)[R]) {
+                        if constexpr (R == 8)
+                            tmem_ld_16x256b_x2(addr, r);
+                        else
+                            tmem_ld_16x256b_x4(addr, r);
+                    };
+                    uint32_t ra[2][R], rb[2][R];
                     if (FP8_BLOCK_PIPE) {
-                        tmem_ld_16x256b_x4(taddr, ra[0]);
-                        tmem_ld_16x256b_x4(taddr + (16u << 16), rb[0]);
+                        ld(taddr, ra[0]);
+                        ld(taddr + (16u << 16), rb[0]);
                         tmem_ld_wait();
                         tmem_regs_ready(ra[0]);
                         tmem_regs_ready(rb[0]);
@@ -440,32 +482,28 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                     }
 #pragma unroll
                     for (int c0 = 0; c0 < NC; ++c0) {
-                        uint32_t(&r0)[16] = ra[c0 & 1];
-                        uint32_t(&r1)[16] = rb[c0 & 1];
+                        uint32_t(&r0)[R] = ra[c0 & 1];
+                        uint32_t(&r1)[R] = rb[c0 & 1];
                         if (!FP8_BLOCK_PIPE) {
-                            tmem_ld_16x256b_x4(taddr + 32 * c0, r0);
-                            tmem_ld_16x256b_x4(taddr + (16u << 16) + 32 * c0, r1);
+                            ld(taddr + CW * c0, r0);
+                            ld(taddr + (16u << 16) + CW * c0, r1);
                             tmem_ld_wait();
                             tmem_regs_ready(r0);
                             tmem_regs_ready(r1);
                             if (c0 + 1 == NC) hand_back();
                         } else if (c0 + 1 < NC) {
-                            tmem_ld_16x256b_x4(taddr + 32 * (c0 + 1), ra[(c0 + 1) & 1]);
-                            tmem_ld_16x256b_x4(taddr + (16u << 16) + 32 * (c0 + 1), rb[(c0 + 1) & 1]);
+                            ld(taddr + CW * (c0 + 1), ra[(c0 + 1) & 1]);
+                            ld(taddr + (16u << 16) + CW * (c0 + 1), rb[(c0 + 1) & 1]);
                         }
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            const int j = 4 * c0 + jj;
+                        for (int jj = 0; jj < JJ; ++jj) {
+                            const int j = JJ * c0 + jj;
                             const float2 sbv = *reinterpret_cast<const float2 *>(buf + 8 * j);
                             const uint64_t sb2 = pack2(sbv.x, sbv.y);
-                            acc[0][j] = fma2(pack2(__uint_as_float(r0[4 * jj]), __uint_as_float(r0[4 * jj + 1])),
-                                             mul2(sb2, sa2[0]), acc[0][j]);
-                            acc[1][j] = fma2(pack2(__uint_as_float(r0[4 * jj + 2]), __uint_as_float(r0[4 * jj + 3])),
-                                             mul2(sb2, sa2[1]), acc[1][j]);
-                            acc[2][j] = fma2(pack2(__uint_as_float(r1[4 * jj]), __uint_as_float(r1[4 * jj + 1])),
-                                             mul2(sb2, sa2[2]), acc[2][j]);
-                            acc[3][j] = fma2(pack2(__uint_as_float(r1[4 * jj + 2]), __uint_as_float(r1[4 * jj + 3])),
-                                             mul2(sb2, sa2[3]), acc[3][j]);
+                            acc_fma(acc[0][j], r0[4 * jj], r0[4 * jj + 1], mul2(sb2, sa2[0]));
+                            acc_fma(acc[1][j], r0[4 * jj + 2], r0[4 * jj + 3], mul2(sb2, sa2[1]));
+                            acc_fma(acc[2][j], r1[4 * jj], r1[4 * jj + 1], mul2(sb2, sa2[2]));
+                            acc_fma(acc[3][j], r1[4 * jj + 2], r1[4 * jj + 3], mul2(sb2, sa2[3]));
                         }
                         if (FP8_BLOCK_PIPE && c0 + 1 < NC) {
                             tmem_ld_wait();
@@ -482,18 +520,14 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                         if (row >= p.M) continue;
                         uint32_t *dst = reinterpret_cast<uint32_t *>(p.d + (int64_t)row * p.ldd + j0 + 2 * fc);
 #pragma unroll
-                        for (int j = 0; j < COLS / 8; ++j) {
-                            float lo, hi;
-                            unpack2(acc[i][j], lo, hi);
-                            dst[4 * j] = pack_bf16x2(lo, hi);
-                        }
+                        for (int j = 0; j < COLS / 8; ++j) dst[4 * j] = acc_bf16x2(acc[i][j]);
                     }
                 }
             }
         } else {
         for (int tile = unit; tile < num_tiles; tile += units) {
             int tm, tn;
-            grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
+            grouped_tile(tile, m_tiles, n_tiles, p.group_m, tm, tn);
             const int row = tm * TM + (int)rank * BM + quarter * 32 + lane;
             const int j0 = tn * BN + group * COLS;  // first output column of this thread
             const float *sa_row = sc.sa + (int64_t)min(row, p.M - 1) * sc.sa_row;
@@ -507,10 +541,10 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
             // pair), single for per-row B (a multiply and an FMA per element
             // measured faster there than their packed forms: 1356 against
             // 1297 TFLOP/s for wgrad at 32768 x 8192 x 8192)
-            uint64_t acc[COLS / 2];
+            AccT acc[COLS / 2];
             float accs[COLS];
 #pragma unroll
-            for (int j = 0; j < COLS / 2; ++j) acc[j] = 0ull;
+            for (int j = 0; j < COLS / 2; ++j) acc_zero(acc[j]);
 #pragma unroll
             for (int j = 0; j < COLS; ++j) accs[j] = 0.f;
             // scalar scales of the next PD groups (contraction blocks past the
@@ -623,12 +657,9 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                             }
                         } else {
 #pragma unroll
-                            for (int a = 0; a < 16 * CH; ++a) {
-                                const uint64_t pv =
-                                    pack2(__uint_as_float(r[a / 16][(2 * a) % 32]),
-                                          __uint_as_float(r[a / 16][(2 * a) % 32 + 1]));
-                                acc[16 * c0 + a] = fma2(pv, fts, acc[16 * c0 + a]);
-                            }
+                            for (int a = 0; a < 16 * CH; ++a)
+                                acc_fma(acc[16 * c0 + a], r[a / 16][(2 * a) % 32],
+                                        r[a / 16][(2 * a) % 32 + 1], fts);
                         }
                         if constexpr (kPipe) {
                             if (c0 + 1 < NC) {
@@ -644,18 +675,15 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
                 uint4 *dst = reinterpret_cast<uint4 *>(p.d + (int64_t)row * p.ldd + j0);
 #pragma unroll
                 for (int c = 0; c < COLS / 8; ++c) {
-                    float v[8];
+                    uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        if constexpr (kPerRowB) {
-                            v[2 * e] = accs[8 * c + 2 * e];
-                            v[2 * e + 1] = accs[8 * c + 2 * e + 1];
-                        } else {
-                            unpack2(acc[4 * c + e], v[2 * e], v[2 * e + 1]);
-                        }
+                        if constexpr (kPerRowB)
+                            w[e] = pack_bf16x2(accs[8 * c + 2 * e], accs[8 * c + 2 * e + 1]);
+                        else
+                            w[e] = acc_bf16x2(acc[4 * c + e]);
                     }
-                    dst[c] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                        pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                    dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
         }
@@ -678,463 +706,26 @@ __device__ __forceinline__ void block_gemm_body(const CUtensorMap &tma_a, const 
     }
 }
 
-// ---------------------------------------------------------------------------
-// Sixteen epilogue warps.  The 128 x 256 tile's fp32 accumulators (128 KB of
-// registers per SM) spread over four warps per SM sub-partition instead of
-// two, 64 per thread, so that while one warp waits on a TMEM load or a
-// barrier three others have promotion work to issue: with two warps the
-// epilogue left the FMA pipe, the issue slots and the tensor pipe all under
-// 55 % busy.  Warp w = 4..19 reads TMEM lanes 32*(w%4).. of columns
-// 64*((w-4)/4)..+63 as four-row fragments (16-lane loads, 16 columns per
-// load pair): thread t holds rows 8i + t/4 of its lane quarter and columns
-// 16c + 8j + 2(t%4), +1 (c < 4, j < 2).  Warp 2 stages each contraction
-// block's scales (this CTA's 128 A rows, and B's 256 rows or two tile
-// scales) into a shared-memory ring with cp.async, whose completion arrives
-// on the ring slot's barrier, running up to SC_SLOTS blocks ahead; the
-// epilogue reads them from there.  Registers: the first warpgroup (TMA, MMA,
-// scale stager, one idle warp) drops to REGS_LOW with setmaxnreg and the four
-// epilogue warpgroups rise to REGS_HIGH, 128 * REGS_LOW + 512 * REGS_HIGH =
-// 640 * 96, the launch's allocation.
-template <bool kPair> struct Shape16 {
-    static constexpr int BN = 256;
-    static constexpr int B_ROWS = kPair ? BN / 2 : BN;
-    static constexpr int A_STAGE = A_BLK, B_STAGE = B_ROWS * BK;
-    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int SC_SLOTS = 4;
-    static constexpr int SC_FLOATS = BM + BN;  // A rows, then B rows (or B's two tile scales)
-    static constexpr int SC_BYTES = SC_SLOTS * SC_FLOATS * 4;
-    static constexpr int STAGES_FIT = (int)((227 * 1024 - 1024 - SC_BYTES - 512) / STAGE_BYTES);
-    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-    static constexpr uint32_t IDESC = idesc_f8_f32(kPair ? 2 * BM : BM, BN);
-    static constexpr int EPI_WARPS = 16, EPI0 = 4;
-    static constexpr int THREADS = 32 * (EPI0 + EPI_WARPS);
-    static constexpr int REGS_LAUNCH = 96, REGS_LOW = 32, REGS_HIGH = 112;
-    static_assert(128 * REGS_LOW + (THREADS - 128) * REGS_HIGH <= THREADS * REGS_LAUNCH,
-                  "the register split fits the 640-thread launch's allocation");
-    static constexpr uint32_t TMEM_COLS = GSLOTS * BN;
-    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + SC_BYTES + 512;
-    static_assert(STAGES >= 3, "TMA ring depth");
-    static_assert(SMEM <= 227 * 1024, "smem");
-    static_assert(TMEM_COLS == 512, "two 256-column slots");
-};
-
-template <bool kPerRowB, bool kPair>
-__device__ __forceinline__ void block16_body(const CUtensorMap &tma_a, const CUtensorMap &tma_b,
-                                             const BlockArgs &p) {
-    using S = Shape16<kPair>;
-    constexpr int STAGES = S::STAGES, A_STAGE = S::A_STAGE, B_STAGE = S::B_STAGE, BN = S::BN;
-    constexpr int SC = S::SC_SLOTS, SCF = S::SC_FLOATS;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * A_STAGE;
-    float *sring = reinterpret_cast<float *>(smem + STAGES * S::STAGE_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sring + SC * SCF);
-    uint64_t *full = bars;                 // [STAGES] TMA -> MMA
-    uint64_t *empty = bars + STAGES;       // [STAGES] MMA -> TMA
-    uint64_t *sfull = bars + 2 * STAGES;   // [GSLOTS] MMA -> epilogue
-    uint64_t *sempty = sfull + GSLOTS;     // [GSLOTS] epilogue -> MMA (the leader's, in a pair)
-    uint64_t *scfull = sempty + GSLOTS;    // [SC] scale copies landed
-    uint64_t *scempty = scfull + SC;       // [SC] scale slot read by every epilogue warp
-    uint64_t *drain = scempty + SC;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-    const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    constexpr int TM = kPair ? 2 * BM : BM;
-    const int m_tiles = (p.M + TM - 1) / TM, n_tiles = (p.N + BN - 1) / BN;
-    const int num_tiles = m_tiles * n_tiles;
-    const int nk = (p.K + BK - 1) / BK;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int s = 0; s < GSLOTS; ++s) {
-            mbar_init(&sfull[s], 1);
-            mbar_init(&sempty[s], kPair ? 2 * S::EPI_WARPS : S::EPI_WARPS);
-        }
-        for (int s = 0; s < SC; ++s) {
-            mbar_init(&scfull[s], 32);  // one cp.async-completion arrive per stager lane
-            mbar_init(&scempty[s], S::EPI_WARPS);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_mbarrier_init();
-        tma_prefetch_desc(&tma_a);
-        tma_prefetch_desc(&tma_b);
-    }
-    if (warp == 1) {
-        if constexpr (kPair) {
-            tmem_alloc_pair(tmem_holder, S::TMEM_COLS);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(tmem_holder, S::TMEM_COLS);
-            tmem_relinquish();
-        }
-    }
-    tc_fence_before();
-    if constexpr (kPair)
-        cluster_sync_all();
-    else
-        __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_holder;
-    pdl_wait_prior();
-    pdl_allow_next();
-
-    if (warp < S::EPI0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::REGS_LOW));
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int tile = unit; tile < num_tiles && ok; tile += units) {
-                int tm, tn;
-                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
-                const int arow = tm * TM + (int)rank * BM;
-                const int brow = tn * BN + (int)rank * S::B_ROWS;
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait_bounded<true>(&empty[stage], phase ^ 1u, abort_flag,
-                                                 p.wait_limit_ns, kStatusTimeoutTma, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    if constexpr (kPair) {
-                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (A_STAGE + B_STAGE));
-                        const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
-                        tma_load_2d_pair(sA + stage * A_STAGE, &tma_a, leader_full, kb * BK, arow);
-                        tma_load_2d_pair(sB + stage * B_STAGE, &tma_b, leader_full, kb * BK, brow);
-                    } else {
-                        mbar_arrive_expect_tx(&full[stage], A_STAGE + B_STAGE);
-                        tma_load_2d(sA + stage * A_STAGE, &tma_a, &full[stage], kb * BK, arow);
-                        tma_load_2d(sB + stage * B_STAGE, &tma_b, &full[stage], kb * BK, brow);
-                    }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok && rank == 0) {
-                for (int s = 0; s < STAGES; ++s) {
-                    stage = stage == 0 ? STAGES - 1 : stage - 1;
-                    if (stage == STAGES - 1) phase ^= 1u;
-                    volatile int no_abort = 0;
-                    mbar_wait_bounded(&full[stage], phase, &no_abort, 10000000ull,
-                                      kStatusTimeoutTma, p.status);
-                }
-            }
-        } else if (warp == 1 && lane == 0 && rank == 0) {
-            // ------------------------------------------- MMA issuer (leader)
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t g = 0;
-            bool ok = true;
-            for (int tile = unit; tile < num_tiles && ok; tile += units) {
-                for (int kb = 0; kb < nk; ++kb, ++g) {
-                    const uint32_t gs = g % GSLOTS, gphase = (g / GSLOTS) & 1u;
-                    if (!mbar_wait_bounded<true>(&sempty[gs], gphase ^ 1u, abort_flag,
-                                                 p.wait_limit_ns, kStatusTimeoutMma, p.status) ||
-                        !mbar_wait_bounded<true>(&full[stage], phase, abort_flag, p.wait_limit_ns,
-                                                 kStatusTimeoutMma, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
-                    const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
-                    const uint32_t d_tmem = tmem_base + gs * BN;
-#pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
-                        if constexpr (kPair)
-                            mma_f8_pair(d_tmem, smem_desc_sw128(a0 + 32 * k),
-                                        smem_desc_sw128(b0 + 32 * k), S::IDESC, k != 0);
-                        else
-                            mma_f8(d_tmem, smem_desc_sw128(a0 + 32 * k),
-                                   smem_desc_sw128(b0 + 32 * k), S::IDESC, k != 0);
-                    }
-                    if constexpr (kPair) {
-                        mma_commit_pair(&empty[stage], 0x3);
-                        mma_commit_pair(&sfull[gs], 0x3);
-                    } else {
-                        mma_commit(&empty[stage]);
-                        mma_commit(&sfull[gs]);
-                    }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if constexpr (kPair)
-                mma_commit_pair(drain, 0x1);
-            else
-                mma_commit(drain);
-            volatile int no_abort = 0;
-            mbar_wait_bounded(drain, 0, &no_abort, p.wait_limit_ns, kStatusTimeoutMma, p.status);
-        } else if (warp == 2) {
-            // ------------------------------------------------ scale stager
-            // lane l copies A rows l + 32i of this CTA's 128 and B rows
-            // l + 32i of the tile's 256 (per-row B) or, in lanes 0 and 1,
-            // the scale of the tile's first and second 128-row half of B
-            const BlockScales &sc = p.sc;
-            int slot = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int tile = unit; tile < num_tiles && ok; tile += units) {
-                int tm, tn;
-                grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
-                const int r0 = tm * TM + (int)rank * BM, c0 = tn * BN;
-                const float *arow[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    arow[i] = sc.sa + (int64_t)min(r0 + lane + 32 * i, p.M - 1) * sc.sa_row;
-                for (int kb = 0; kb < nk; ++kb) {
-                    bool w = mbar_wait_bounded<true>(&scempty[slot], ph ^ 1u, abort_flag,
-                                                     p.wait_limit_ns, kStatusTimeoutEpilogue,
-                                                     p.status);
-                    if (!__all_sync(0xFFFFFFFFu, w)) {
-                        ok = false;
-                        break;
-                    }
-                    float *dst = sring + slot * SCF;
-                    const int64_t ka = (int64_t)kb * sc.sa_k, kbo = (int64_t)kb * sc.sb_k;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) cp_async4(dst + lane + 32 * i, arow[i] + ka);
-                    if constexpr (kPerRowB) {
-#pragma unroll
-                        for (int i = 0; i < BN / 32; ++i) {
-                            const int col = min(c0 + lane + 32 * i, p.N - 1);
-                            cp_async4(dst + BM + lane + 32 * i, sc.sb + (int64_t)col * sc.sb_row + kbo);
-                        }
-                    } else if (lane < 2) {
-                        const int col = min(c0 + 128 * lane, p.N - 1);
-                        cp_async4(dst + BM + lane,
-                                  sc.sb + (int64_t)(col / sc.b_rows) * sc.sb_row + kbo);
-                    }
-                    cp_async_arrive_noinc(&scfull[slot]);
-                    if (++slot == SC) {
-                        slot = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            cp_async_wait_all();
-        }
-    } else {
-        // --------------------------------------------- epilogue (16 warps)
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::REGS_HIGH));
-        const int quarter = warp & 3;
-        const int cg = (warp - S::EPI0) >> 2;  // columns 64*cg .. +63 of the tile
-        const int fr = lane >> 2, fc = lane & 3;
-        uint32_t g = 0;
-        int slot = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int tile = unit; tile < num_tiles; tile += units) {
-            int tm, tn;
-            grouped_tile(tile, m_tiles, n_tiles, GROUP_M, tm, tn);
-            const int row0 = tm * TM + (int)rank * BM + quarter * 32 + fr;  // rows row0 + 8i
-            const int col0 = tn * BN + 64 * cg + 2 * fc;  // columns col0 + 16c + 8j, +1
-            uint64_t acc[4][8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = 0ull;
-            for (int kb = 0; kb < nk; ++kb, ++g) {
-                const uint32_t gs = g % GSLOTS, gphase = (g / GSLOTS) & 1u;
-                if (ok)
-                    ok = mbar_wait_bounded<true>(&scfull[slot], ph, abort_flag, p.wait_limit_ns,
-                                                 kStatusTimeoutEpilogue, p.status) &&
-                         mbar_wait_bounded<true>(&sfull[gs], gphase, abort_flag, p.wait_limit_ns,
-                                                 kStatusTimeoutEpilogue, p.status);
-                ok = __all_sync(0xFFFFFFFFu, ok);
-                const float *scs = sring + slot * SCF;
-                if (++slot == SC) {
-                    slot = 0;
-                    ph ^= 1u;
-                }
-                if (!ok) continue;  // outputs invalid; keep the loop shape
-                tc_fence_after();
-                uint64_t f2[4];  // per-row B: (sa, sa); per-tile B: (sa*sb, sa*sb)
-                float sbt = 1.f;
-                if constexpr (!kPerRowB) sbt = scs[BM + (cg >> 1)];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float a = scs[quarter * 32 + fr + 8 * i];
-                    const float f = kPerRowB ? a : a * sbt;
-                    f2[i] = pack2(f, f);
-                }
-                const float *sbc = scs + BM + 64 * cg + 2 * fc;
-                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + gs * BN +
-                                       (uint32_t)(64 * cg);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t ra[8], rb[8];
-                    tmem_ld_16x256b_x2(taddr + 16 * c, ra);
-                    tmem_ld_16x256b_x2(taddr + (16u << 16) + 16 * c, rb);
-                    tmem_ld_wait();
-                    tmem_regs_ready(ra);
-                    tmem_regs_ready(rb);
-                    if (c == 3) {  // the block's partial is in registers: hand the slot back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if constexpr (kPair)
-                                mbar_arrive_cluster(mapa_shared(smem_u32(&sempty[gs]), 0));
-                            else
-                                mbar_arrive(&sempty[gs]);
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        uint64_t m2[4];
-                        if constexpr (kPerRowB) {
-                            const float2 sbv = *reinterpret_cast<const float2 *>(sbc + 16 * c + 8 * j);
-                            const uint64_t sb2 = pack2(sbv.x, sbv.y);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) m2[i] = mul2(sb2, f2[i]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) m2[i] = f2[i];
-                        }
-                        const int a = 2 * c + j;
-                        acc[0][a] = fma2(pack2(__uint_as_float(ra[4 * j]), __uint_as_float(ra[4 * j + 1])),
-                                         m2[0], acc[0][a]);
-                        acc[1][a] = fma2(pack2(__uint_as_float(ra[4 * j + 2]), __uint_as_float(ra[4 * j + 3])),
-                                         m2[1], acc[1][a]);
-                        acc[2][a] = fma2(pack2(__uint_as_float(rb[4 * j]), __uint_as_float(rb[4 * j + 1])),
-                                         m2[2], acc[2][a]);
-                        acc[3][a] = fma2(pack2(__uint_as_float(rb[4 * j + 2]), __uint_as_float(rb[4 * j + 3])),
-                                         m2[3], acc[3][a]);
-                    }
-                }
-                __syncwarp();  // every lane's reads of this slot's scales are done
-                if (lane == 0) mbar_arrive(&scempty[slot == 0 ? SC - 1 : slot - 1]);
-            }
-            if (ok) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = row0 + 8 * i;
-                    if (row >= p.M) continue;
-                    uint16_t *drow = p.d + (int64_t)row * p.ldd;
-#pragma unroll
-                    for (int a = 0; a < 8; ++a) {
-                        const int col = col0 + 16 * (a >> 1) + 8 * (a & 1);
-                        if (col < p.N) {
-                            float lo, hi;
-                            unpack2(acc[i][a], lo, hi);
-                            *reinterpret_cast<uint32_t *>(drow + col) = pack_bf16x2(lo, hi);
-                        }
-                    }
-                }
-            }
-        }
-    }
-
-    __syncwarp();
-    tc_fence_before();
-    if constexpr (kPair)
-        cluster_sync_all();
-    else
-        __syncthreads();
-    tc_fence_after();
-    if (warp == 1) {
-        __syncwarp();
-        if constexpr (kPair)
-            tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
-        else
-            tmem_dealloc(tmem_base, S::TMEM_COLS);
-    }
-}
-
-template <bool kPerRowB>
-__global__ void __launch_bounds__(Shape16<false>::THREADS, 1)
-    gemm_f8_block16_kernel(const __grid_constant__ CUtensorMap tma_a,
-                           const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
-    block16_body<kPerRowB, false>(tma_a, tma_b, p);
-}
-
-template <bool kPerRowB>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape16<true>::THREADS, 1)
-    gemm_f8_block16_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
-                                const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
-    block16_body<kPerRowB, true>(tma_a, tma_b, p);
-}
-
-template <bool kPerRowB, bool kPair>
-cudaError_t launch_block16(const CUtensorMap &ta, const CUtensorMap &tb, const BlockArgs &args,
-                           int grid, cudaStream_t s, const char **why) {
-    using S = Shape16<kPair>;
-    auto kernel = kPair ? gemm_f8_block16_pair_kernel<kPerRowB> : gemm_f8_block16_kernel<kPerRowB>;
-    static std::atomic<bool> attr_done[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        // setmaxnreg.inc waits until the CTA's launch allocation can supply
-        // the raised counts: refuse a build whose register count at launch
-        // would leave it waiting
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-        if (e != cudaSuccess) return e;
-        if ((int64_t)fa.numRegs * S::THREADS <
-            (int64_t)128 * S::REGS_LOW + (int64_t)(S::THREADS - 128) * S::REGS_HIGH) {
-            *why = "block GEMM: the register split does not fit the kernel's launch allocation";
-            return cudaErrorInvalidConfiguration;
-        }
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
-    return launch_pdl(kernel, grid, S::THREADS, S::SMEM, s, ta, tb, args);
-}
-
-template <bool kPair>
-cudaError_t launch_shape16(const uint8_t *A, const uint8_t *B, const BlockArgs &args,
-                           cudaStream_t s, const char **why) {
-    CUtensorMap ta, tb;
-    if (!make_tmap_k128(&ta, A, args.M, args.K, BM) ||
-        !make_tmap_k128(&tb, B, args.N, args.K, Shape16<kPair>::B_ROWS)) {
-        *why = "cuTensorMapEncodeTiled failed";
-        return cudaErrorInvalidValue;
-    }
-    const int64_t tm = kPair ? 2 * BM : BM;
-    const int64_t tiles = ((args.M + tm - 1) / tm) * ((args.N + 255) / 256);
-    const int64_t units = kPair ? num_sms() / 2 : num_sms();
-    const int grid = (int)(tiles < units ? tiles : units) * (kPair ? 2 : 1);
-    if (args.sc.b_rows == 1) return launch_block16<true, kPair>(ta, tb, args, grid, s, why);
-    if (args.sc.b_rows == 128) return launch_block16<false, kPair>(ta, tb, args, grid, s, why);
-    *why = "B scales must be per row or per 128-row tile";
-    return cudaErrorInvalidValue;
-}
-
-template <bool kPerRowB, int kBN>
+template <bool kPerRowB, int kBN, bool kScalar>
 __global__ void __launch_bounds__(Shape<false, kBN>::THREADS, 1)
     gemm_f8_block_kernel(const __grid_constant__ CUtensorMap tma_a,
                          const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
-    block_gemm_body<kPerRowB, false, kBN>(tma_a, tma_b, p);
+    block_gemm_body<kPerRowB, false, kBN, kScalar>(tma_a, tma_b, p);
 }
 
-template <bool kPerRowB, int kBN>
+template <bool kPerRowB, int kBN, bool kScalar>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<true, kBN>::THREADS, 1)
     gemm_f8_block_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                               const __grid_constant__ CUtensorMap tma_b, const BlockArgs p) {
-    block_gemm_body<kPerRowB, true, kBN>(tma_a, tma_b, p);
+    block_gemm_body<kPerRowB, true, kBN, kScalar>(tma_a, tma_b, p);
 }
 
-template <bool kPerRowB, bool kPair, int kBN>
+template <bool kPerRowB, bool kPair, int kBN, bool kScalar>
 cudaError_t launch_block(const CUtensorMap &ta, const CUtensorMap &tb, const BlockArgs &args,
                          int grid, cudaStream_t s, const char **why) {
     using S = Shape<kPair, kBN>;
-    auto kernel = kPair ? gemm_f8_block_pair_kernel<kPerRowB, kBN>
-                        : gemm_f8_block_kernel<kPerRowB, kBN>;
+    auto kernel = kPair ? gemm_f8_block_pair_kernel<kPerRowB, kBN, kScalar>
+                        : gemm_f8_block_kernel<kPerRowB, kBN, kScalar>;
     constexpr size_t smem = S::SMEM;
     static std::atomic<bool> attr_done[64];
     int dev = 0;
@@ -1162,9 +753,30 @@ cudaError_t launch_block(const CUtensorMap &ta, const CUtensorMap &tb, const Blo
     return launch_pdl(kernel, grid, S::THREADS, smem, s, ta, tb, args);
 }
 
-template <bool kPair, int kBN>
-cudaError_t launch_shape(const uint8_t *A, const uint8_t *B, const BlockArgs &args,
+// Row tiles per raster group.  The CTAs running at one time cover `group`
+// row tiles by units/group column tiles, and each streams its row panel of A
+// (tm rows) and column panel of B (bn rows) over the whole contraction; with
+// the panels in L2 while that wave runs, the wave reads
+// group * tm + ceil(units / group) * bn rows of contraction bytes from DRAM,
+// which this minimises (for 32768 x 8192 x 8192 on 152 SMs: 17 row tiles of
+// 128 by 9 column tiles of 256, against the 8 by 19 of a fixed group of 8).
+int block_raster_group(int64_t m_tiles, int64_t units, int tm, int bn) {
+    int best = 1;
+    int64_t best_rows = INT64_MAX;
+    for (int64_t g = 1; g <= m_tiles && g <= units; ++g) {
+        const int64_t rows = g * tm + ((units + g - 1) / g) * bn;
+        if (rows < best_rows) {
+            best_rows = rows;
+            best = (int)g;
+        }
+    }
+    return best;
+}
+
+template <bool kPair, int kBN, bool kScalar>
+cudaError_t launch_shape(const uint8_t *A, const uint8_t *B, const BlockArgs &args_in,
                          cudaStream_t s, const char **why) {
+    BlockArgs args = args_in;
     CUtensorMap ta, tb;
     if (!make_tmap_k128(&ta, A, args.M, args.K, BM) ||
         !make_tmap_k128(&tb, B, args.N, args.K, Shape<kPair, kBN>::B_ROWS)) {
@@ -1175,8 +787,12 @@ cudaError_t launch_shape(const uint8_t *A, const uint8_t *B, const BlockArgs &ar
     const int64_t tiles = ((args.M + tm - 1) / tm) * ((args.N + kBN - 1) / kBN);
     const int64_t units = kPair ? num_sms() / 2 : num_sms();
     const int grid = (int)(tiles < units ? tiles : units) * (kPair ? 2 : 1);
-    if (args.sc.b_rows == 1) return launch_block<true, kPair, kBN>(ta, tb, args, grid, s, why);
-    if (args.sc.b_rows == 128) return launch_block<false, kPair, kBN>(ta, tb, args, grid, s, why);
+    const char *ge = getenv("FP8LINEAR_BLOCK_GROUP");
+    args.group_m = ge != nullptr && atoi(ge) > 0
+                       ? atoi(ge)
+                       : block_raster_group((args.M + tm - 1) / tm, units, (int)tm, kBN);
+    if (args.sc.b_rows == 1) return launch_block<true, kPair, kBN, kScalar>(ta, tb, args, grid, s, why);
+    if (args.sc.b_rows == 128) return launch_block<false, kPair, kBN, kScalar>(ta, tb, args, grid, s, why);
     *why = "B scales must be per row or per 128-row tile";
     return cudaErrorInvalidValue;
 }
@@ -1185,11 +801,14 @@ cudaError_t launch_shape(const uint8_t *A, const uint8_t *B, const BlockArgs &ar
 
 // Kernel choice, measured at 32768 x 8192 x 8192 (TFLOP/s):
 //                       one CTA 128   one CTA 256   pair 128   pair 256
-//   per-tile B (fprop)      1829          2552-2582     1697       1871-1887
-//   per-row B (wgrad)       1374          1476          1311       1489
-// One CTA with 256-wide tiles by default; problems with fewer 128 x 256 tiles
-// than SMs take 128-wide tiles.  FP8LINEAR_BLOCK_PAIR=0/1 and
-// FP8LINEAR_BLOCK_BN=128/256 override the choice (the tests run all four).
+//   per-tile B (fprop)      1829          2541-2561     1697       2570-2593
+//   per-row B (wgrad)       1374          1627-1636     1311       1633-1650
+// (256-wide tiles: packed accumulators for per-tile B, scalar ones for
+// per-row B.)  CTA pairs with 256-wide tiles by default; problems with fewer
+// 128 x 256 tiles than SMs take one CTA with 128-wide tiles.
+// FP8LINEAR_BLOCK_PAIR=0/1, FP8LINEAR_BLOCK_BN=128/256, FP8LINEAR_BLOCK_ACC=0/1
+// and FP8LINEAR_BLOCK_GROUP=<row tiles> override the choice (the tests run
+// every kernel).
 cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
                               const BlockScales &sc, uint16_t *D, cudaStream_t s,
                               const char **why) {
@@ -1204,19 +823,23 @@ cudaError_t launch_gemm_block(const uint8_t *A, const uint8_t *B, int64_t M, int
     args.status = device_status_word();
     const char *pe = getenv("FP8LINEAR_BLOCK_PAIR");
     const char *be = getenv("FP8LINEAR_BLOCK_BN");
-    const char *ee = getenv("FP8LINEAR_BLOCK_EPI");
     const bool wide = be != nullptr ? atoi(be) == 256
                                     : ((M + 127) / 128) * ((N + 255) / 256) >= num_sms();
-    const bool pair = pe != nullptr && atoi(pe) == 1;
-    const bool epi16 = ee != nullptr && atoi(ee) == 16;
-    if (wide && epi16)
-        return pair ? launch_shape16<true>(A, B, args, s, why)
-                    : launch_shape16<false>(A, B, args, s, why);
-    if (wide)
-        return pair ? launch_shape<true, 256>(A, B, args, s, why)
-                    : launch_shape<false, 256>(A, B, args, s, why);
-    return pair ? launch_shape<true, 128>(A, B, args, s, why)
-                : launch_shape<false, 128>(A, B, args, s, why);
+    // CTA pairs for wide tiles (each SM streams half of B's bytes), one CTA for
+    // narrow ones; FP8LINEAR_BLOCK_PAIR=0/1 overrides
+    const bool pair = pe != nullptr ? atoi(pe) == 1 : wide;
+    // wide tiles, per-row B: scalar accumulators (below); FP8LINEAR_BLOCK_ACC=0/1 overrides
+    const char *ae = getenv("FP8LINEAR_BLOCK_ACC");
+    const bool scalar = ae != nullptr ? atoi(ae) == 1 : sc.b_rows == 1;
+    if (wide) {
+        if (scalar)
+            return pair ? launch_shape<true, 256, true>(A, B, args, s, why)
+                        : launch_shape<false, 256, true>(A, B, args, s, why);
+        return pair ? launch_shape<true, 256, false>(A, B, args, s, why)
+                    : launch_shape<false, 256, false>(A, B, args, s, why);
+    }
+    return pair ? launch_shape<true, 128, false>(A, B, args, s, why)
+                : launch_shape<false, 128, false>(A, B, args, s, why);
 }
 
 }  // namespace fp8
