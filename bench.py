@@ -18,7 +18,7 @@ kernel boundaries of every 10th step), the roofline of the dgrad+wgrad launch,
 an end-to-end figure with host copies, SM clocks sampled during the timed
 region, and the CPU oracle's time on a bounded sample.  On one GPU the line
 also carries `workloads`: configuration 1's latency (quantise X, W + fprop at
-64x256x256), the MLP block, the packed THD batch and the block recipe
+64x256x256, in one launch and in three), the MLP block, the packed THD batch and the block recipe
 (whole-step TFLOP/s and each one's dominant kernel), and the quantisers at
 2^30 elements.
 
@@ -934,13 +934,15 @@ def workload_sweep(args, lgs=range(20, 31, 2), multi=True, only=None):
 
 def workload_config1(args, iters=1000):
     """Configuration 1, the latency case: X [64,256] ~N(0,1), W [256,256]
-    ~N(0,0.02), seed 0, both quantised by the single-launch dynamic quantiser,
-    then fprop: three launches.  Median µs per iteration over `iters`
-    iterations, each bracketed by events (eager: host launch gaps included),
-    and per iteration of a CUDA graph of the three launches replayed
-    back to back (device time only).  A bf16 torch.matmul (cuBLAS) of the
-    same shape is timed the same way as context: the pages report FP8 slower
-    than bf16 on small matmuls."""
+    ~N(0,0.02), seed 0, current scaling, fprop.  Two paths through the public
+    API: one launch (fp8_linear_fprop_dynamic_small: amaxes, scales, casts and
+    the GEMM in one CTA) and three launches (the single-launch dynamic
+    quantiser on X and on W, then fp8_linear_fprop).  For each, the median µs
+    per iteration over `iters` iterations bracketed by events (eager: host
+    launch overhead included) and the µs per iteration of a CUDA graph of the
+    iteration's launches replayed back to back (device time).  A bf16
+    torch.matmul (cuBLAS) of the same shape is timed the same way as context:
+    the pages report FP8 slower than bf16 on small matmuls."""
     import torch
     import scaled_linear_layers_gb300 as fp8
     c = synth.CONFIG1
@@ -953,16 +955,21 @@ def workload_config1(args, iters=1000):
     w = to_dev(synth.normal_bf16((Nc, Kc), c["w_sigma"], c["seed"], "w"))
     f32 = dict(dtype=torch.float32, device=dev)
     sc = torch.empty(6, **f32)
+    sc1 = torch.empty(4, **f32)
     xq = torch.empty((Mc, Kc), dtype=torch.uint8, device=dev)
     wq = torch.empty((Nc, Kc), dtype=torch.uint8, device=dev)
     y = torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev)
+    y1 = torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev)
     n = fp8.fp8_quantize_fused_workspace_bytes() // 4
     wsp = torch.zeros(2 * n, dtype=torch.int32, device=dev)
 
-    def run(_=0):
+    def run3(_=0):
         fp8.fp8_quantize_fused_dynamic(x, sc[0:1], sc[1:2], xq, None, sc[4:5], wsp[:n])
         fp8.fp8_quantize_fused_dynamic(w, sc[2:3], sc[3:4], wq, None, sc[5:6], wsp[n:])
         fp8.fp8_linear_fprop(xq, sc[0:1], wq, sc[2:3], Mc, Nc, Kc, fp8.DYNAMIC, None, y)
+
+    def run1(_=0):
+        fp8.fp8_linear_fprop_dynamic_small(x, w, sc1, y1)
 
     def median_us(fn):
         for _ in range(20):
@@ -976,20 +983,30 @@ def workload_config1(args, iters=1000):
             b.record()
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
-    eager = median_us(run)
-    t_graph, mode = _graph_time(torch, run, reps=100)
+    eager1 = median_us(run1)
+    t1, mode1 = _graph_time(torch, run1, reps=100)
+    eager3 = median_us(run3)
+    t3, mode3 = _graph_time(torch, run3, reps=100)
     fp8.fp8_check_device_status()
+    same = bool(torch.equal(y, y1))
     bf16 = median_us(lambda: torch.matmul(x, w.t()))
+    yb = torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev)
+    tb, _ = _graph_time(torch, lambda _=0: torch.matmul(x, w.t(), out=yb), reps=100)
     flop = 2.0 * Mc * Nc * Kc
-    return {"metric": "latency of quantise X, W (dynamic) + fprop", "value": round(eager, 2),
-            "unit": "us", "higher_is_better": False,
+    return {"metric": "latency of current-scaling fprop (quantise X, W + GEMM)",
+            "value": round(eager1, 2), "unit": "us", "higher_is_better": False,
             "config": {"workload": "single FP8 linear fprop, dynamic tensorwise scaling, "
                                    "X [64,256], W [256,256], seed 0", "M": Mc, "N": Nc, "K": Kc},
-            "launches_per_iteration": 3, "iterations": iters,
-            "median_us_eager": round(eager, 2),
-            "us_per_iteration_graph": round(t_graph * 1e6, 2), "graph_timing": mode,
-            "tflops_graph": round(flop / t_graph / 1e12, 3),
+            "iterations": iters,
+            "one_launch": {"median_us_eager": round(eager1, 2),
+                           "us_per_iteration_graph": round(t1 * 1e6, 2), "graph_timing": mode1,
+                           "tflops_graph": round(flop / t1 / 1e12, 3)},
+            "three_launches": {"median_us_eager": round(eager3, 2),
+                               "us_per_iteration_graph": round(t3 * 1e6, 2),
+                               "graph_timing": mode3},
+            "same_output_bits": same,
             "bf16_torch_matmul_median_us": round(bf16, 2),
+            "bf16_torch_matmul_us_per_iteration_graph": round(tb * 1e6, 2),
             "note": "latency-bound: roofline fractions are not meaningful at this size"}
 
 

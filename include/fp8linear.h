@@ -400,6 +400,26 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
 fp8_status fp8_linear_step_dynamic(const fp8_linear_step_io *io, float *scales, void *workspace,
                                    int64_t M, int64_t N, int64_t K, cudaStream_t s);
 
+/* Current-scaling (dynamic tensorwise) fprop of a linear that fits one output
+ * tile, in one launch: amax of x [M,K] and of w [N,K], scale = amax/448 and
+ * scale_inv = 448/amax for each (amax clamped to 1e-12), the saturating e4m3
+ * casts, and y [M,N] = bf16(x_scale*w_scale * xq*wqᵀ (+ bias[N], fp32 add
+ * before the rounding)).  The same bytes, scales and outputs as
+ * fp8_quantize_fused_dynamic on x and on w followed by fp8_linear_fprop, in one
+ * launch instead of three: for the small, latency-bound shapes on which the
+ * NeMo SALMAutomodel page reports FP8 slower than bf16 (the configuration
+ * X [64,256], W [256,256]).  M <= 128, N <= 256, K <= 512, each a multiple of
+ * 16 (else FP8_ERR_ALIGNMENT or, for larger shapes, FP8_ERR_UNSUPPORTED).
+ * `scales`: 4 device floats, receives x scale, x scale_inv, w scale,
+ * w scale_inv.  `amax` (2 device floats: x, w), `xq` [M,K], `wq` [N,K] and
+ * `bias` are nullable.  x, w, xq, wq, y 16-byte aligned.  No workspace.
+ * Source: SpecForge "Add training.fp8_linear" (dynamic tensorwise scaling);
+ * AstrAI fp8_state.py (scale rule, D = A_SCALE * B_SCALE * A * B). */
+fp8_status fp8_linear_fprop_dynamic_small(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N,
+                                          int64_t K, const uint16_t *bias, float *scales,
+                                          float *amax, uint8_t *xq, uint8_t *wq, uint16_t *y,
+                                          cudaStream_t s);
+
 /* One training step of one linear under the block recipe (TE recipe=block,
  * the NeMo "Add FP8 support for SALMAutomodel" page; 1x128 activation and
  * gradient tiles, 128x128 weight tiles): X -> xq with 1x128 row-tile scales

@@ -25,6 +25,7 @@ __all__ = [
     "fp8_dbias_workspace_bytes", "fp8_quantize_transpose_dbias", "fp8_pad_multiple",
     "fp8_padded_seq_len", "fp8_pad_tokens_bshd", "fp8_multi_amax_scales",
     "fp8_linear_step_dynamic", "DynamicStepState", "fp8_linear_step_block", "BlockStepScales",
+    "fp8_linear_fprop_dynamic_small",
     "fp8_meta_record",
     "fp8_meta_refresh", "fp8_state_step", "fp8_padded_rows", "fp8_pad_tokens",
     "fp8_check_device_status", "fp8_selftest_wait_timeout", "fp8_set_wait_limit_ns",
@@ -153,6 +154,20 @@ def fp8_linear_dgrad_wgrad(gq, gqt, g_scale, wqt, w_scale, xqt, x_scale, M, N, K
                                        _ptr(_u8(wqt)), _ptr(w_scale), _ptr(_u8(xqt)),
                                        _ptr(x_scale), M, N, K, recipe, _ptr(dx), _ptr(dw),
                                        _stream(stream)))
+
+
+def fp8_linear_fprop_dynamic_small(x, w, scales, y, bias=None, amax=None, xq=None, wq=None,
+                                   stream=None):
+    """Current-scaling fprop of a one-tile linear in one launch (see the C
+    header): x [M,K], w [N,K] bf16 -> y [M,N]; scales: 4 device floats."""
+    _bf16(x)
+    _bf16(w)
+    M, K = x.shape
+    N = w.shape[0]
+    assert w.shape[1] == K and tuple(y.shape) == (M, N)
+    _check(_LIB.fp8_linear_fprop_dynamic_small(_ptr(x), _ptr(w), M, N, K, _ptr(bias),
+                                               _ptr(scales), _ptr(amax), _ptr(_u8(xq)),
+                                               _ptr(_u8(wq)), _ptr(y), _stream(stream)))
 
 
 class DynamicStepState:

@@ -76,6 +76,7 @@ SIGNATURES = {
     "fp8_linear_step_delayed": (S, [ctypes.POINTER(fp8_meta), ctypes.POINTER(I64),
                                     ctypes.POINTER(fp8_linear_step_io), I64, I64, I64, P, P]),
     "fp8_linear_step_dynamic": (S, [ctypes.POINTER(fp8_linear_step_io), P, P, I64, I64, I64, P]),
+    "fp8_linear_fprop_dynamic_small": (S, [P, P, I64, I64, I64, P, P, P, P, P, P, P]),
     "fp8_linear_step_block": (S, [ctypes.POINTER(fp8_linear_step_io),
                                   ctypes.POINTER(fp8_block_step_scales), I64, I64, I64, P]),
     "fp8_padded_rows": (I64, [I64, I64]),

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libfp8linear.so")
 SOURCES = ["api.cu", "quantize.cu", "quantize_fused.cu", "gemm.cu", "gemm_pair.cu",
-           "gemm_block.cu", "meta.cu", "multi.cu"]
+           "gemm_block.cu", "meta.cu", "multi.cu", "linear_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-Xptxas", "-v", "--expt-relaxed-constexpr"]

@@ -90,6 +90,13 @@ cudaError_t launch_quantize_fused_dynamic_noalloc(const uint16_t *x, int64_t row
                                                   float *scale, float *scale_inv, uint8_t *q,
                                                   uint8_t *qt, float *amax_out, cudaStream_t s,
                                                   const char **why);
+// Current-scaling fprop of one output tile in one launch (linear_small.cu):
+// M <= 128, N <= 256, K <= 512 (linear_small_fits).
+bool linear_small_fits(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_linear_small_dynamic(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N,
+                                        int64_t K, const uint16_t *bias, float *scales,
+                                        float *amax, uint8_t *xq, uint8_t *wq, uint16_t *y,
+                                        cudaStream_t s);
 // amax[i], scale[i], scale_inv[i] of the bf16 tensors w[i] (numel[i]
 // elements, 16-byte aligned): current scaling, one amax launch per 64
 // tensors and one scale launch.
@@ -143,6 +150,10 @@ cudaError_t launch_meta_init(float *dev, int interval, cudaStream_t s);
 cudaError_t launch_meta_copy(float *dst, const float *src, cudaStream_t s);
 cudaError_t launch_meta_lag(float *scale, float *scale_inv, const float *amax, cudaStream_t s);
 cudaError_t launch_meta_refresh(float *dev, int interval, cudaStream_t s);
+// p[0..n) = 0 as a kernel launched with programmatic dependent launch, so
+// that it keeps the launch chain of a stream unbroken (a memset node would
+// not).
+cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t timeout_us, cudaStream_t s);
 
 }  // namespace fp8

@@ -34,6 +34,13 @@ __global__ void meta_lag_kernel(float *scale, float *scale_inv, const float *ama
     *scale_inv = si;
 }
 
+__global__ void zero_f32_kernel(float *p, int64_t n) {
+    pdl_wait_prior();
+    pdl_allow_next();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) p[i] = 0.0f;
+}
+
 __global__ void meta_fwd_kernel(float *dev, int idx, const float *amax_x, const float *amax_w) {
     pdl_wait_prior();
     pdl_allow_next();
@@ -109,6 +116,12 @@ cudaError_t launch_meta_lag(float *scale, float *scale_inv, const float *amax, c
 cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const float *amax_w,
                             cudaStream_t s) {
     return launch_pdl(meta_fwd_kernel, 1, 1, 0, s, dev, idx, amax_x, amax_w);
+}
+
+cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int threads = n < 256 ? 32 : 256;
+    return launch_pdl(zero_f32_kernel, (unsigned)((n + threads - 1) / threads), threads, 0, s, p, n);
 }
 
 cudaError_t launch_meta_refresh(float *dev, int interval, cudaStream_t s) {

@@ -80,7 +80,7 @@ cudaError_t launch_multi_amax_scales(const uint16_t *const *w, const int64_t *nu
                                      float *amax, float *scale, float *scale_inv,
                                      cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)n * sizeof(float), s);
+    cudaError_t e = launch_zero_f32(amax, n, s);
     if (e != cudaSuccess) return e;
     for (int base = 0; base < n; base += kMultiMax) {
         MultiArgs a;

@@ -489,7 +489,7 @@ static int grid_for(int64_t work_items, int per_block) {
 }
 
 cudaError_t launch_amax(const uint16_t *x, int64_t n, float *amax_out, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    cudaError_t e = launch_zero_f32(amax_out, 1, s);
     if (e != cudaSuccess || n == 0) return e;
     return launch_pdl(amax_kernel, grid_for((n >> 3) / 4 + 1, 256), 256, 0, s, x, n, amax_out);
 }
@@ -505,7 +505,7 @@ cudaError_t launch_quantize_tensor(const uint16_t *x, int64_t n, bool dynamic, f
                        (float *)nullptr, scale, scale_inv);
         if (e != cudaSuccess) return e;
     } else {
-        if (amax_out != nullptr && (e = cudaMemsetAsync(amax_out, 0, sizeof(float), s)) != cudaSuccess)
+        if (amax_out != nullptr && (e = launch_zero_f32(amax_out, 1, s)) != cudaSuccess)
             return e;
         if (n == 0) return cudaSuccess;
         e = launch_pdl(quantize_kernel<false>, grid, 256, 0, s, x, n, (const float *)scale_inv, q,
@@ -519,7 +519,7 @@ cudaError_t launch_quantize_rowtiles(const uint16_t *x, int64_t rows, int64_t co
                                      float *scale_inv, uint8_t *q, float *amax_out,
                                      cudaStream_t s) {
     cudaError_t e;
-    if (amax_out != nullptr && (e = cudaMemsetAsync(amax_out, 0, sizeof(float), s)) != cudaSuccess)
+    if (amax_out != nullptr && (e = launch_zero_f32(amax_out, 1, s)) != cudaSuccess)
         return e;
     const int64_t ntiles = rows * (cols / 128);
     if (ntiles == 0) return cudaSuccess;
@@ -569,7 +569,7 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
         if ((e = launch_amax(x, rows * cols, amax_out, s)) != cudaSuccess) return e;
         src = amax_out;
     } else {
-        if (amax_out != nullptr && (e = cudaMemsetAsync(amax_out, 0, sizeof(float), s)) != cudaSuccess)
+        if (amax_out != nullptr && (e = launch_zero_f32(amax_out, 1, s)) != cudaSuccess)
             return e;
         if (mode == kTensorDelayed) src = scale_inv;
     }

@@ -338,3 +338,16 @@ def test_fused_dynamic_rejects_more_tiles_than_int32(lib):
         assert fn(p, rows, cols, p, p, p, None, p, None) == 2   # FP8_ERR_SHAPE
     assert lib.fp8_quantize_fused_dynamic(p, rows, cols, p, p, p, None, p, p, None) == 2
     assert "tiles" in lib.fp8_last_error().decode()
+
+
+def test_small_fprop_host_checks(lib):
+    p = ctypes.c_void_p(0x1000)
+    f = lib.fp8_linear_fprop_dynamic_small
+    assert f(p, p, 144, 256, 256, None, p, None, None, None, p, None) == 4   # larger than a tile
+    assert "one tile" in lib.fp8_last_error().decode()
+    assert f(p, p, 64, 272, 256, None, p, None, None, None, p, None) == 4
+    assert f(p, p, 64, 256, 528, None, p, None, None, None, p, None) == 4
+    assert f(p, p, 64, 256, 24, None, p, None, None, None, p, None) == 3    # K % 16
+    assert f(p, p, 0, 256, 256, None, p, None, None, None, p, None) == 2
+    assert f(None, p, 64, 256, 256, None, p, None, None, None, p, None) == 1
+    assert f(p, p, 64, 256, 256, None, p, None, ctypes.c_void_p(0x1001), None, p, None) == 3
