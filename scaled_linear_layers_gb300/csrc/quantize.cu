@@ -220,11 +220,15 @@ struct QtJobs {
     float *snap_dst;
 };
 
-// Four CTAs per SM for every mode: the row+column mode would otherwise take
-// 120 registers and run two (32768 x 8192: 4625 against 3839 GB/s); the
-// others fit 64 registers anyway.
+// Four CTAs per SM for the row+column, 2D-tile and dynamic modes (the
+// row+column mode would otherwise take 120 registers and run two: 32768 x 8192,
+// 4625 against 3839 GB/s), five for the delayed mode the training step runs:
+// 48 registers without spills, so 760 slots take a 4096^2 step's 2048 tiles in
+// 2.7 waves instead of 3.4 (in-step forward / backward launches 23.2-23.5 /
+// 24.4-24.7 us against 23.6-23.9 / 24.9-25.2; six CTAs at 40 registers spill
+// and took 27.2 / 28.8).
 template <int kMode>
-__global__ void __launch_bounds__(256, 4) quantize_transpose_kernel(const QtJobs jobs) {
+__global__ void __launch_bounds__(256, kMode == kTensorDelayed ? 5 : 4) quantize_transpose_kernel(const QtJobs jobs) {
     __shared__ uint32_t tile[128 * 32];
     __shared__ uint32_t red[8];
     __shared__ uint32_t colmax[8][128];
