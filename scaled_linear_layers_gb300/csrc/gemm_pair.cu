@@ -23,6 +23,8 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <cstdlib>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -43,10 +45,20 @@ constexpr size_t SMEM_LIMIT = 227 * 1024;
 // 128*KSUB): narrower N tiles take two boxes per stage so each barrier round
 // trip covers 8 MMAs (measured: +7% at 4096^3 for N=224, a loss at N=256
 // where only three 64 KB stages would fit).
-template <int BN>
+// Stage shape and MMA rounds, measured on the 4096^3 step (CUDA events, µs):
+// the single thread that issues the MMAs paces the tensor pipe, so how many
+// MMAs it issues per barrier round matters as much as the ring depth.
+//   N tile 224: two 128-byte boxes per stage (three 60 KB stages), one stage per
+//     round: fprop 48.0-48.3; one box per stage (seven 30 KB stages) taken one /
+//     two / three per round: 52.4 / 48.95-49.5 / 49.4-49.9.
+//   N tile 256: one box per stage (seven 32 KB stages) taken two per round:
+//     dgrad+wgrad 85.3-86.5; one / three / four per round: 88.1-90.1 /
+//     87.2-87.5 / 89.3; two boxes per stage (three 64 KB stages): 88.5.
+template <int BN, int KS = (BN < 256 ? 2 : 1), int BATCH = (BN < 256 ? 1 : 2)>
 struct PairCfg {
     static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "N tile");
-    static constexpr int KSUB = BN < 256 ? 2 : 1;
+    static constexpr int KSUB = KS;
+    static constexpr int MMA_BATCH = BATCH;  // stages the MMA issuer takes per round
     static constexpr int BK = 128 * KSUB;
     static constexpr int BNH = BN / 2;  // B rows held by each CTA
     static constexpr int A_SUB = 128 * 128, B_SUB = BNH * 128;  // one 128-byte box
@@ -88,13 +100,13 @@ __device__ __forceinline__ TileRef locate(const PairArgs &p, int tile) {
     return r;
 }
 
-template <int BN>
+template <int BN, int KS, int BATCH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_f8_pair_kernel(const __grid_constant__ CUtensorMap tma_a0,
                         const __grid_constant__ CUtensorMap tma_b0,
                         const __grid_constant__ CUtensorMap tma_a1,
                         const __grid_constant__ CUtensorMap tma_b1, const PairArgs p) {
-    using C = PairCfg<BN>;
+    using C = PairCfg<BN, KS, BATCH>;
     constexpr int STAGES = C::STAGES, A_STAGE = C::A_STAGE, B_STAGE = C::B_STAGE;
     constexpr int BNH = C::BNH, BK = C::BK, KSUB = C::KSUB;
 
@@ -200,6 +212,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int it = 0;
+            // descriptors of stage 0's A and B boxes; a descriptor's address
+            // field holds (address >> 4) in 14 bits and shared addresses stay
+            // below 2^18, so adding an offset >> 4 never carries out of it
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA));
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB));
             for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++it) {
                 const int nk = ((tile >= p.pr[0].tiles ? p.pr[1].K : p.pr[0].K) + BK - 1) / BK;
                 const int acc = it & 1;
@@ -211,28 +228,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.wait_limit_ns,
-                                           kStatusTimeoutMma, p.status)) {
-                        ok = false;
-                        break;
+                // One round: wait for NB stages, then issue their MMAs and a
+                // commit per stage.  This single thread's instruction path
+                // paces the tensor pipe, so the rounds are unrolled and the
+                // shared-memory descriptors advance by adding the byte
+                // offset >> 4 to the address field of a precomputed base.
+                int kb = 0;
+                auto round = [&](auto nb_const) -> bool {
+                    constexpr int NB = decltype(nb_const)::value;
+                    int st = stage;
+                    uint32_t ph = phase;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        if (!mbar_wait_bounded(&full[st], ph, abort_flag, p.wait_limit_ns,
+                                               kStatusTimeoutMma, p.status))
+                            return false;
+                        if (++st == STAGES) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
-                    const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
 #pragma unroll
-                    for (int ks = 0; ks < KSUB; ++ks)
+                    for (int b = 0; b < NB; ++b) {
+                        const uint64_t ad = a_desc0 + (uint64_t)((stage * A_STAGE) >> 4);
+                        const uint64_t bd = b_desc0 + (uint64_t)((stage * B_STAGE) >> 4);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_f8_pair(d_tmem, smem_desc_sw128(a0 + ks * C::A_SUB + 32 * k),
-                                        smem_desc_sw128(b0 + ks * C::B_SUB + 32 * k), C::IDESC,
-                                        (kb | ks | k) != 0);
-                    mma_commit_pair(&empty[stage], 0x3);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                        for (int ks = 0; ks < KSUB; ++ks)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_f8_pair(d_tmem, ad + (uint64_t)((ks * C::A_SUB + 32 * k) >> 4),
+                                            bd + (uint64_t)((ks * C::B_SUB + 32 * k) >> 4),
+                                            C::IDESC, ((kb + b) | ks | k) != 0);
+                        mma_commit_pair(&empty[stage], 0x3);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                }
+                    kb += NB;
+                    return true;
+                };
+                while (ok && kb + C::MMA_BATCH <= nk)
+                    ok = round(std::integral_constant<int, C::MMA_BATCH>{});
+                while (ok && kb < nk) ok = round(std::integral_constant<int, 1>{});
                 if (ok) mma_commit_pair(&tfull[acc], 0x3);
             }
             mma_commit_pair(drain, 0x1);
@@ -311,14 +350,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int BN>
+template <int BN, int KS = (BN < 256 ? 2 : 1), int BATCH = (BN < 256 ? 1 : 2)>
 cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char **why) {
-    using C = PairCfg<BN>;
+    using C = PairCfg<BN, KS, BATCH>;
     static std::atomic<bool> attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_f8_pair_kernel<BN>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_f8_pair_kernel<BN, KS, BATCH>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -352,7 +391,7 @@ cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char 
     args.status = device_status_word();
     const int64_t pairs = num_sms() / 2;
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    return launch_pdl(gemm_f8_pair_kernel<BN>, grid, NUM_THREADS, C::SMEM_BYTES, s, ta[0], tb[0],
+    return launch_pdl(gemm_f8_pair_kernel<BN, KS, BATCH>, grid, NUM_THREADS, C::SMEM_BYTES, s, ta[0], tb[0],
                       ta[1], tb[1], args);
 }
 
@@ -383,7 +422,8 @@ cudaError_t launch_gemm_pair(const PairGemm *g, int n, int bn, cudaStream_t s, c
         *why = "a pair launch takes one or two problems";
         return cudaErrorInvalidValue;
     }
-    switch (bn ? bn : choose_pair_bn(g, n, num_sms() / 2)) {
+    const int b = bn ? bn : choose_pair_bn(g, n, num_sms() / 2);
+    switch (b) {
     case 224: return launch_pair_bn<224>(g, n, s, why);
     case 192: return launch_pair_bn<192>(g, n, s, why);
     case 160: return launch_pair_bn<160>(g, n, s, why);
