@@ -54,6 +54,22 @@ constexpr size_t SMEM_LIMIT = 227 * 1024;
 //   N tile 256: one box per stage (seven 32 KB stages) taken two per round:
 //     dgrad+wgrad 85.3-86.5; one / three / four per round: 88.1-90.1 /
 //     87.2-87.5 / 89.3; two boxes per stage (three 64 KB stages): 88.5.
+// (Those figures predate the staged output path below, whose 16 KB leave the
+// 256-wide tile six stages.)
+//
+// Output path, measured back to back on one GPU (fprop / dgrad+wgrad / whole
+// step, µs; the same code differs by about 2 µs between GPUs, so only figures
+// taken on one GPU compare):
+//   per-thread 16-byte stores, one row per thread:  49.0 / 87.3 / 172.3
+//   staged in shared memory, coalesced stores:       47.6 / 85.3 / 168.4
+//   staged, one 32 x 32 TMA box store per chunk:     47.6 / 85.5 / 166.3
+//   no global stores at all (timing probe only):     43.3 / 79.0 / 157.4
+// Writing the staging boxes costs nothing measurable (43.9 / 78.7 without
+// the copies); the global writes themselves cost 2.5-4 µs per launch whatever
+// their shape, also when every tile writes one L2-resident region.  64-column
+// boxes (128-byte swizzle, 32 KB of staging) gain 0.5 µs per launch but no
+// longer leave room for the step's backward quantiser to run beside fprop,
+// which costs the step 5 µs.
 template <int BN, int KS = (BN < 256 ? 2 : 1), int BATCH = (BN < 256 ? 1 : 2)>
 struct PairCfg {
     static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "N tile");
@@ -64,18 +80,19 @@ struct PairCfg {
     static constexpr int A_SUB = 128 * 128, B_SUB = BNH * 128;  // one 128-byte box
     static constexpr int A_STAGE = A_SUB * KSUB, B_STAGE = B_SUB * KSUB;
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;  // per CTA
-    static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - 1024 - 256) / STAGE_BYTES);
+    // output staging: two 32 x 32 bf16 boxes (2 KB each) per epilogue warp
+    static constexpr int STAGING = 4 * 2 * 2048;
+    static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - 1024 - 1024 - STAGING) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr uint32_t IDESC = idesc_f8_f32(256, BN);
-    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+    // alignment slack, the stage ring, barriers (in a 1 KB slot), staging
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 1024 + STAGING;
 };
 
 struct PairProblem {
     int M, N, K;
     const float *sa, *sb;
     const uint16_t *bias;
-    uint16_t *d;
-    int64_t ldd;
     int m_tiles, n_tiles, tiles;
 };
 
@@ -105,7 +122,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_f8_pair_kernel(const __grid_constant__ CUtensorMap tma_a0,
                         const __grid_constant__ CUtensorMap tma_b0,
                         const __grid_constant__ CUtensorMap tma_a1,
-                        const __grid_constant__ CUtensorMap tma_b1, const PairArgs p) {
+                        const __grid_constant__ CUtensorMap tma_b1,
+                        const __grid_constant__ CUtensorMap tma_d0,
+                        const __grid_constant__ CUtensorMap tma_d1, const PairArgs p) {
     using C = PairCfg<BN, KS, BATCH>;
     constexpr int STAGES = C::STAGES, A_STAGE = C::A_STAGE, B_STAGE = C::B_STAGE;
     constexpr int BNH = C::BNH, BK = C::BK, KSUB = C::KSUB;
@@ -123,6 +142,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    uint8_t *staging = smem + STAGES * C::STAGE_BYTES + 1024;  // 1024-byte aligned
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -143,9 +163,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         fence_mbarrier_init();
         tma_prefetch_desc(&tma_a0);
         tma_prefetch_desc(&tma_b0);
+        tma_prefetch_desc(&tma_d0);
         if (p.pr[1].tiles > 0) {
             tma_prefetch_desc(&tma_a1);
             tma_prefetch_desc(&tma_b1);
+            tma_prefetch_desc(&tma_d1);
         }
     }
     if (warp == 1) {
@@ -280,7 +302,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ---------------------------------------------- epilogue (both CTAs)
+        // Warp q owns accumulator lanes 32q..32q+31 (one output row per
+        // thread).  Each 32-column chunk is scaled, rounded to bf16 and
+        // written into one of the warp's two 2 KB staging boxes in the 64-byte
+        // swizzled layout (conflict-free), and lane 0 stores the box with one
+        // TMA copy.  Per-thread row stores (32 rows per warp instruction) cost
+        // the MMA pipe 7-10 µs per launch at 4096^3 in measurement; the
+        // staged box needs one issue per chunk.
         const int quarter = warp & 3;
+        uint8_t *stg = staging + quarter * 4096;
+        uint32_t chunk = 0;
         int it = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
             const int acc = it & 1;
@@ -291,14 +322,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const TileRef tr = locate(p, tile);
             const int tm = tr.tm, tn = tr.tn;
-            const int pM = tr.pi ? p.pr[1].M : p.pr[0].M;
             const int pN = tr.pi ? p.pr[1].N : p.pr[0].N;
             const uint16_t *bias = tr.pi ? p.pr[1].bias : p.pr[0].bias;
+            const CUtensorMap *td = tr.pi ? &tma_d1 : &tma_d0;
             const float s = tr.pi ? __fmul_rn(*p.pr[1].sa, *p.pr[1].sb)
                                   : __fmul_rn(*p.pr[0].sa, *p.pr[0].sb);
-            const int row = tm * 256 + (int)rank * 128 + quarter * 32 + lane;
-            uint16_t *drow = (tr.pi ? p.pr[1].d : p.pr[0].d) +
-                             (int64_t)row * (tr.pi ? p.pr[1].ldd : p.pr[0].ldd);
+            const int row0 = tm * 256 + (int)rank * 128 + quarter * 32;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
@@ -307,37 +336,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                    r);
                 tmem_ld_wait();
                 const int col = tn * BN + c * 32;
-                if (row < pM && col < pN) {
-                    uint32_t packed[16];
-                    if (bias != nullptr) {
+                if (col >= pN) continue;  // warp-uniform; rows past M are clipped by the copy
+                uint32_t packed[16];
+                if (bias != nullptr) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float b0 = __uint_as_float((uint32_t)bias[col + 2 * j] << 16);
-                            const float b1 =
-                                __uint_as_float((uint32_t)bias[col + 2 * j + 1] << 16);
-                            packed[j] =
-                                pack_bf16x2(__fadd_rn(__fmul_rn(__uint_as_float(r[2 * j]), s), b0),
-                                            __fadd_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), s), b1));
-                        }
-                    } else {
+                    for (int j = 0; j < 16; ++j) {
+                        const float b0 = __uint_as_float((uint32_t)bias[col + 2 * j] << 16);
+                        const float b1 = __uint_as_float((uint32_t)bias[col + 2 * j + 1] << 16);
+                        packed[j] =
+                            pack_bf16x2(__fadd_rn(__fmul_rn(__uint_as_float(r[2 * j]), s), b0),
+                                        __fadd_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), s), b1));
+                    }
+                } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            packed[j] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * j]), s),
-                                                    __fmul_rn(__uint_as_float(r[2 * j + 1]), s));
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(drow + col);
-                    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    if (col + 16 < pN) {
-                        dst[2] = make_uint4(packed[8], packed[9], packed[10], packed[11]);
-                        dst[3] = make_uint4(packed[12], packed[13], packed[14], packed[15]);
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        packed[j] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * j]), s),
+                                                __fmul_rn(__uint_as_float(r[2 * j + 1]), s));
+                }
+                uint8_t *box = stg + (chunk & 1u) * 2048;
+                ++chunk;
+                if (lane == 0) bulk_wait_group_read<1>();  // this box's previous copy has read it
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(box + lane * 64 + 16 * (q ^ ((lane >> 1) & 3))) =
+                        make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                   packed[4 * q + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(td, smem_u32(box), col, row0);
+                    bulk_commit_group();
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
         }
+        if (lane == 0) bulk_wait_group_all();  // outputs written before the CTA retires
     }
 
     __syncwarp();  // lanes that skipped a role wait here for their warp's lane 0
@@ -363,13 +399,14 @@ cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char 
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    CUtensorMap ta[2], tb[2];
+    CUtensorMap ta[2], tb[2], td[2];
     PairArgs args;
     int64_t tiles = 0;
     for (int i = 0; i < 2; ++i) {
         const PairGemm &q = g[i < n ? i : 0];  // an absent second problem: copies, no tiles
         if (!make_tmap_k128(&ta[i], q.A, q.M, q.K, 128) ||
-            !make_tmap_k128(&tb[i], q.B, q.N, q.K, C::BNH)) {
+            !make_tmap_k128(&tb[i], q.B, q.N, q.K, C::BNH) ||
+            !make_tmap_bf16_store32(&td[i], q.D, q.M, q.N, q.N)) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
@@ -380,8 +417,6 @@ cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char 
         pr.sa = q.sa;
         pr.sb = q.sb;
         pr.bias = q.bias;
-        pr.d = q.D;
-        pr.ldd = q.N;
         pr.m_tiles = (int)((q.M + 255) / 256);
         pr.n_tiles = (int)((q.N + BN - 1) / BN);
         pr.tiles = i < n ? pr.m_tiles * pr.n_tiles : 0;
@@ -392,7 +427,7 @@ cudaError_t launch_pair_bn(const PairGemm *g, int n, cudaStream_t s, const char 
     const int64_t pairs = num_sms() / 2;
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
     return launch_pdl(gemm_f8_pair_kernel<BN, KS, BATCH>, grid, NUM_THREADS, C::SMEM_BYTES, s, ta[0], tb[0],
-                      ta[1], tb[1], args);
+                      ta[1], tb[1], td[0], td[1], args);
 }
 
 }  // namespace

@@ -44,4 +44,21 @@ inline bool make_tmap_k128(CUtensorMap *m, const uint8_t *base, int64_t rows, in
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D bf16 matrix [rows, cols] with row stride ld elements (ld * 2 a multiple
+// of 16 bytes) as the target of 32-row x 32-column box stores from shared
+// memory laid out with the 64-byte swizzle: the 16-byte chunk c of box row r
+// sits at r * 64 + 16 * (c ^ ((r >> 1) & 3)) from a 512-byte-aligned base.
+inline bool make_tmap_bf16_store32(CUtensorMap *m, const uint16_t *base, int64_t rows,
+                                   int64_t cols, int64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fp8
