@@ -59,7 +59,10 @@ STEP_FLOP = 3 * GEMM_FLOP
 # algorithmic bytes of the quantisers per step (bf16 in, e4m3 out)
 # forward launch: X -> Xq (3 B/el) and W -> Wq, Wqᵀ (4 B/el); backward launch:
 # G -> Gq, Gqᵀ (4 B/el) and X -> Xqᵀ (3 B/el)
-QBYTES = {"quant_fwd": 3 * M * K + 4 * N * K, "quant_bwd": 4 * M * N + 3 * M * K}
+# algorithmic bytes of the step's two quantiser launches: forward X -> xq and
+# W -> wq (bf16 read, e4m3 written); backward G -> gq, gqt and X -> xqt, plus
+# wqt as the byte transpose of wq (read and written once)
+QBYTES = {"quant_fwd": 3 * M * K + 3 * N * K, "quant_bwd": 4 * M * N + 3 * M * K + 2 * N * K}
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate on Blackwell (4.5 : 2.25 PFLOP/s)
 
 

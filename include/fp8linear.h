@@ -350,14 +350,15 @@ typedef struct {
  * fp8_linear_forward, then fp8_linear_backward), as one call that enqueues
  * every kernel:
  *   fp8_state_step (refresh every m->interval steps); amax[0..2] cleared;
- *   X -> xq with x_scale_inv (amax[0]) and W -> wq, wqt with scale_inv
- *   (amax[1]), one launch, which also copies x_scale to slot
- *   FP8_META_X_SCALE_FWD;
+ *   X -> xq with x_scale_inv (amax[0]) and W -> wq with scale_inv
+ *   (amax[1]; also wqt when g is NULL), one launch, which also copies
+ *   x_scale to slot FP8_META_X_SCALE_FWD;
  *   y = fprop(xq, x scale of that slot, wq, scale, bias);
  *   history[idx] = amax[1] and the lag update of the x scale from amax[0],
  *   one launch;
- *   if g: G -> gq, gqt with g_scale_inv (amax[2]) and X -> xqt with the
- *   updated x_scale_inv, one launch, which also copies g_scale to slot
+ *   if g: G -> gq, gqt with g_scale_inv (amax[2]), X -> xqt with the
+ *   updated x_scale_inv and wqt = wq's bytes transposed, one launch, which
+ *   also copies g_scale to slot
  *   FP8_META_G_SCALE_BWD (and, with dbias, sums G's columns as
  *   fp8_quantize_transpose_dbias does); the lag update of the g scale from
  *   amax[2];
@@ -371,8 +372,8 @@ typedef struct {
  * forked from and joined back into `s` with events: the memory-bound
  * quantisation overlaps the compute-bound GEMM.  To the caller everything is
  * ordered on `s` (work enqueued on `s` after this call sees all results).
- * The backward reuses the forward's Wqᵀ: the page quantises w again with the
- * same scale_inv, which gives the same bytes.  M, N, K multiples of 16.
+ * The backward's Wqᵀ is the forward's Wq transposed byte for byte: the page
+ * quantises w again with the same scale_inv, which gives the same bytes.  M, N, K multiples of 16.
  * `events` (nullable) receives FP8_STEP_NEVENTS cudaEventRecord calls on the
  * stream of each segment (before: the forward quantisation, fprop, the
  * forward state update, the backward quantisation, the backward state

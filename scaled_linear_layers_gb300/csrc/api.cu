@@ -660,14 +660,18 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     // between the previous step's last kernel and this step's first would break
     // their launch overlap (measured: 174.2 -> 172.0-172.7 us per 4096^3 step)
     FP8_TRY(cuda_status(launch_zero_f32(io->amax, 3, s), who));
-    // forward: X (lagged x scale, q only) and W (q and qt) in one launch,
-    // which also keeps the x scale fprop must use
+    // forward: X (lagged x scale, q only) and W (q, and qt for a forward-only
+    // step) in one launch, which also keeps the x scale fprop must use
     FP8_TRY(mark(s));
     DelayedQuantJob jx{io->x, M, K, d + FP8_META_X_SCALE_INV, io->xq,
                        save_x ? io->xqt : nullptr, io->amax + 0};
-    DelayedQuantJob jw{io->w, N, K, d + FP8_META_SCALE_INV, io->wq, io->wqt, io->amax + 1};
-    // W's tiles (q and qᵀ) take the launch's first CTAs and X's (q only) its
-    // last, so the partly filled last wave holds the cheaper tiles
+    // with a backward, Wqᵀ (only dgrad reads it) comes from the backward
+    // launch as the byte transpose of Wq, off the path to fprop: the
+    // forward launch then moves 98 MB instead of 117 at 4096^3
+    DelayedQuantJob jw{io->w, N, K, d + FP8_META_SCALE_INV, io->wq, bwd ? nullptr : io->wqt,
+                       io->amax + 1};
+    // W's tiles take the launch's first CTAs and X's (q only) its last, so
+    // the partly filled last wave holds the cheaper tiles
     FP8_TRY(cuda_status(launch_quantize_delayed_pair(jw, jx, s, d + FP8_META_X_SCALE,
                                                      d + FP8_META_X_SCALE_FWD),
                         who));
@@ -683,8 +687,9 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
     FP8_TRY(cuda_status(launch_meta_fwd(d, m->idx, io->amax + 0, io->amax + 1, s2), who));
     m->idx = (m->idx + 1) % m->interval;
     if (bwd) {
-        // backward: G (q and qt) and X again, transposed, with the updated
-        // scale; the launch keeps the g scale the backward GEMMs must use, so
+        // backward: G (q and qt), X again, transposed, with the updated
+        // scale, and Wqᵀ from Wq's bytes; the launch keeps the g scale the
+        // backward GEMMs must use, so
         // the lag update of the g scale runs right after it, off the GEMMs'
         // critical path
         FP8_TRY(mark(s2));
@@ -694,8 +699,9 @@ fp8_status fp8_linear_step_delayed(fp8_meta *m, int64_t *step_count, const fp8_l
         DelayedQuantJob jxt{io->x, save_x ? 0 : M, K, d + FP8_META_X_SCALE_INV, nullptr, io->xqt,
                             nullptr};
         jg.colsum = io->dbias != nullptr ? io->dbias_workspace : nullptr;  // G's column sums
+        const ByteTransposeJob wt{io->wq, N, K, io->wqt};  // Wqᵀ for dgrad
         FP8_TRY(cuda_status(launch_quantize_delayed_pair(jg, jxt, s2, d + FP8_META_G_SCALE,
-                                                         d + FP8_META_G_SCALE_BWD),
+                                                         d + FP8_META_G_SCALE_BWD, &wt),
                             who));
         if (io->dbias != nullptr)
             FP8_TRY(cuda_status(launch_colsum_reduce(io->dbias_workspace, M, N, io->dbias, s2),

@@ -70,9 +70,18 @@ struct DelayedQuantJob {
     float *amax_out;
     float *colsum = nullptr;  // per-tile column sums (bias gradient), nullable
 };
+// qt [cols, rows] = q [rows, cols]ᵀ for existing e4m3 bytes
+struct ByteTransposeJob {
+    const uint8_t *q;
+    int64_t rows, cols;
+    uint8_t *qt;
+};
+// The two delayed-mode casts in one launch, optionally with a byte transpose
+// in the same launch (tiles after the casts').
 cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const DelayedQuantJob &b,
                                          cudaStream_t s, const float *snap_src = nullptr,
-                                         float *snap_dst = nullptr);
+                                         float *snap_dst = nullptr,
+                                         const ByteTransposeJob *bt = nullptr);
 // Forward state update in one launch: history[idx] = *amax_w, then the lag
 // update of the x scale from *amax_x.
 cudaError_t launch_meta_fwd(float *dev, int idx, const float *amax_x, const float *amax_w,

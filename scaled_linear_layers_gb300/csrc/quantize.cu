@@ -211,8 +211,19 @@ struct QtJob {
     // colsum_reduce_kernel turns them into the bias gradient
     float *colsum;
 };
+// A byte transpose riding in the same launch (delayed mode): qt [C, R] =
+// q [R, C]ᵀ for e4m3 bytes that already exist, in 128 x 128 tiles after the
+// two jobs' tiles.  The step uses it to give dgrad Wqᵀ from Wq in the
+// backward launch, off the forward's critical path, with the same bytes a
+// second cast of W would give.
+struct QtBytes {
+    const uint8_t *q;
+    int R, C, tiles_x, tiles;
+    uint8_t *qt;
+};
 struct QtJobs {
     QtJob job[2];
+    QtBytes bytes;
     // optional scalar copy done by block 0 (snap_dst = *snap_src): lets a
     // step keep the scale its forward GEMM must use while a concurrent state
     // update replaces it
@@ -229,7 +240,7 @@ struct QtJobs {
 // and took 27.2 / 28.8).
 template <int kMode>
 __global__ void __launch_bounds__(256, kMode == kTensorDelayed ? 5 : 4) quantize_transpose_kernel(const QtJobs jobs) {
-    __shared__ uint32_t tile[128 * 32];
+    __shared__ __align__(16) uint32_t tile[128 * 32];
     __shared__ uint32_t red[8];
     __shared__ uint32_t colmax[8][128];
     __shared__ float col_si[128];
@@ -238,6 +249,30 @@ __global__ void __launch_bounds__(256, kMode == kTensorDelayed ? 5 : 4) quantize
     pdl_allow_next();
     if (blockIdx.x == 0 && threadIdx.x == 0 && jobs.snap_dst != nullptr)
         *jobs.snap_dst = *jobs.snap_src;
+    if (kMode == kTensorDelayed) {
+        const int cast_tiles = jobs.job[0].tiles + jobs.job[1].tiles;
+        if ((int)blockIdx.x >= cast_tiles) {
+            // byte transpose: thread t moves 16-byte chunk t%8 of rows t/8 + 32i
+            // into the shared tile's layout (chunk c of row r at word
+            // 4 * (c ^ (r / 16 % 8)), conflict-free), then the same
+            // transposed store as the cast
+            const QtBytes &B = jobs.bytes;
+            const int id = (int)blockIdx.x - cast_tiles;
+            const int r0 = (id / B.tiles_x) * 128, c0 = (id % B.tiles_x) * 128;
+            const int ch = threadIdx.x & 7, rs = threadIdx.x >> 3;
+            const int gc = c0 + 16 * ch;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = rs + 32 * i, gr = r0 + row;
+                const uint4 v = (gr < B.R && gc < B.C) ? ldg_nc_v4(B.q + (int64_t)gr * B.C + gc)
+                                                       : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(&tile[row * 32 + 4 * (ch ^ ((row >> 4) & 7))]) = v;
+            }
+            __syncthreads();
+            tile_transpose_store(tile, B.qt, B.R, B.C, r0, c0);
+            return;
+        }
+    }
 
     const bool second = (int)blockIdx.x >= jobs.job[0].tiles;
     const QtJob J = second ? jobs.job[1] : jobs.job[0];
@@ -553,7 +588,8 @@ static QtJob make_job(const uint16_t *x, int64_t rows, int64_t cols, const float
 }
 
 static cudaError_t launch_jobs(int mode, const QtJobs &jobs, cudaStream_t s) {
-    const int grid = jobs.job[0].tiles + jobs.job[1].tiles;
+    const int grid = jobs.job[0].tiles + jobs.job[1].tiles +
+                     (mode == kTensorDelayed ? jobs.bytes.tiles : 0);
     if (grid == 0) return cudaSuccess;
     switch (mode) {
     case kTensorDelayed: return launch_pdl(quantize_transpose_kernel<kTensorDelayed>, grid, 256, 0, s, jobs);
@@ -583,6 +619,7 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
     jobs.job[0].colsum = colsum;
     jobs.job[1] = jobs.job[0];
     jobs.job[1].tiles = 0;
+    jobs.bytes = QtBytes{};
     jobs.snap_src = nullptr;
     jobs.snap_dst = nullptr;
     return launch_jobs(mode, jobs, s);
@@ -590,8 +627,17 @@ cudaError_t launch_quantize_transpose(const uint16_t *x, int64_t rows, int64_t c
 
 cudaError_t launch_quantize_delayed_pair(const DelayedQuantJob &a, const DelayedQuantJob &b,
                                          cudaStream_t s, const float *snap_src,
-                                         float *snap_dst) {
+                                         float *snap_dst, const ByteTransposeJob *bt) {
     QtJobs jobs;
+    jobs.bytes = QtBytes{};
+    if (bt != nullptr && bt->rows * bt->cols > 0) {
+        jobs.bytes.q = bt->q;
+        jobs.bytes.R = (int)bt->rows;
+        jobs.bytes.C = (int)bt->cols;
+        jobs.bytes.tiles_x = (int)((bt->cols + 127) / 128);
+        jobs.bytes.tiles = jobs.bytes.tiles_x * (int)((bt->rows + 127) / 128);
+        jobs.bytes.qt = bt->qt;
+    }
     jobs.snap_src = snap_src;
     jobs.snap_dst = snap_dst;
     jobs.job[0] = make_job(a.x, a.rows, a.cols, a.scale_inv, nullptr, nullptr, a.q, a.qt, nullptr,
