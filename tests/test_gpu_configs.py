@@ -147,6 +147,9 @@ def run_delayed(M, N, K, steps, full_gemm, seed=0):
         # bytes and amaxes
         assert np.array_equal(host_u8(gpu.xq), f["xq"]), first_diff(host_u8(gpu.xq), f["xq"])
         assert np.array_equal(host_u8(gpu.wq), f["wq"])
+        # Wqᵀ (from the backward launch, as Wq's bytes transposed): the bytes
+        # the page's second quantisation of W with the same scale gives
+        assert np.array_equal(host_u8(gpu.wqt), f["wq"].T)
         assert np.array_equal(host_u8(gpu.gq), b["gq"])
         assert np.array_equal(host_u8(gpu.xqt), b["xq_bwd"].T)
         assert f32bits(gpu.ax.item()) == f32bits(f["amax_x"])
