@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(256, kMode == kTensorDelayed ? 5 : 4) quantize
 
     // amax: whole tile (tensor / tile modes), or per row and per column.
     float row_si[8];
+    uint32_t m_delayed = 0;  // this thread's |x| maximum (delayed mode)
     if (kMode == kRowCol) {
         // rows: the 16 threads sharing rsub hold one 128-element row per i
         // (a warp holds rows 2*warp + h + 16*i, h = lane/16)
@@ -422,8 +423,12 @@ __global__ void __launch_bounds__(256, kMode == kTensorDelayed ? 5 : 4) quantize
         if (kMode != kTensorDynamic) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) m = max(m, absmax_bits8_u16x2(v[i]));
-            m = block_max_u32(m, red);
+            // delayed scaling casts with a known scale: its block reduction
+            // waits until after the stores (below), so no warp holds its
+            // cast back for the other warps' loads
+            if (kMode != kTensorDelayed) m = block_max_u32(m, red);
         }
+        m_delayed = m;
         if (kMode == kTile2D) {
             if (t == 0) {
                 float s, si;
@@ -436,7 +441,8 @@ __global__ void __launch_bounds__(256, kMode == kTensorDelayed ? 5 : 4) quantize
             __syncthreads();
             si_all = tile_si;
         }
-        if (kMode != kTensorDynamic && amax_out != nullptr && t == 0 && m != 0)
+        if (kMode != kTensorDynamic && kMode != kTensorDelayed && amax_out != nullptr && t == 0 &&
+            m != 0)
             atomicMax(reinterpret_cast<unsigned int *>(amax_out), bf16bits_to_f32bits(m));
     }
 
@@ -472,6 +478,11 @@ __global__ void __launch_bounds__(256, kMode == kTensorDelayed ? 5 : 4) quantize
             const int wcol = (chunk * 2) ^ (4 * (row >> 4));
             *reinterpret_cast<uint2 *>(&tile[row * 32 + wcol]) = make_uint2(t0, t1);
         }
+    }
+    if (kMode == kTensorDelayed && amax_out != nullptr) {
+        const uint32_t m = block_max_u32(m_delayed, red);
+        if (t == 0 && m != 0)
+            atomicMax(reinterpret_cast<unsigned int *>(amax_out), bf16bits_to_f32bits(m));
     }
     if (qt == nullptr) return;  // q only: no transpose
     __syncthreads();
