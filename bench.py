@@ -259,9 +259,9 @@ class Step:
             if ev is not None:
                 self.events.append(ev)
         self.fp8.fp8_linear_step_delayed(self.meta, self.count, self.io, events=ev)
-        # kernels: 2 quantiser launches + fprop + one dgrad/wgrad launch + 2
-        # state updates (+1 refresh)
-        self.launches += 6 + (1 if self.count[0] % 16 == 0 else 0)
+        # kernels: the amax reset, 2 quantiser launches, fprop, one
+        # dgrad/wgrad launch, 2 state updates (+1 refresh every 16 steps)
+        self.launches += 7 + (1 if self.count[0] % 16 == 0 else 0)
 
 
 def kernel_times(steps_events):
