@@ -807,6 +807,8 @@ def workload_block(args, steps=None, warmup=None):
     c = synth.CONFIG5
     dev = torch.device("cuda", 0)
     M, K, N = c["M"], c["K"], c["N"]
+    if getattr(args, "block_shape", None):  # a smaller case of the same recipe (profiling)
+        M, N, K = (int(v) for v in args.block_shape.split(","))
     out = (c["p"], c["factor"])
     x = _seeded_normal(torch, (M, K), c["sigma"], 51, dev, out)
     w = _seeded_normal(torch, (N, K), c["sigma"], 52, dev, out)
@@ -843,7 +845,7 @@ def workload_block(args, steps=None, warmup=None):
     peaks = load_peaks()
     line = _gemm_line(METRIC, flop / (ms * 1e-3) / 1e12, ms, flop,
                       "block-scaled recipe (1x128 activation/gradient tiles, 128x128 weight "
-                      "tiles), M=32768, K=N=8192, 1% outliers x50, fwd+dgrad+wgrad",
+                      f"tiles), M={M}, N={N}, K={K}, 1% outliers x50, fwd+dgrad+wgrad",
                       {"M": M, "N": N, "K": K, "recipe": "block"}, peaks)
     gflop = 2.0 * M * N * K
     qbytes = 4 * M * K + 4 * N * K + 4 * M * N + 16 * (M * K + M * N) // 128 + 8 * (N * K) // (128 * 128)
@@ -1075,6 +1077,9 @@ def main():
                     choices=["linear4096", "mlp", "thd", "block", "sweep", "config1"])
     ap.add_argument("--no-workloads", action="store_true",
                     help="leave the other configurations out of the default line")
+    ap.add_argument("--block-shape", default=None, metavar="M,N,K",
+                    help="--workload block on another shape (multiples of 128), e.g. for a "
+                         "profiler capture of a small case")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
