@@ -184,11 +184,14 @@ def test_config2_delayed_full_size_first_steps():
     run_delayed(4096, 4096, 4096, steps=2, full_gemm=False)
 
 
-def test_composite_step_matches_oracle_20_steps():
+@pytest.mark.parametrize("shape", [(256, 384, 512), (272, 400, 528)])
+def test_composite_step_matches_oracle_20_steps(shape):
     """fp8_linear_step_delayed (one native call per training step) against
-    the oracle's state machine: all 20 steps at 256x384x512, full compare."""
+    the oracle's state machine: all 20 steps, full compare, at 256x384x512
+    and at a shape with partial 128-row and 128-column tiles in every
+    quantised tensor (the byte transpose that makes Wqᵀ included)."""
     c = synth.CONFIG2
-    M, N, K = 256, 384, 512
+    M, N, K = shape
     w = synth.normal_bf16((N, K), c["w_sigma"], 7, "w")
     wd = dev_bf16(w)
     step = fp8.LinearStep(M, N, K)
