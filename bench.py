@@ -5,18 +5,20 @@ TE-style delayed scaling, X ~ N(0,1) and G ~ N(0,1e-3) drawn fresh for every
 step (20 seeded sets, 1.25 GiB together, rotated so the inputs of a step are
 never L2-resident), W ~ N(0,0.02) fixed, 16-step weight amax history, X and G
 scales lagged one call.  One step = the whole hot path, one native call
-(fp8_linear_step_delayed), six kernel launches:
-    state step (refresh every 16th) ->
-    quantise X (delayed, emits amax_x) and quantise+transpose W (emits amax_w),
-    one launch -> fprop GEMM ; beside it, on the library's second stream:
-    record amax_w + lag-update the x scale ; quantise+transpose G (emits
-    amax_g) and quantise X again, transposed, with the updated x scale, one
-    launch ; lag-update the g scale -> dgrad and wgrad GEMMs in one launch.
+(fp8_linear_step_delayed), seven kernel launches:
+    state step (refresh every 16th) -> amax reset ->
+    quantise X and W (delayed, q only; emits amax_x, amax_w), one launch ->
+    fprop GEMM ; beside it, on the library's second stream: record amax_w +
+    lag-update the x scale ; quantise+transpose G (emits amax_g), quantise X
+    again, transposed, with the updated x scale, and transpose Wq's bytes into
+    Wqᵀ, one launch ; lag-update the g scale -> dgrad and wgrad GEMMs in one
+    launch.
 Metric: GEMM TFLOP/s of the whole step (3 x 2*4096^3 FLOP per step divided by
 the step time), plus per-kernel achieved TFLOP/s and GB/s (CUDA events at the
-kernel boundaries of every 10th step), the roofline of the dgrad+wgrad launch,
-an end-to-end figure with host copies, SM clocks sampled during the timed
-region, and the CPU oracle's time on a bounded sample.  On one GPU the line
+kernel boundaries of further steps run after the timed region), the roofline
+of the dgrad+wgrad launch, end-to-end figures with host copies, SM clocks
+sampled during the timed region, and the CPU oracle's time on a bounded
+sample.  On one GPU the line
 also carries `workloads`: configuration 1's latency (quantise X, W + fprop at
 64x256x256, in one launch and in three), the MLP block, the packed THD batch and the block recipe
 (whole-step TFLOP/s and each one's dominant kernel), and the quantisers at
