@@ -31,3 +31,13 @@ def test_nvml_reason_bits_are_distinct():
     bits = list(bench.NVML_REASON_BITS.values())
     assert len(set(bits)) == 4 and all(b & (b - 1) == 0 for b in bits)
     assert set(bench.NVML_REASON_BITS) == set(bench.REASON_NAMES)
+
+
+def test_roofline_traffic_comes_from_the_committed_profile():
+    """The line's roofline traffic is read from the committed ncu summary of
+    the dgrad+wgrad launch: the file must keep a parseable per-launch figure
+    of the size the step's operands and results imply (67 MB of e4m3
+    operands read and up to 67 MB of bf16 results written)."""
+    t = bench.profile_traffic("gemm_fp8_pair_dgrad_wgrad_4096.md")
+    assert t is not None and 60e6 < t < 160e6
+    assert bench.profile_traffic("no_such_profile.md") is None
