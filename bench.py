@@ -357,16 +357,21 @@ def gpu_arm(args, rank, world):
     fp8.fp8_check_device_status()
 
     # --- per-kernel segments: the same steps continued live right after the
-    # timed region, with CUDA events at every kernel boundary of each step
+    # timed region, as many again, with CUDA events at every kernel boundary
+    # of every event_every-th step (the others run as the timed ones do, so
+    # the event steps see the loop's steady power state)
     segs = None
     n_ev = 0
     if not args.no_kernel_events:
-        n_ev = max(20, args.steps // max(1, args.event_every))
-        step.prepare_events(n_ev, 1)
+        every = max(1, args.event_every)
+        n_seg = max(args.steps, 20 * every)
+        step.prepare_events(n_seg, every)
         torch.cuda.synchronize()
-        for t in range(args.warmup + args.steps, args.warmup + args.steps + n_ev):
+        t0 = args.warmup + args.steps
+        for t in range(t0, t0 + n_seg):
             step.run(t)
         torch.cuda.synchronize()
+        n_ev = len(step.events)
         segs = kernel_times(step.events)
         step.events = None
         fp8.fp8_check_device_status()
@@ -501,9 +506,9 @@ def gpu_arm(args, rank, world):
                              "result_read": "Y, dX and dW in full"},
         "gpu_launches": launches,
         "kernel_timing": None if segs is None else
-        f"CUDA events at the kernel boundaries of {n_ev} steps run right after the timed region "
-        "(an event between two kernels stops their programmatic overlap, so these steps are "
-        "not part of the timed region)",
+        f"CUDA events at the kernel boundaries of {n_ev} steps (every {max(1, args.event_every)}-th "
+        "of a second loop run right after the timed region; an event between two kernels stops "
+        "their programmatic overlap, so these steps are not part of the timed region)",
         "clocks": clocks,
     }
     return line
@@ -1091,9 +1096,10 @@ def main():
     ap.add_argument("--no-kernel-events", action="store_true",
                     help="time the step without per-kernel events (no per-kernel breakdown)")
     ap.add_argument("--event-every", type=int, default=10,
-                    help="the per-kernel segments come from max(20, steps / n) further steps "
-                         "with events at every kernel boundary, run after the timed region: an "
-                         "event between two kernels stops the second from overlapping the first")
+                    help="the per-kernel segments come from every n-th step of a second loop "
+                         "(as long as the timed one, at least 20 n steps) run after the timed "
+                         "region, with events at every kernel boundary: an event between two "
+                         "kernels stops the second from overlapping the first")
     ap.add_argument("--workload", default="linear4096",
                     choices=["linear4096", "mlp", "thd", "block", "sweep", "config1"])
     ap.add_argument("--no-workloads", action="store_true",
