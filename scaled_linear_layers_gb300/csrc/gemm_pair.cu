@@ -339,10 +339,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 if (col >= pN) continue;  // warp-uniform; rows past M are clipped by the copy
                 uint32_t packed[16];
                 if (bias != nullptr) {
+                    // N is a multiple of 16: a last chunk may hold only 16
+                    // columns, whose upper half is neither read nor stored
+                    const int jn = col + 16 < pN ? 16 : 8;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float b0 = __uint_as_float((uint32_t)bias[col + 2 * j] << 16);
-                        const float b1 = __uint_as_float((uint32_t)bias[col + 2 * j + 1] << 16);
+                        const float b0 =
+                            j < jn ? __uint_as_float((uint32_t)bias[col + 2 * j] << 16) : 0.f;
+                        const float b1 =
+                            j < jn ? __uint_as_float((uint32_t)bias[col + 2 * j + 1] << 16) : 0.f;
                         packed[j] =
                             pack_bf16x2(__fadd_rn(__fmul_rn(__uint_as_float(r[2 * j]), s), b0),
                                         __fadd_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), s), b1));

@@ -97,12 +97,15 @@ def test_gemm_pair_kernel_every_tile_width(bn, which, monkeypatch):
         assert ok.all(), f"pair BN={bn} {(M, N, K)}: {(~ok).sum()} bad"
 
 
-def test_gemm_pair_kernel_bias(monkeypatch):
+@pytest.mark.parametrize("n", [384, 400])
+def test_gemm_pair_kernel_bias(n, monkeypatch):
+    """Bias in the 2-SM kernel's epilogue; N = 400 ends in a 16-column chunk,
+    whose upper half (past the bias array) is neither read nor stored."""
     monkeypatch.setenv("FP8LINEAR_GEMM_PAIR", "1")
     rng = np.random.default_rng(3)
     A = random_codes(rng, (512, 512))
-    B = random_codes(rng, (384, 512))
-    bias = synth.normal_bf16((384,), 1.0, seed=4, tensor="bias")
+    B = random_codes(rng, (n, 512))
+    bias = synth.normal_bf16((n,), 1.0, seed=4, tensor="bias")
     got = run_tensor_gemm(A, B, 0.01, 0.02, bias=bias)
     _, ref, bound = oracle.gemm(A, B, np.float32(0.01), np.float32(0.02), bias)
     assert oracle.gemm_tolerance_ok(got, ref, bound).all()
@@ -123,11 +126,15 @@ def test_gemm_exact_on_integer_operands():
     assert np.array_equal(got, ref)
 
 
-def test_gemm_bias():
+@pytest.mark.parametrize("n", [384, 400])
+def test_gemm_bias(n, monkeypatch):
+    """Bias in the one-CTA kernel's epilogue (N = 400: a last chunk of 16
+    columns)."""
+    monkeypatch.setenv("FP8LINEAR_GEMM_PAIR", "0")
     rng = np.random.default_rng(3)
     A = random_codes(rng, (256, 512))
-    B = random_codes(rng, (384, 512))
-    bias = synth.normal_bf16((384,), 1.0, seed=3, tensor="bias")
+    B = random_codes(rng, (n, 512))
+    bias = synth.normal_bf16((n,), 1.0, seed=3, tensor="bias")
     got = run_tensor_gemm(A, B, 0.01, 0.02, bias=bias)
     _, ref, bound = oracle.gemm(A, B, np.float32(0.01), np.float32(0.02), bias)
     assert oracle.gemm_tolerance_ok(got, ref, bound).all()
